@@ -1,0 +1,152 @@
+/*
+ * bitnet.h -- C ABI of the GB300 (sm_103a) W2A8 ternary matmul library (libbitnet_gb300.so).
+ *
+ * The library computes the BitNet b1.58 linear layer with ternary weights stored as 2-bit
+ * codes in the i2_s layout and per-token absmax int8 activations:
+ *
+ *   out[m][n] = ( sum_k (code[n][k] - 1) * xq[m][k] ) / s[m] * w_scale
+ *
+ * where code in {0,1,2} encodes w in {-1,0,+1}. The integer sum is formed as the raw code
+ * dot sum_k code*xq minus the activation row sum sum_k xq (an identity), which is how the
+ * packed CPU kernels of bitnet.cpp compute it.
+ *
+ * Sources (by page title and section):
+ *   [DeepDive]  "BitNet 딥다이브 -- 작은 숫자를 빠른 연산으로 바꾸는 추론 엔진", §1-1 (code map),
+ *               §4-2 (i2_s packing, quantize_i2_s), §4-5 (GPU path, per-token quant_input)
+ *   [Scalar]    "[분석/검증-3] BitNet.cpp ARM 커널 재작성 : 스칼라 폴백구현을 통한 최종 검증",
+ *               §3 (scalar i2_s x int8 dot, row stride, 4x32 interleave)
+ *   [Report]    "[기술 분석 보고서] ARM64 모바일 환경에서의 1.58-bit 양자화 모델 추론 붕괴 원인 분석
+ *               및 C++ 커널 역공학을 통한 해결", §3.1 (interleave), §3.2 (codes multiplied as stored)
+ *   [bitnet.rs] "bitnet.rs -- BitNet b1.58 Inference Engine in Rust", "Mathematical Foundation"
+ *               (AbsMean weight scale, AbsMax activation quantisation, quantised forward pass)
+ *
+ * Common rules for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library keeps no
+ *     pointer after the call returns and allocates no device memory.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream). Results are valid once the stream has reached the call.
+ *   - Arguments are validated on the host before anything is launched; an invalid call
+ *     launches nothing and returns a negative status. No exception crosses the ABI.
+ *   - Layouts are dense row-major. K (the reduction length) must be a positive multiple of
+ *     128 (one i2_s block) wherever packed weights are involved.
+ *   - Each call runs on the device that is current on the calling thread; that device must
+ *     be an sm_103 GPU (GB300), else BITNET_EUNSUPPORTED.
+ *   - Inputs must be finite; NaN/Inf activations are outside the contract.
+ */
+#ifndef BITNET_GB300_H
+#define BITNET_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BITNET_API __attribute__((visibility("default")))
+#else
+#define BITNET_API
+#endif
+
+/* ---- status codes ---- */
+#define BITNET_OK 0
+#define BITNET_EINVAL (-1)        /* null pointer, size <= 0 or out of range, K % 128 != 0, bad enum */
+#define BITNET_EALIGN (-2)        /* a pointer is not aligned as the entry point requires        */
+#define BITNET_ECUDA (-3)         /* a CUDA runtime call or kernel launch failed                  */
+#define BITNET_EUNSUPPORTED (-4)  /* current device is not sm_103, or no device                 */
+#define BITNET_ETIMEOUT (-5)      /* a device-side bounded wait gave up (reported by the next call
+                                     to bitnet_last_device_error); the result is not valid      */
+
+/* ---- activation dtypes (bitnet_quant_act) ---- */
+#define BITNET_F32 0
+#define BITNET_BF16 1
+
+/* ---- matmul kernel selection (bitnet_i2s_matmul_algo) ---- */
+#define BITNET_ALGO_AUTO 0   /* decode GEMV for M <= 64, tensor-core GEMM otherwise */
+#define BITNET_ALGO_GEMV 1   /* force the dp4a decode GEMV (any M)                   */
+#define BITNET_ALGO_GEMM 2   /* force the tcgen05 tensor-core GEMM (any M)           */
+
+/* Library ABI version (major*100 + minor). */
+BITNET_API int bitnet_version(void);
+
+/* Human-readable text for a status code. Never NULL; static storage. */
+BITNET_API const char *bitnet_strerror(int status);
+
+/*
+ * bitnet_pack_i2s -- ternary int8 weights -> i2_s packed bytes.
+ *   [DeepDive] §4-2 (quantize_i2_s, x86 ACT_PARALLEL branch) and §1-1 (code map).
+ *
+ *   w             : N x K int8, values in {-1, 0, +1}                      (device, read)
+ *   wp            : N x K/4 uint8                                           (device, written)
+ *                   Byte (n, 32*i + g) holds, at bit pairs 7:6, 5:4, 3:2, 1:0, the codes of
+ *                   weights (n, 128*i + g), (n, 128*i + 32 + g), (n, 128*i + 64 + g),
+ *                   (n, 128*i + 96 + g); code = w + 1.
+ *   N, K          : N >= 1, K >= 128, K % 128 == 0, K <= 65536
+ *   invalid_count : optional (may be NULL) device int32; set to the number of entries of w
+ *                   outside {-1,0,+1}. Such entries are packed by sign (>0 -> 2, <0 -> 0).
+ *   w and wp must be 16-byte aligned (BITNET_EALIGN otherwise).
+ */
+BITNET_API int bitnet_pack_i2s(const int8_t *w, uint8_t *wp, int64_t N, int64_t K,
+                               int32_t *invalid_count, void *stream);
+
+/*
+ * bitnet_quant_act -- per-token absmax int8 quantisation of activation rows.
+ *   [DeepDive] §4-5 (BitLinearKernel.quant_input: s = 127 / max(max|x|, 1e-5), round,
+ *   clamp, int8); [bitnet.rs] "8-bit Activation Quantisation (AbsMax, per-token)".
+ *
+ *   x          : M x K, fp32 (dtype BITNET_F32) or bf16 (BITNET_BF16)       (device, read)
+ *                bf16 is widened to fp32 exactly before any arithmetic.
+ *   xq         : M x K int8, q = clamp(rne(x * s), -127, 127)              (device, written)
+ *   act_scale  : M fp32, s = 127 / max(max_k |x|, 1e-5) (IEEE fp32 divide) (device, written)
+ *   rowsum     : M int32, sum_k xq[m][k]                                    (device, written)
+ *   M >= 1, K >= 128, K % 128 == 0, K <= 65536. x and xq must be 16-byte aligned.
+ */
+BITNET_API int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *xq,
+                                float *act_scale, int32_t *rowsum, void *stream);
+
+/*
+ * bitnet_i2s_matmul -- W2A8 ternary matmul with the -sum(y) correction and the scales.
+ *   [Scalar] §3 and [Report] §3.2/§4 (raw code dot over the 4x32-interleaved bytes, codes
+ *   multiplied as stored); the zero-point correction acc = raw - rowsum is exact; the
+ *   dequantisation follows [bitnet.rs] "Quantised Forward Pass" read as
+ *   out = acc * alpha_W * alpha_x with alpha_x = 1/s.
+ *
+ *   xq        : M x K int8 activations                                      (device, read)
+ *   act_scale : M fp32 activation scales s                                   (device, read)
+ *   rowsum    : M int32, sum_k xq[m][k] (as written by bitnet_quant_act)     (device, read)
+ *   wp        : N x K/4 uint8, i2_s packed weights                           (device, read)
+ *   w_scale   : per-tensor weight scale alpha_W = mean|W| of the source weights
+ *   out       : M x N fp32, out[m][n] = ((float)acc[m][n] / s[m]) * w_scale  (device, written)
+ *   acc_out   : optional (may be NULL) M x N int32, acc[m][n] = sum_k (code-1)*xq (written)
+ *   M, N >= 1; M, N <= 2^31 - 1; K >= 128, K % 128 == 0, K <= 65536. The tensor-core GEMM
+ *   takes K <= 32768 (BITNET_EINVAL if forced beyond); auto dispatch then uses the GEMV.
+ *   xq and wp must be 16-byte aligned; out and acc_out 4-byte aligned.
+ *   The 2-bit field value 3 never comes out of bitnet_pack_i2s; if present it is used
+ *   arithmetically (3 - 1 = +2), the same rule as the unpacking of [DeepDive] §8.
+ *   For M <= 64 a dp4a GEMV streams the packed weights; for larger M a tcgen05 tensor-core
+ *   GEMM expands the codes in shared memory (exact: every partial sum is an integer
+ *   below 2^24 accumulated in fp32). Both give bit-identical results.
+ */
+BITNET_API int bitnet_i2s_matmul(const int8_t *xq, const float *act_scale, const int32_t *rowsum,
+                                 const uint8_t *wp, float w_scale, float *out, int32_t *acc_out,
+                                 int64_t M, int64_t N, int64_t K, void *stream);
+
+/* Same as bitnet_i2s_matmul with an explicit kernel choice (BITNET_ALGO_*). */
+BITNET_API int bitnet_i2s_matmul_algo(const int8_t *xq, const float *act_scale,
+                                      const int32_t *rowsum, const uint8_t *wp, float w_scale,
+                                      float *out, int32_t *acc_out, int64_t M, int64_t N,
+                                      int64_t K, int algo, void *stream);
+
+/*
+ * bitnet_last_device_error -- read and clear the device-side error word of the current
+ * device. Kernels that wait on an mbarrier give up after a bounded number of polls and
+ * record BITNET_ETIMEOUT there instead of hanging. Synchronises the device.
+ * Returns BITNET_OK, BITNET_ETIMEOUT or BITNET_ECUDA.
+ */
+BITNET_API int bitnet_last_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITNET_GB300_H */

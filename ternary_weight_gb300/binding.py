@@ -1,0 +1,154 @@
+"""ctypes binding of libbitnet_gb300 (the C ABI in include/bitnet.h).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels. Tensors are torch CUDA tensors (torch supplies device memory and streams); the
+functions pass their data pointers and the current stream to the C entry points and raise
+``BitnetError`` on a negative status. There is no CPU fallback: if the shared library is
+missing or fails to load, ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+BITNET_OK = 0
+BITNET_EINVAL = -1
+BITNET_EALIGN = -2
+BITNET_ECUDA = -3
+BITNET_EUNSUPPORTED = -4
+BITNET_ETIMEOUT = -5
+
+BITNET_F32 = 0
+BITNET_BF16 = 1
+
+ALGO = {"auto": 0, "gemv": 1, "gemm": 2}
+
+# every entry point of include/bitnet.h with its ctypes signature
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+SIGNATURES = {
+    "bitnet_version": ([], ctypes.c_int),
+    "bitnet_strerror": ([ctypes.c_int], ctypes.c_char_p),
+    "bitnet_pack_i2s": ([_P, _P, _I64, _I64, _P, _P], ctypes.c_int),
+    "bitnet_quant_act": ([_P, ctypes.c_int, _I64, _I64, _P, _P, _P, _P], ctypes.c_int),
+    "bitnet_i2s_matmul": ([_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
+    "bitnet_i2s_matmul_algo": (
+        [_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
+    "bitnet_last_device_error": ([], ctypes.c_int),
+}
+
+_lib = None
+
+
+class BitnetError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib().bitnet_strerror(status).decode() if _lib is not None else str(status)
+        super().__init__("%s failed with status %d: %s" % (where, status, msg))
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load the CUDA library (built in-tree by ``_build.build()``); raise if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "libbitnet_gb300.so is not built (%s); run ternary_weight_gb300._build.build() "
+            "or __graft_entry__.build() first -- there is no CPU fallback" % path)
+    l = ctypes.CDLL(path)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(l, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = l
+    return l
+
+
+def _check(status: int, where: str):
+    if status != BITNET_OK:
+        raise BitnetError(status, where)
+
+
+def _stream(stream=None):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def pack_i2s(w, out=None, invalid_count=None, stream=None):
+    """Ternary int8 weights (N x K, CUDA) -> i2_s packed uint8 (N x K/4)."""
+    import torch
+
+    N, K = w.shape
+    if out is None:
+        out = torch.empty((N, K // 4), dtype=torch.uint8, device=w.device)
+    _require_cuda(w, out, invalid_count)
+    _check(lib().bitnet_pack_i2s(_ptr(w), _ptr(out), N, K, _ptr(invalid_count), _stream(stream)),
+           "bitnet_pack_i2s")
+    return out
+
+
+def quant_act(x, xq=None, scale=None, rowsum=None, stream=None):
+    """fp32 or bf16 rows (M x K, CUDA) -> (xq int8 M x K, s fp32 M, rowsum int32 M)."""
+    import torch
+
+    if x.dtype == torch.float32:
+        dt = BITNET_F32
+    elif x.dtype == torch.bfloat16:
+        dt = BITNET_BF16
+    else:
+        raise ValueError("x must be float32 or bfloat16")
+    M, K = x.shape
+    dev = x.device
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev) if xq is None else xq
+    scale = torch.empty(M, dtype=torch.float32, device=dev) if scale is None else scale
+    rowsum = torch.empty(M, dtype=torch.int32, device=dev) if rowsum is None else rowsum
+    _require_cuda(x, xq, scale, rowsum)
+    _check(lib().bitnet_quant_act(_ptr(x), dt, M, K, _ptr(xq), _ptr(scale), _ptr(rowsum), _stream(stream)),
+           "bitnet_quant_act")
+    return xq, scale, rowsum
+
+
+def i2s_matmul(xq, scale, rowsum, wp, w_scale, out=None, acc_out=None, algo="auto", stream=None):
+    """W2A8 ternary matmul: returns out (M x N fp32); fills acc_out (M x N int32) if given."""
+    import torch
+
+    M, K = xq.shape
+    N = wp.shape[0]
+    if wp.shape[1] * 4 != K:
+        raise ValueError("wp must be N x K/4")
+    out = torch.empty((M, N), dtype=torch.float32, device=xq.device) if out is None else out
+    _require_cuda(xq, scale, rowsum, wp, out, acc_out)
+    _check(lib().bitnet_i2s_matmul_algo(_ptr(xq), _ptr(scale), _ptr(rowsum), _ptr(wp), float(w_scale),
+                                        _ptr(out), _ptr(acc_out), M, N, K, ALGO[algo], _stream(stream)),
+           "bitnet_i2s_matmul")
+    return out
+
+
+def last_device_error() -> int:
+    return lib().bitnet_last_device_error()
+
+
+def linear(x, wp, w_scale, out=None, algo="auto", stream=None):
+    """Quantise activation rows and multiply them with packed ternary weights (two launches)."""
+    xq, s, rs = quant_act(x, stream=stream)
+    return i2s_matmul(xq, s, rs, wp, w_scale, out=out, algo=algo, stream=stream)

@@ -1,0 +1,132 @@
+// capi.cu -- the extern "C" boundary of libbitnet_gb300 (declared in include/bitnet.h).
+//
+// Every entry point validates its arguments on the host before anything is launched and
+// returns a status code; no C++ exception crosses the ABI. The library holds no device
+// allocation: the only device-side state is one error word written by bounded waits.
+#include "bitnet.h"
+#include "bitnet_dev.cuh"
+
+#include <atomic>
+#include <cstdint>
+
+namespace bitnet {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxK = 1 << 16;          // staged activation rows must fit shared memory
+constexpr int64_t kMaxKTensorCore = 1 << 15; // exact fp32 accumulation bound of the GEMM
+constexpr int64_t kGemvMaxM = 64;           // auto dispatch: GEMV up to here, GEMM above
+
+// per-device: 0 = unchecked, 1 = sm_103 ok, -1 = unsupported; and SM count
+std::atomic<int> g_dev_state[kMaxDevices];
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+int check_device(int* num_sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return BITNET_EUNSUPPORTED;
+  }
+  int st = g_dev_state[dev].load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return BITNET_EUNSUPPORTED;
+    }
+    st = (major == 10 && minor == 3) ? 1 : -1;
+    g_dev_sms[dev].store(sms, std::memory_order_relaxed);
+    g_dev_state[dev].store(st, std::memory_order_release);
+  }
+  if (st != 1) return BITNET_EUNSUPPORTED;
+  if (num_sms) *num_sms = g_dev_sms[dev].load(std::memory_order_relaxed);
+  return BITNET_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? BITNET_OK : BITNET_ECUDA; }
+
+bool valid_k(int64_t K) { return K >= 128 && K % 128 == 0 && K <= kMaxK; }
+
+}  // namespace
+}  // namespace bitnet
+
+using namespace bitnet;
+
+extern "C" {
+
+BITNET_API int bitnet_version(void) { return 100; }
+
+BITNET_API const char* bitnet_strerror(int status) {
+  switch (status) {
+    case BITNET_OK: return "ok";
+    case BITNET_EINVAL: return "invalid argument (null pointer, size out of range, K not a multiple of 128, bad enum)";
+    case BITNET_EALIGN: return "misaligned pointer (16-byte alignment required)";
+    case BITNET_ECUDA: return "CUDA runtime error or kernel launch failure";
+    case BITNET_EUNSUPPORTED: return "unsupported device (an sm_103 / GB300 GPU is required)";
+    case BITNET_ETIMEOUT: return "a device-side bounded wait timed out; results are invalid";
+    default: return "unknown status";
+  }
+}
+
+BITNET_API int bitnet_pack_i2s(const int8_t* w, uint8_t* wp, int64_t N, int64_t K, int32_t* invalid_count,
+                               void* stream) {
+  if (!w || !wp || N < 1 || N > INT32_MAX || !valid_k(K)) return BITNET_EINVAL;
+  if (!aligned(w, 16) || !aligned(wp, 16) || (invalid_count && !aligned(invalid_count, 4))) return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  return status_of(launch_pack_i2s(w, wp, N, K, invalid_count, static_cast<cudaStream_t>(stream)));
+}
+
+BITNET_API int bitnet_quant_act(const void* x, int dtype, int64_t M, int64_t K, int8_t* xq, float* act_scale,
+                                int32_t* rowsum, void* stream) {
+  if (!x || !xq || !act_scale || !rowsum) return BITNET_EINVAL;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_EINVAL;
+  if (M < 1 || M > INT32_MAX || !valid_k(K)) return BITNET_EINVAL;
+  if (!aligned(x, 16) || !aligned(xq, 16) || !aligned(act_scale, 4) || !aligned(rowsum, 4)) return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  return status_of(launch_quant_act(x, dtype, M, K, xq, act_scale, rowsum, static_cast<cudaStream_t>(stream)));
+}
+
+BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, const int32_t* rowsum,
+                                      const uint8_t* wp, float w_scale, float* out, int32_t* acc_out, int64_t M,
+                                      int64_t N, int64_t K, int algo, void* stream) {
+  if (!xq || !act_scale || !rowsum || !wp || !out) return BITNET_EINVAL;
+  if (M < 1 || M > INT32_MAX || N < 1 || N > INT32_MAX || !valid_k(K)) return BITNET_EINVAL;
+  if (algo < BITNET_ALGO_AUTO || algo > BITNET_ALGO_GEMM) return BITNET_EINVAL;
+  if (!aligned(xq, 16) || !aligned(wp, 16) || !aligned(act_scale, 4) || !aligned(rowsum, 4) || !aligned(out, 4) ||
+      (acc_out && !aligned(acc_out, 4)))
+    return BITNET_EALIGN;
+  if (algo == BITNET_ALGO_AUTO) algo = (M <= kGemvMaxM || K > kMaxKTensorCore) ? BITNET_ALGO_GEMV : BITNET_ALGO_GEMM;
+  if (algo == BITNET_ALGO_GEMM && (K > kMaxKTensorCore || M > 65535LL * 128)) return BITNET_EINVAL;
+  if (algo == BITNET_ALGO_GEMV && M > 65535LL * 8) return BITNET_EINVAL;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (algo == BITNET_ALGO_GEMV)
+                      ? launch_gemv_i2s(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s)
+                      : launch_gemm_i2s_tc(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
+  return status_of(e);
+}
+
+BITNET_API int bitnet_i2s_matmul(const int8_t* xq, const float* act_scale, const int32_t* rowsum,
+                                 const uint8_t* wp, float w_scale, float* out, int32_t* acc_out, int64_t M,
+                                 int64_t N, int64_t K, void* stream) {
+  return bitnet_i2s_matmul_algo(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, BITNET_ALGO_AUTO,
+                                stream);
+}
+
+BITNET_API int bitnet_last_device_error(void) {
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return BITNET_ECUDA;
+  int v = 0;
+  if (read_clear_device_error_gemm(&v) != cudaSuccess) return BITNET_ECUDA;
+  return v == 0 ? BITNET_OK : v;
+}
+
+}  // extern "C"

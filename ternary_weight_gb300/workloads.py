@@ -175,3 +175,16 @@ def decode_sweep_specs(n_layers: int = N_LAYERS) -> List[DecodeLayerSpec]:
 def decode_sweep_weight_bytes(n_layers: int = N_LAYERS) -> int:
     """Packed i2_s bytes of the sweep (2 bits per weight)."""
     return n_layers * sum(N * K // 4 for _, N, K in LAYER_MATRICES)
+
+
+def random_packed_bytes(N: int, K: int, seed: int) -> np.ndarray:
+    """N x K/4 uniformly random bytes: every 2-bit field, the unused code 3 included, with
+    probability 1/4 each. Used for adversarial parity cases (the layout is irrelevant to it)."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+
+
+def random_int8(M: int, K: int, seed: int, lo: int = -127, hi: int = 127) -> np.ndarray:
+    """M x K uniformly random int8 in [lo, hi]."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi + 1, size=(M, K), dtype=np.int16).astype(np.int8)

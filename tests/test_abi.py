@@ -1,0 +1,112 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry point that
+include/bitnet.h declares, and rejects bad arguments on the host before any CUDA call.
+No kernel is launched here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from ternary_weight_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.lib()
+
+
+def declared_entry_points():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"BITNET_API\s+[\w\s\*]+?\b(bitnet_\w+)\s*\(", src)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for required in ("bitnet_pack_i2s", "bitnet_quant_act", "bitnet_i2s_matmul"):
+        assert required in names
+    assert set(names) == set(binding.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_entry_points():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    # nothing but the C ABI is exported
+    assert {e for e in exported if e.startswith("bitnet")} == set(declared_entry_points())
+
+
+def test_version_and_strerror(lib):
+    assert lib.bitnet_version() >= 100
+    for st in (0, -1, -2, -3, -4, -5, -99):
+        assert isinstance(lib.bitnet_strerror(st), bytes) and lib.bitnet_strerror(st)
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null pointer value; never dereferenced: validation fails first
+
+
+def _mm(lib, xq=FAKE, s=FAKE, rs=FAKE, wp=FAKE, out=FAKE, acc=None, M=1, N=1, K=128, algo=0):
+    return lib.bitnet_i2s_matmul_algo(xq, s, rs, wp, 1.0, out, acc, M, N, K, algo, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(xq=None), -1), (dict(s=None), -1), (dict(rs=None), -1), (dict(wp=None), -1), (dict(out=None), -1),
+    (dict(K=100), -1), (dict(K=0), -1), (dict(K=-128), -1), (dict(K=128 * 513 * 2), -1),
+    (dict(M=0), -1), (dict(N=0), -1), (dict(M=-5), -1), (dict(N=1 << 31), -1),
+    (dict(algo=3), -1), (dict(algo=-1), -1), (dict(algo=2, K=65536), -1),
+    (dict(xq=FAKE + 8), -2), (dict(wp=FAKE + 4), -2), (dict(out=FAKE + 2), -2), (dict(acc=FAKE + 1), -2),
+    (dict(s=FAKE + 1), -2), (dict(rs=FAKE + 2), -2),
+])
+def test_matmul_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _mm(lib, **kw) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, 0, 1, 128, FAKE, FAKE, FAKE), -1),
+    ((FAKE, 2, 1, 128, FAKE, FAKE, FAKE), -1),
+    ((FAKE, 0, 0, 128, FAKE, FAKE, FAKE), -1),
+    ((FAKE, 0, 1, 130, FAKE, FAKE, FAKE), -1),
+    ((FAKE + 4, 0, 1, 128, FAKE, FAKE, FAKE), -2),
+    ((FAKE, 1, 1, 128, FAKE + 8, FAKE, FAKE), -2),
+])
+def test_quant_act_rejects_bad_arguments_on_host(lib, args, status):
+    assert lib.bitnet_quant_act(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, FAKE, 1, 128, None), -1),
+    ((FAKE, None, 1, 128, None), -1),
+    ((FAKE, FAKE, 0, 128, None), -1),
+    ((FAKE, FAKE, 1, 64, None), -1),
+    ((FAKE + 1, FAKE, 1, 128, None), -2),
+    ((FAKE, FAKE + 8, 1, 128, None), -2),
+    ((FAKE, FAKE, 1, 128, FAKE + 2), -2),
+])
+def test_pack_rejects_bad_arguments_on_host(lib, args, status):
+    assert lib.bitnet_pack_i2s(*args, None) == status
+
+
+def test_valid_call_without_gpu_is_unsupported(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the gpu tests")
+    assert _mm(lib) == -4
+    assert lib.bitnet_last_device_error() == -4
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.lib()

@@ -1,0 +1,251 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle, element by element.
+
+Integers (packed bytes, xq, rowsum, acc) must match bit for bit; the fp32 scale s must match
+bit for bit (both sides do one IEEE divide); fp32 outputs must agree within 1e-5 relative
+(they are in fact produced by the same IEEE operations in the same order, and the tests
+also count exact matches). Inputs come from ternary_weight_gb300.workloads; expected values
+come only from oracle/.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ternary_weight_gb300 import _build, binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 1e-5
+NT = oracle.default_threads()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.fail("gpu tests need a CUDA device")
+    _build.build()
+    binding.lib()
+    yield
+    assert binding.last_device_error() == 0, "a kernel recorded a device-side error"
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def x_device(x_np, dtype):
+    if dtype == "f32":
+        return dev(x_np)
+    return dev(x_np.view(np.int16)).view(torch.bfloat16)
+
+
+def assert_out_close(out_gpu, out_ref):
+    assert out_gpu.shape == out_ref.shape
+    ref = out_ref.astype(np.float64)
+    got = out_gpu.astype(np.float64)
+    err = np.abs(got - ref)
+    bound = REL_TOL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), "fp32 outputs off by more than 1e-5 rel at %d places, max rel %.3g" % (
+        bad.sum(), (err / np.maximum(np.abs(ref), 1e-30)).max())
+
+
+def run_chain(x_np, dtype, w_np, w_scale, algo="auto"):
+    """GPU: pack -> quant -> matmul. Oracle: the same on the CPU. Returns both."""
+    g_wp = binding.pack_i2s(dev(w_np))
+    g_xq, g_s, g_rs = binding.quant_act(x_device(x_np, dtype))
+    M, N = x_np.shape[0], w_np.shape[0]
+    g_acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    g_out = binding.i2s_matmul(g_xq, g_s, g_rs, g_wp, w_scale, acc_out=g_acc, algo=algo)
+    torch.cuda.synchronize()
+    o_wp, _ = oracle.pack_i2s(w_np)
+    o_xq, o_s, o_rs = oracle.quant_act(x_np, dtype)
+    o_out, o_acc = oracle.ternary_matmul(o_xq, o_s, o_wp, w_scale, nthreads=NT)
+    return (dict(wp=host(g_wp), xq=host(g_xq), s=host(g_s), rs=host(g_rs), acc=host(g_acc), out=host(g_out)),
+            dict(wp=o_wp, xq=o_xq, s=o_s, rs=o_rs, acc=o_acc, out=o_out))
+
+
+def assert_chain_equal(g, o):
+    assert np.array_equal(g["wp"], o["wp"]), "packed bytes differ"
+    assert np.array_equal(g["xq"], o["xq"]), "xq differs"
+    assert np.array_equal(g["s"].view(np.uint32), o["s"].view(np.uint32)), "scale differs"
+    assert np.array_equal(g["rs"], o["rs"]), "rowsum differs"
+    assert np.array_equal(g["acc"], o["acc"]), "int32 accumulators differ"
+    assert_out_close(g["out"], o["out"])
+    assert np.array_equal(g["out"].view(np.uint32), o["out"].view(np.uint32)), "fp32 out not bit-identical"
+
+
+# ----------------------------------------------------------------------------- pack
+
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 384), (640, 2560), (33, 6912), (5, 8192)])
+def test_pack_parity(N, K):
+    w = workloads.ternary_weights(N, K, seed=100 + N)
+    assert np.array_equal(host(binding.pack_i2s(dev(w))), oracle.pack_i2s(w)[0])
+
+
+def test_pack_non_ternary_count():
+    w = workloads.ternary_weights(9, 256, seed=101)
+    w[0, 5], w[3, 200], w[8, 255], w[2, 0] = 5, -7, 127, -128
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = binding.pack_i2s(dev(w), invalid_count=cnt)
+    o, bad = oracle.pack_i2s(w)
+    assert np.array_equal(host(g), o) and int(cnt.item()) == bad == 4
+
+
+# ----------------------------------------------------------------------------- quant
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,K,outlier", [(1, 128, 0.0), (1, 2560, 0.0), (3, 6912, 0.01), (64, 2560, 0.01),
+                                         (129, 384, 0.0), (2, 8192, 0.0), (4, 16384, 0.01), (2, 65536, 0.0)])
+def test_quant_parity(dtype, M, K, outlier):
+    x = workloads.activations(M, K, seed=200 + M + K, dtype=dtype, outlier_p=outlier)
+    g = [host(t) for t in binding.quant_act(x_device(x, dtype))]
+    o = oracle.quant_act(x, dtype)
+    assert np.array_equal(g[0], o[0])
+    assert np.array_equal(g[1].view(np.uint32), o[1].view(np.uint32))
+    assert np.array_equal(g[2], o[2])
+
+
+def test_quant_edge_rows():
+    K = 256
+    x = np.zeros((6, K), np.float32)
+    x[1, 7] = 3e-6                          # below the 1e-5 floor
+    x[2, :] = 1.0                           # constant row -> all 127
+    x[3, :] = -2.5e30                       # huge values
+    x[4, ::2], x[4, 1::2] = 127.0, -0.5     # s = 1 exactly: ties at -0.5 -> 0 (even)
+    amax = np.array([1090775969], np.uint32).view(np.float32)[0]  # near-tie row (multiply form)
+    s = np.float32(np.float32(127.0) / amax)
+    x[5, 0] = amax
+    x[5, 1:120] = [np.float32((k + 0.5) / float(s)) for k in range(1, 120)]
+    g = [host(t) for t in binding.quant_act(dev(x))]
+    o = oracle.quant_act(x)
+    for a, b in zip(g, o):
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                              b.view(np.uint32) if b.dtype == np.float32 else b)
+
+
+# ----------------------------------------------------------------------------- matmul (full chain)
+
+SMALL_CHAIN = [
+    # (M, N, K, dtype) -- several tiles and ragged tails, oracle finishes in seconds
+    (1, 1, 128, "f32"), (1, 7, 384, "f32"), (1, 2560, 2560, "f32"), (1, 640, 2560, "f32"),
+    (1, 2561, 6912, "bf16"), (2, 300, 8192, "bf16"), (3, 257, 2560, "bf16"), (4, 1000, 6912, "bf16"),
+    (7, 129, 1024, "f32"), (16, 700, 2560, "bf16"), (63, 300, 6912, "bf16"), (64, 513, 2560, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype", SMALL_CHAIN)
+def test_chain_parity_gemv(M, N, K, dtype):
+    x = workloads.activations(M, K, seed=300 + M, dtype=dtype, outlier_p=0.01)
+    w = workloads.ternary_weights(N, K, seed=301 + N)
+    g, o = run_chain(x, dtype, w, workloads.weight_scale(N, K, 302), algo="gemv")
+    assert_chain_equal(g, o)
+
+
+GEMM_CHAIN = [
+    (1, 256, 128, "f32"), (65, 300, 2560, "bf16"), (127, 257, 384, "bf16"), (128, 256, 2560, "bf16"),
+    (129, 513, 1024, "f32"), (200, 1000, 6912, "bf16"), (300, 700, 2560, "bf16"), (256, 640, 8192, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype", GEMM_CHAIN)
+def test_chain_parity_gemm(M, N, K, dtype):
+    x = workloads.activations(M, K, seed=400 + M, dtype=dtype, outlier_p=0.0)
+    w = workloads.ternary_weights(N, K, seed=401 + N)
+    g, o = run_chain(x, dtype, w, workloads.weight_scale(N, K, 402), algo="gemm")
+    assert_chain_equal(g, o)
+
+
+def _matmul_only(xq, s, wp, w_scale, algo):
+    rs = xq.astype(np.int64).sum(axis=1).astype(np.int32)
+    M, N = xq.shape[0], wp.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    out = binding.i2s_matmul(dev(xq), dev(s), dev(rs), dev(wp), w_scale, acc_out=acc, algo=algo)
+    return host(out), host(acc)
+
+
+@pytest.mark.parametrize("algo", ["gemv", "gemm"])
+def test_max_magnitude_accumulators(algo):
+    """xq all +-127 against all-(+1) weights: |acc| = 127*K, the largest a ternary row gives."""
+    K, N, M = 8192, 260, 3
+    xq = np.full((M, K), 127, np.int8)
+    xq[1] = -127
+    xq[2, ::2] = -127
+    wp, _ = oracle.pack_i2s(np.ones((N, K), np.int8))
+    s = np.ones(M, np.float32)
+    out, acc = _matmul_only(xq, s, wp, 1.0, algo)
+    o_out, o_acc = oracle.ternary_matmul(xq, s, wp, 1.0, nthreads=NT)
+    assert np.array_equal(acc, o_acc) and acc[0, 0] == 127 * K and acc[1, 0] == -127 * K
+    assert np.array_equal(out.view(np.uint32), o_out.view(np.uint32))
+
+
+@pytest.mark.parametrize("algo", ["gemv", "gemm"])
+@pytest.mark.parametrize("M,N,K", [(5, 77, 2560), (130, 300, 1024)])
+def test_random_bytes_including_code3(algo, M, N, K):
+    """Arbitrary packed bytes (code 3 included, read as +2 by the c - 1 rule)."""
+    wp = workloads.random_packed_bytes(N, K, seed=500 + M)
+    xq = workloads.random_int8(M, K, seed=501 + M)
+    s = (np.random.default_rng(502).random(M).astype(np.float32) * 3 + 0.1).astype(np.float32)
+    out, acc = _matmul_only(xq, s, wp, 0.0173, algo)
+    o_out, o_acc = oracle.ternary_matmul(xq, s, wp, 0.0173, nthreads=NT)
+    assert np.array_equal(acc, o_acc)
+    assert_out_close(out, o_out)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 63, 64, 65, 127, 128, 129])
+def test_gemv_and_gemm_agree(M):
+    K, N = 2560, 600
+    xq = workloads.random_int8(M, K, seed=600 + M)
+    wp, _ = oracle.pack_i2s(workloads.ternary_weights(N, K, 601))
+    s = np.full(M, 1.7, np.float32)
+    a = _matmul_only(xq, s, wp, 0.02, "gemv")
+    b = _matmul_only(xq, s, wp, 0.02, "gemm")
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[0].view(np.uint32), b[0].view(np.uint32))
+
+
+def test_misaligned_pointer_is_rejected():
+    xq = torch.zeros(2 * 128 + 16, dtype=torch.int8, device="cuda")
+    wp = torch.zeros((4, 32), dtype=torch.uint8, device="cuda")
+    s = torch.ones(1, device="cuda")
+    rs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad = xq[1:129].view(1, 128)
+    with pytest.raises(binding.BitnetError) as e:
+        binding.i2s_matmul(bad, s, rs, wp, 1.0)
+    assert e.value.status == binding.BITNET_EALIGN
+
+
+# ----------------------------------------------------------------------------- full-size configs
+
+def _sampled_full_size(case, algo="auto", n_rows=16, n_cols=384):
+    """Full-size GPU run; the oracle recomputes sampled outputs one by one (all of xq/s/rowsum
+    and the packed weights are compared in full)."""
+    x, w, ws = case.x(), case.weights(), case.w_scale()
+    g_wp = binding.pack_i2s(dev(w))
+    g_xq, g_s, g_rs = binding.quant_act(x_device(x, case.act_dtype))
+    g_acc = torch.empty((case.M, case.N), dtype=torch.int32, device="cuda")
+    g_out = binding.i2s_matmul(g_xq, g_s, g_rs, g_wp, ws, acc_out=g_acc, algo=algo)
+    torch.cuda.synchronize()
+    o_wp, _ = oracle.pack_i2s(w)
+    o_xq, o_s, o_rs = oracle.quant_act(x, case.act_dtype)
+    assert np.array_equal(host(g_wp), o_wp)
+    assert np.array_equal(host(g_xq), o_xq)
+    assert np.array_equal(host(g_s).view(np.uint32), o_s.view(np.uint32))
+    assert np.array_equal(host(g_rs), o_rs)
+    rng = np.random.default_rng(700)
+    mi = np.unique(np.concatenate([[0, case.M - 1], rng.integers(0, case.M, n_rows)]))
+    ni = np.unique(np.concatenate([[0, case.N - 1], rng.integers(0, case.N, n_cols)]))
+    o_out, o_acc = oracle.ternary_matmul(o_xq[mi], o_s[mi], o_wp[ni], ws, nthreads=NT)
+    acc = host(g_acc)[np.ix_(mi, ni)]
+    out = host(g_out)[np.ix_(mi, ni)]
+    assert np.array_equal(acc, o_acc)
+    assert_out_close(out, o_out)
+
+
+@pytest.mark.parametrize("case", [workloads.single_gemv()] + workloads.batched_decode_cases()
+                         + workloads.prefill_cases() + workloads.large_cases(), ids=lambda c: c.name)
+def test_full_size_configs(case):
+    _sampled_full_size(case)
