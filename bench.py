@@ -1,0 +1,535 @@
+#!/usr/bin/env python
+"""Benchmark of the W2A8 ternary matmul hot path on GB300.
+
+Default workload (one "step"): the decode pass of a 2B-4T-shaped BitNet b1.58 model at
+M = 1 -- 30 layers x {q, k, v, o: 2560x2560 / 640x2560, gate, up: 6912x2560, down:
+2560x6912} ternary projections, grouped by shared input; each group's fp32 activation row is
+quantised per token (bitnet_quant_act) and every projection runs the i2_s GEMV
+(bitnet_i2s_matmul). 521 MB of packed weights per step stay resident in HBM; the step is one
+CUDA graph. The metric is algorithmic bytes moved per second (GB/s, 2 bits per weight).
+
+Also measured in the same run and reported alongside: the prefill GEMM (M=4096, K=6912,
+N=2560, bf16 activations) in TOPS, the end-to-end figure through host buffers (e2e), the
+roofline fraction of the dominant kernel, and the CPU oracle on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run: each rank runs its own replica (the projections of
+a decode step are independent per device; there is no data-path collective), and the
+timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from ternary_weight_gb300 import workloads  # noqa: E402
+
+METRIC = "i2_s ternary GEMV HBM GB/s (M=1) & prefill int8 TOPS, % of GB300 roofline"
+UNIT = "GB/s"
+N_LAYERS = workloads.N_LAYERS
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--layers", type=int, default=N_LAYERS)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
+    p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill"], default="decode_sweep",
+                   help="decode_sweep (default, the headline) or one single-kernel leg")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def aggregate(per_rank_seconds, per_rank_units):
+    """Whole-job throughput: units summed over ranks / slowest rank's time."""
+    t = max(per_rank_seconds)
+    return sum(per_rank_units) / t, t
+
+
+def allgather_floats(dist, world, values, device):
+    import torch
+
+    if world == 1:
+        return [list(values)]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    outs = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(outs, t)
+    return [o.tolist() for o in outs]
+
+
+# ------------------------------------------------------------------------------ workload
+
+def sweep_plan(n_layers):
+    """[(layer, group name, K, [(matrix name, N, K)])] of the decode sweep, in step order."""
+    mats = {name: (N, K) for name, N, K in workloads.LAYER_MATRICES}
+    plan = []
+    for spec in workloads.decode_sweep_specs(n_layers):
+        for gname, names, K in workloads.LAYER_GROUPS:
+            plan.append((spec, gname, K, [(n, mats[n][0], mats[n][1]) for n in names]))
+    return plan
+
+
+def build_stack(n_layers, device):
+    """Generate, upload and pack the sweep's weights; fill the step's fp32 activation rows."""
+    import torch
+
+    from ternary_weight_gb300.stack import Group, PackedLinear, TernaryStack
+
+    groups = []
+    for spec, gname, K, mats in sweep_plan(n_layers):
+        lins = []
+        for name, N, _ in mats:
+            w = torch.from_numpy(workloads.ternary_weights(N, K, spec.weight_seeds[name])).to(device)
+            ws = workloads.weight_scale(N, K, spec.scale_seeds[name])
+            lins.append(PackedLinear.from_ternary("L%d.%s" % (spec.layer, name), w, ws))
+            del w
+        groups.append(Group("L%d.%s" % (spec.layer, gname), K, lins))
+    stack = TernaryStack(groups, M=1, act_dtype=torch.float32, device=device)
+    xs = [workloads.activations_f32(1, g.K, spec.act_seeds[gname])
+          for g, (spec, gname, _, _) in zip(groups, sweep_plan(n_layers))]
+    x_host = torch.from_numpy(np.concatenate([x.ravel() for x in xs]))
+    stack.x_all.copy_(x_host)
+    torch.cuda.synchronize(device)
+    return stack, x_host
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        return self.summarise(rows)
+
+    @staticmethod
+    def summarise(rows):
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        smax = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(names, r[6:10]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------ timing helpers
+
+def time_replays(graph, steps, stream):
+    import torch
+
+    st = torch.cuda.Event(enable_timing=True)
+    en = torch.cuda.Event(enable_timing=True)
+    st.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    en.record(stream)
+    en.synchronize()
+    return st.elapsed_time(en) * 1e-3
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(kernel_file):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, valid only while the
+    kernel source is unchanged (profiles/traffic.txt: file sha16 bytes_per_launch workload)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "ternary_weight_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_file and parts[1] == sha:
+                return float(parts[2])
+    return None
+
+
+# ------------------------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(seconds, n_layers):
+    """Time the CPU oracle (as it stands) on whole groups of the sweep, in step order, until
+    the budget is spent. Returns (GB/s, sample description, threads)."""
+    import oracle
+
+    nt = oracle.default_threads()
+    plan = sweep_plan(n_layers)
+    done_bytes, t_total, groups_done, gi = 0, 0.0, 0, 0
+    cache = {}
+    while t_total < seconds and groups_done < 4 * len(plan):
+        spec, gname, K, mats = plan[gi % len(plan)]
+        key = gi % len(plan)
+        if key not in cache:
+            packed = []
+            for name, N, _ in mats:
+                wp, _ = oracle.pack_i2s(workloads.ternary_weights(N, K, spec.weight_seeds[name]))
+                packed.append((wp, workloads.weight_scale(N, K, spec.scale_seeds[name]), N))
+            cache[key] = (workloads.activations_f32(1, K, spec.act_seeds[gname]), packed)
+        x, packed = cache[key]
+        t0 = time.perf_counter()
+        xq, s, _ = oracle.quant_act(x)
+        for wp, ws, N in packed:
+            oracle.ternary_matmul(xq, s, wp, ws, nthreads=nt)
+        t_total += time.perf_counter() - t0
+        done_bytes += K * 5 + 8 + sum(wp.nbytes + K + 8 + 4 * N for wp, _, N in packed)
+        groups_done += 1
+        gi += 1
+    desc = "%d projection groups of the decode sweep (quant + GEMVs, layers 0..%d, cycled), %d threads" % (
+        groups_done, min(n_layers, (groups_done + 3) // 4) - 1, nt)
+    return done_bytes / t_total / 1e9, desc, nt, t_total, groups_done
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    steps, warmup = args.steps, args.warmup
+    import oracle
+
+    nt = oracle.default_threads()
+    plan = sweep_plan(min(args.layers, 2))  # bounded: the first two layers' groups, cycled
+    prepared = []
+    for spec, gname, K, mats in plan:
+        packed = []
+        for name, N, _ in mats:
+            wp, _ = oracle.pack_i2s(workloads.ternary_weights(N, K, spec.weight_seeds[name]))
+            packed.append((wp, workloads.weight_scale(N, K, spec.scale_seeds[name]), N))
+        prepared.append((workloads.activations_f32(1, K, spec.act_seeds[gname]), K, packed))
+
+    def one(i):
+        x, K, packed = prepared[i % len(prepared)]
+        xq, s, _ = oracle.quant_act(x)
+        for wp, ws, N in packed:
+            oracle.ternary_matmul(xq, s, wp, ws, nthreads=nt)
+        return K * 5 + 8 + sum(wp.nbytes + K + 8 + 4 * N for wp, _, N in packed)
+
+    for i in range(warmup):
+        one(i)
+    t0 = time.perf_counter()
+    total = 0
+    for i in range(steps):
+        total += one(i)
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    sample = "each step: one projection group of the decode sweep (quant + its GEMVs), cycling over layers 0-1"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": steps,
+        "warmup": warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "i8xi2->i32", "data": "synthetic",
+        "config": {"workload": "2B-4T decode sweep, M=1 (CPU oracle on a bounded sample)", "parallelism": "none"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ single-kernel legs
+
+def kernel_leg(kind, device, peaks, reps=20, warmup=3, sets=None):
+    """One matmul shape over rotating input sets whose total exceeds L2, timed with CUDA events.
+
+    kind = "prefill": tensor-core GEMM, M=4096, K=6912, N=2560, bf16 activations (8 sets);
+    kind = "gemv_100b": decode GEMV, M=1, K=8192, N=28672, bf16 activations (4 sets, 235 MB).
+    """
+    import torch
+
+    from ternary_weight_gb300 import binding
+
+    case = workloads.large_cases()[0 if kind == "prefill" else 1]
+    M, N, K = case.M, case.N, case.K
+    nsets = sets or (8 if kind == "prefill" else 4)
+    data = []
+    for i in range(nsets):
+        w = torch.from_numpy(workloads.ternary_weights(N, K, case.seed + 1 + 97 * i)).to(device)
+        x = torch.from_numpy(workloads.activations(M, K, case.seed + 97 * i, "bf16").view(np.int16)).to(device)
+        wp = binding.pack_i2s(w)
+        xq, s, rs = binding.quant_act(x.view(torch.bfloat16))
+        data.append((xq, s, rs, wp, workloads.weight_scale(N, K, case.seed + 2 + 97 * i),
+                     torch.empty((M, N), dtype=torch.float32, device=device)))
+        del w, x
+    stream = torch.cuda.current_stream(device)
+
+    def call(i):
+        xq, s, rs, wp, ws, out = data[i % nsets]
+        binding.i2s_matmul(xq, s, rs, wp, ws, out=out)
+
+    for i in range(max(3, warmup)):
+        call(i)
+    torch.cuda.synchronize(device)
+    # capture the timed launches in one graph so host launch cost does not enter the timing
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize(device)
+    st = torch.cuda.Event(enable_timing=True)
+    en = torch.cuda.Event(enable_timing=True)
+    st.record(stream)
+    g.replay()
+    en.record(stream)
+    en.synchronize()
+    dt = st.elapsed_time(en) * 1e-3 / reps
+    if kind == "prefill":
+        tops = 2.0 * M * N * K / dt / 1e12
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        return {"workload": "prefill GEMM M=4096 K=6912 N=2560 (bf16 activations quantised to int8)",
+                "value": tops, "unit": "TOPS", "ms_per_call": dt * 1e3, "launches": reps,
+                "roofline": {"bound": "tensor", "achieved": tops, "peak": peak, "unit": "TFLOP/s",
+                             "frac": tops / peak, "traffic": recorded_traffic("gemm_i2s_tc.cu"),
+                             "note": "int8 x ternary products run as exact fp16 tcgen05 MMAs (kind::i8 does "
+                                     "not exist on sm_103a); peak = measured dense bf16 burst, the fp16 rate"}}
+    byts = N * K / 4 + M * K + 8 * M + 4 * M * N
+    gbs = byts / dt / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"workload": "100B-class GEMV M=1 K=8192 N=28672 (bf16 activations quantised to int8)",
+            "value": gbs, "unit": "GB/s", "ms_per_call": dt * 1e3, "launches": reps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": recorded_traffic("gemv_i2s.cu")}}
+
+
+def run_kernel_workload(args):
+    """--workload gemv_100b | prefill: one line for that single kernel (no e2e / CPU leg)."""
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from ternary_weight_gb300 import _build, binding
+
+    _build.build()
+    binding.lib()
+    peaks, _ = measured_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    leg = kernel_leg(args.workload, device, peaks, reps=args.steps, warmup=args.warmup)
+    clocks = sampler.stop()
+    line = {"metric": METRIC, "value": leg["value"], "unit": leg["unit"], "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": leg["ms_per_call"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "i8xi2->i32", "data": "synthetic",
+            "config": {"workload": leg["workload"], "l2": "rotating input sets larger than L2"},
+            "gpu_launches": args.steps, "clocks": clocks, "roofline": leg["roofline"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ main arm
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+
+    from ternary_weight_gb300 import _build, binding
+
+    if rank == 0 or not os.path.exists(_build.LIB_PATH):
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    binding.lib()
+
+    peaks, peak_kind = measured_peaks()
+    stack, x_host = build_stack(args.layers, device)
+    graph = stack.capture()
+    gemv_graph = stack.capture(gemv_only=True)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(device)
+
+    # ---- timed region: K graph replays of the whole step ----
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    t_step = time_replays(graph, args.steps, stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    bytes_step = stack.bytes_per_step()
+    per_rank = allgather_floats(dist, world, [t_step, float(bytes_step * args.steps)], device)
+    value_bps, t_max = aggregate([r[0] for r in per_rank], [r[1] for r in per_rank])
+    ms_per_step = t_max / args.steps * 1e3
+
+    # ---- dominant kernel (the GEMV): same launches without the quantisation, CUDA events ----
+    for _ in range(3):
+        gemv_graph.replay()
+    reps = max(20, args.steps // 4)
+    t_gemv = time_replays(gemv_graph, reps, stream) / reps
+    n_gemv = stack.gemv_launches_per_step()
+    gemv_bytes_launch = stack.gemv_bytes_per_step() / n_gemv
+    achieved = gemv_bytes_launch / (t_gemv / n_gemv) / 1e9
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    traffic = recorded_traffic("gemv_i2s.cu")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": traffic, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback",
+                "kernel": "gemv_i2s_kernel (avg over the step's %d GEMV launches, back to back in one graph)" % n_gemv}
+
+    # ---- e2e: pinned host activations in, every projection's output back, each step ----
+    x_pin = x_host.pin_memory()
+    out_pin = torch.empty(stack.out_elems, dtype=torch.float32).pin_memory()
+    e2e_steps = max(10, args.steps // 4)
+    for _ in range(3):
+        stack.x_all.copy_(x_pin, non_blocking=True)
+        graph.replay()
+        out_pin.copy_(stack.out_all, non_blocking=True)
+    torch.cuda.synchronize(device)
+    st = torch.cuda.Event(enable_timing=True)
+    en = torch.cuda.Event(enable_timing=True)
+    st.record(stream)
+    for _ in range(e2e_steps):
+        stack.x_all.copy_(x_pin, non_blocking=True)
+        graph.replay()
+        out_pin.copy_(stack.out_all, non_blocking=True)
+    en.record(stream)
+    en.synchronize()
+    t_e2e = st.elapsed_time(en) * 1e-3
+    per_rank_e2e = allgather_floats(dist, world, [t_e2e, float(bytes_step * e2e_steps)], device)
+    e2e_bps, _ = aggregate([r[0] for r in per_rank_e2e], [r[1] for r in per_rank_e2e])
+
+    prefill = None if args.no_prefill else kernel_leg("prefill", device, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, desc, nt, _, _ = oracle_sample(args.cpu_seconds, args.layers)
+        cpu = {"value": gbs, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value_bps / 1e9, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "i8xi2->i32", "data": "synthetic (seeded numpy PCG64; see workloads.py)",
+        "config": {
+            "workload": "decode sweep of a 2B-4T-shaped model: %d layers x {q,k,v,o,gate,up,down}, M=1, fp32 "
+                        "activations quantised per token to int8" % args.layers,
+            "layers": args.layers, "M": 1, "bytes_per_step": bytes_step,
+            "packed_weight_bytes_per_step": sum(l.weight_bytes() for g in stack.groups for l in g.linears),
+            "l2": "inputs larger than L2: %.0f MB of packed weights streamed per step (L2 is 129 MB)"
+                  % (sum(l.weight_bytes() for g in stack.groups for l in g.linears) / 1e6),
+            "graph": "one CUDA graph per step: %d launches" % stack.launches_per_step(),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "gpu_launches": stack.launches_per_step() * args.steps,
+        "clocks": clocks,
+        "roofline": roofline,
+        "e2e": {"value": e2e_bps / 1e9, "unit": UNIT, "h2d_bytes_per_step": stack.act_bytes_in,
+                "d2h_bytes_per_step": stack.out_elems * 4,
+                "note": "pinned host activations -> device, graph step, all projection outputs -> host, each step"},
+        "prefill": prefill,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.workload != "decode_sweep":
+        return run_kernel_workload(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -27,6 +27,8 @@
 
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 namespace bitnet {
 namespace {
 
@@ -245,8 +247,17 @@ cudaError_t launch_gemm_i2s_tc(const int8_t* xq, const float* act_scale, const i
                                const uint8_t* wp, float w_scale, float* out, int32_t* acc_out, int64_t M,
                                int64_t N, int64_t K, int num_sms, cudaStream_t stream) {
   (void)num_sms;
-  cudaError_t e = cudaFuncSetAttribute(gemm_i2s_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  // the large dynamic shared-memory opt-in is a per-device function attribute: set it once
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gemm_i2s_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
   gemm_i2s_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(xq, act_scale, rowsum, wp, w_scale, out, acc_out,
                                                              (int)M, (int)N, (int)K);

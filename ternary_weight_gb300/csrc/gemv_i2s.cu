@@ -27,6 +27,8 @@
 //    are reduced with xor-shuffles inside the G-lane group.
 #include "bitnet_dev.cuh"
 
+#include <atomic>
+
 namespace bitnet {
 namespace {
 
@@ -151,8 +153,17 @@ cudaError_t launch_cfg(const int8_t* xq, const float* s, const int32_t* rs, cons
   const int smem = MT * K;
   auto kern = gemv_i2s_kernel<MT, R>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // per-device opt-in to the largest staging size this instantiation can need, set once
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxActSmem);
+      if (e != cudaSuccess) return e;
+      configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
   }
   const int rows_per_tile = (32 >> log2G) * R;
   const int64_t tiles = ((int64_t)N + rows_per_tile - 1) / rows_per_tile;

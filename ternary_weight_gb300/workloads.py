@@ -10,8 +10,9 @@ attention with 4 query heads per KV head -> k/v projections of 640 rows), as des
 GEMV shape K=8192, N=28672.
 
 Recipe (all draws use numpy's PCG64 ``default_rng`` with the seed stated per tensor):
-  * ternary weights: iid, P(-1) = 0.3, P(0) = 0.4, P(+1) = 0.3, drawn as a uniform
-    integer u in [0, 10): u < 3 -> -1, u < 7 -> 0, else +1;
+  * ternary weights: iid, P(-1) = 0.3, P(0) = 0.4, P(+1) = 0.3: a uniform 16-bit b gives
+    u = floor(10 * b / 65536) in [0, 10) (each u has probability 0.1 to within 1e-4
+    relative), then u < 3 -> -1, u < 7 -> 0, else +1;
   * weight scale alpha_W = mean|W_src| of a separately drawn N(0, 0.02) source (a sample
     of min(N*K, 2**20) elements stands for the full matrix; the expectation is
     0.02*sqrt(2/pi) ~= 0.01596);
@@ -50,13 +51,15 @@ LAYER_GROUPS: List[Tuple[str, List[str], int]] = [
 ]
 
 _TERNARY_OF_U = np.array([-1, -1, -1, 0, 0, 0, 0, 1, 1, 1], dtype=np.int8)
+# the same map applied to every 16-bit draw b: u = floor(10 * b / 65536)
+_TERNARY_OF_B16 = _TERNARY_OF_U[(np.arange(1 << 16, dtype=np.uint32) * 10) >> 16]
 
 
 def ternary_weights(N: int, K: int, seed: int) -> np.ndarray:
     """N x K int8 ternary matrix, iid P(-1)=P(+1)=0.3, P(0)=0.4."""
     rng = np.random.default_rng(seed)
-    u = rng.integers(0, 10, size=(N, K), dtype=np.uint8)
-    return _TERNARY_OF_U[u]
+    b = rng.integers(0, 1 << 16, size=(N, K), dtype=np.uint16)
+    return _TERNARY_OF_B16[b]
 
 
 def weight_scale(N: int, K: int, seed: int) -> float:
