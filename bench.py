@@ -5,8 +5,8 @@ Default workload (one "step"): the decode pass of a 2B-4T-shaped BitNet b1.58 mo
 M = 1 -- 30 layers x {q, k, v, o: 2560x2560 / 640x2560, gate, up: 6912x2560, down:
 2560x6912} ternary projections, grouped by shared input; each group's fp32 activation row is
 quantised per token (bitnet_quant_act) and every projection runs the i2_s GEMV
-(bitnet_i2s_matmul). 521 MB of packed weights per step stay resident in HBM; the step is one
-CUDA graph. The metric is algorithmic bytes moved per second (GB/s, 2 bits per weight).
+(bitnet_i2s_matmul) -- fused into one bitnet_w2a8_linear_group launch per group. 521 MB of
+packed weights per step stay resident in HBM; the step is one CUDA graph. The metric is algorithmic bytes moved per second (GB/s, 2 bits per weight).
 
 Also measured in the same run and reported alongside: the prefill GEMM (M=4096, K=6912,
 N=2560, bf16 activations) in TOPS, the end-to-end figure through host buffers (e2e), the
@@ -423,7 +423,6 @@ def run_ours(args):
     peaks, peak_kind = measured_peaks()
     stack, x_host = build_stack(args.layers, device)
     graph = stack.capture()
-    gemv_graph = stack.capture(gemv_only=True)
     stream = torch.cuda.current_stream(device)
 
     for _ in range(max(3, args.warmup)):
@@ -447,20 +446,17 @@ def run_ours(args):
     value_bps, t_max = aggregate([r[0] for r in per_rank], [r[1] for r in per_rank])
     ms_per_step = t_max / args.steps * 1e3
 
-    # ---- dominant kernel (the GEMV): same launches without the quantisation, CUDA events ----
-    for _ in range(3):
-        gemv_graph.replay()
-    reps = max(20, args.steps // 4)
-    t_gemv = time_replays(gemv_graph, reps, stream) / reps
-    n_gemv = stack.gemv_launches_per_step()
-    gemv_bytes_launch = stack.gemv_bytes_per_step() / n_gemv
-    achieved = gemv_bytes_launch / (t_gemv / n_gemv) / 1e9
+    # ---- dominant kernel: every launch of the fused step is the single-token fused
+    # quantisation + GEMV kernel, so its average launch duration is the timed step over its
+    # launches (CUDA events on the launching stream, back-to-back launches in one graph) ----
+    n_launch = stack.launches_per_step()
+    achieved = (bytes_step / n_launch) / (t_step / args.steps / n_launch) / 1e9
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    traffic = recorded_traffic("gemv_i2s.cu")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": traffic, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                else "fallback",
-                "kernel": "gemv_i2s_kernel (avg over the step's %d GEMV launches, back to back in one graph)" % n_gemv}
+                "traffic": recorded_traffic("gemv_m1.cu"),
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "kernel": "gemv_m1_kernel<T,FUSE> (fused quantisation + grouped GEMV), avg over the step's "
+                          "%d launches; algorithmic bytes per launch %.0f" % (n_launch, bytes_step / n_launch)}
 
     # ---- e2e: pinned host activations in, every projection's output back, each step ----
     x_pin = x_host.pin_memory()

@@ -138,6 +138,36 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t *xq, const float *act_scale,
                                       int64_t K, int algo, void *stream);
 
 /*
+ * bitnet_w2a8_linear_group -- per-token activation quantisation fused with the ternary
+ * matmuls of up to 8 projections that consume the same activation rows (e.g. q/k/v, or
+ * gate/up). Computes, for l = 0..count-1, exactly what bitnet_quant_act followed by
+ * bitnet_i2s_matmul(xq, s, rowsum, wp[l], w_scale[l], out[l], acc_out[l], M, N[l], K) gives.
+ *   [DeepDive] §4-5 (quant_input then the int8 x int2 linear), §4-3 (one decoded activation
+ *   set reused for several weight columns); the arithmetic is that of bitnet_quant_act and
+ *   bitnet_i2s_matmul.
+ *
+ *   x          : M x K fp32 (BITNET_F32) or bf16 (BITNET_BF16)                  (device, read)
+ *   count      : 1..8 projections
+ *   wp, w_scale, N, out, acc_out : HOST arrays of length count (acc_out may be NULL, and so
+ *                may any entry); wp[l] N[l] x K/4 packed (device), out[l] M x N[l] fp32
+ *                (device, written), acc_out[l] M x N[l] int32 (device, written)
+ *   xq, act_scale, rowsum : M x K int8, M fp32, M int32 (device, written). With M == 1 and
+ *                K <= 10240 the whole call is one kernel launch and these three may be NULL
+ *                (each non-NULL one is written); otherwise they are required workspace and
+ *                the call is one quantisation launch plus one matmul launch per projection.
+ *   Same size, alignment and dtype rules as bitnet_quant_act and bitnet_i2s_matmul.
+ */
+BITNET_API int bitnet_w2a8_linear_group(const void *x, int dtype, int64_t M, int64_t K, int count,
+                                        const uint8_t *const *wp, const float *w_scale,
+                                        const int64_t *N, float *const *out, int32_t *const *acc_out,
+                                        int8_t *xq, float *act_scale, int32_t *rowsum, void *stream);
+
+/* bitnet_w2a8_linear -- bitnet_w2a8_linear_group with a single projection. */
+BITNET_API int bitnet_w2a8_linear(const void *x, int dtype, int64_t M, int64_t K, const uint8_t *wp,
+                                  float w_scale, int64_t N, float *out, int32_t *acc_out, int8_t *xq,
+                                  float *act_scale, int32_t *rowsum, void *stream);
+
+/*
  * bitnet_last_device_error -- read and clear the device-side error word of the current
  * device. Kernels that wait on an mbarrier give up after a bounded number of polls and
  * record BITNET_ETIMEOUT there instead of hanging. Synchronises the device.

@@ -36,6 +36,10 @@ SIGNATURES = {
     "bitnet_i2s_matmul": ([_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "bitnet_i2s_matmul_algo": (
         [_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
+    "bitnet_w2a8_linear_group": (
+        [_P, ctypes.c_int, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "bitnet_w2a8_linear": (
+        [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_float, _I64, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "bitnet_last_device_error": ([], ctypes.c_int),
 }
 
@@ -142,6 +146,44 @@ def i2s_matmul(xq, scale, rowsum, wp, w_scale, out=None, acc_out=None, algo="aut
                                         _ptr(out), _ptr(acc_out), M, N, K, ALGO[algo], _stream(stream)),
            "bitnet_i2s_matmul")
     return out
+
+
+def _act_dtype(x):
+    import torch
+
+    if x.dtype == torch.float32:
+        return BITNET_F32
+    if x.dtype == torch.bfloat16:
+        return BITNET_BF16
+    raise ValueError("x must be float32 or bfloat16")
+
+
+def linear_group(x, wps, w_scales, outs=None, accs=None, xq=None, scale=None, rowsum=None, stream=None):
+    """Quantise x (M x K fp32/bf16) and multiply it with up to 8 packed projections sharing it.
+
+    One kernel launch when M == 1 (and K <= 10240); xq/scale/rowsum are then optional outputs.
+    Returns the list of M x N_l fp32 outputs."""
+    import torch
+
+    dt = _act_dtype(x)
+    M, K = x.shape
+    n = len(wps)
+    for w in wps:
+        if w.shape[1] * 4 != K:
+            raise ValueError("every wp must be N x K/4")
+    if outs is None:
+        outs = [torch.empty((M, w.shape[0]), dtype=torch.float32, device=x.device) for w in wps]
+    _require_cuda(x, xq, scale, rowsum, *wps, *outs, *(accs or []))
+    P = ctypes.c_void_p * n
+    wp_arr = P(*[w.data_ptr() for w in wps])
+    out_arr = P(*[o.data_ptr() for o in outs])
+    acc_arr = P(*[(a.data_ptr() if a is not None else None) for a in accs]) if accs is not None else None
+    ws_arr = (ctypes.c_float * n)(*[float(v) for v in w_scales])
+    n_arr = (ctypes.c_int64 * n)(*[int(w.shape[0]) for w in wps])
+    _check(lib().bitnet_w2a8_linear_group(_ptr(x), dt, M, K, n, wp_arr, ws_arr, n_arr, out_arr, acc_arr,
+                                          _ptr(xq), _ptr(scale), _ptr(rowsum), _stream(stream)),
+           "bitnet_w2a8_linear_group")
+    return outs
 
 
 def last_device_error() -> int:

@@ -73,6 +73,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool* 
   return false;
 }
 
+// One arrival that also announces tx_bytes of asynchronous (bulk copy) data for the phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx_bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(tx_bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared (TMA engine); completion is counted on the mbarrier in
+// bytes. dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Named barrier over a subset of the CTA's warps (id 1..15; count a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -167,8 +189,31 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Single-token projections sharing one activation row (kernel parameter, passed by value)
+// ---------------------------------------------------------------------------------------
+constexpr int kMaxGroupLinears = 8;
+struct LinearSet {
+  const uint8_t* wp[kMaxGroupLinears];  // N_l x K/4 packed weights
+  float* out[kMaxGroupLinears];         // N_l fp32 outputs
+  int32_t* acc[kMaxGroupLinears];       // optional N_l int32 accumulators
+  float w_scale[kMaxGroupLinears];
+  int N[kMaxGroupLinears];
+  int count;
+};
+struct QuantOut {  // optional outputs of a fused quantisation (each may be null)
+  int8_t* xq;
+  float* scale;
+  int32_t* rowsum;
+};
+
+// ---------------------------------------------------------------------------------------
 // Launchers (defined in the kernel translation units). All return cudaError_t of the launch.
 // ---------------------------------------------------------------------------------------
+// M = 1 GEMV over a LinearSet. fuse: 0 = x is xq (int8) with act_scale and rowsum; 1 = x is
+// fp32, 2 = x is bf16 (quantised in the kernel, qout optionally written).
+bool gemv_m1_supported(int64_t K);
+cudaError_t launch_gemv_m1(const void* x, int fuse, const float* act_scale, const int32_t* rowsum,
+                           const LinearSet& set, const QuantOut& qout, int64_t K, int num_sms, cudaStream_t stream);
 cudaError_t launch_pack_i2s(const int8_t* w, uint8_t* wp, int64_t N, int64_t K, int32_t* invalid_count,
                             cudaStream_t stream);
 cudaError_t launch_quant_act(const void* x, int dtype, int64_t M, int64_t K, int8_t* xq, float* act_scale,

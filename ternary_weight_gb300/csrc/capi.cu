@@ -120,6 +120,58 @@ BITNET_API int bitnet_i2s_matmul(const int8_t* xq, const float* act_scale, const
                                 stream);
 }
 
+BITNET_API int bitnet_w2a8_linear_group(const void* x, int dtype, int64_t M, int64_t K, int count,
+                                        const uint8_t* const* wp, const float* w_scale, const int64_t* N,
+                                        float* const* out, int32_t* const* acc_out, int8_t* xq, float* act_scale,
+                                        int32_t* rowsum, void* stream) {
+  if (!x || !wp || !w_scale || !N || !out) return BITNET_EINVAL;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_EINVAL;
+  if (count < 1 || count > kMaxGroupLinears) return BITNET_EINVAL;
+  if (M < 1 || M > INT32_MAX || !valid_k(K)) return BITNET_EINVAL;
+  if (!aligned(x, 16)) return BITNET_EALIGN;
+  int64_t total_rows = 0;
+  for (int l = 0; l < count; ++l) {
+    if (!wp[l] || !out[l] || N[l] < 1 || N[l] > INT32_MAX) return BITNET_EINVAL;
+    if (!aligned(wp[l], 16) || !aligned(out[l], 4) || (acc_out && acc_out[l] && !aligned(acc_out[l], 4)))
+      return BITNET_EALIGN;
+    total_rows += N[l];
+  }
+  const bool single_launch = (M == 1 && gemv_m1_supported(K) && total_rows <= INT32_MAX);
+  if (!single_launch && (!xq || !act_scale || !rowsum)) return BITNET_EINVAL;
+  if ((xq && !aligned(xq, 16)) || (act_scale && !aligned(act_scale, 4)) || (rowsum && !aligned(rowsum, 4)))
+    return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (single_launch) {
+    LinearSet set{};
+    for (int l = 0; l < count; ++l) {
+      set.wp[l] = wp[l];
+      set.out[l] = out[l];
+      set.acc[l] = acc_out ? acc_out[l] : nullptr;
+      set.w_scale[l] = w_scale[l];
+      set.N[l] = (int)N[l];
+    }
+    set.count = count;
+    return status_of(launch_gemv_m1(x, dtype == BITNET_BF16 ? 2 : 1, nullptr, nullptr, set,
+                                    QuantOut{xq, act_scale, rowsum}, K, sms, s));
+  }
+  if (cudaError_t e = launch_quant_act(x, dtype, M, K, xq, act_scale, rowsum, s)) return status_of(e);
+  for (int l = 0; l < count; ++l) {
+    int st = bitnet_i2s_matmul_algo(xq, act_scale, rowsum, wp[l], w_scale[l], out[l], acc_out ? acc_out[l] : nullptr,
+                                    M, N[l], K, BITNET_ALGO_AUTO, stream);
+    if (st != BITNET_OK) return st;
+  }
+  return BITNET_OK;
+}
+
+BITNET_API int bitnet_w2a8_linear(const void* x, int dtype, int64_t M, int64_t K, const uint8_t* wp, float w_scale,
+                                  int64_t N, float* out, int32_t* acc_out, int8_t* xq, float* act_scale,
+                                  int32_t* rowsum, void* stream) {
+  int32_t* accs[1] = {acc_out};
+  return bitnet_w2a8_linear_group(x, dtype, M, K, 1, &wp, &w_scale, &N, &out, accs, xq, act_scale, rowsum, stream);
+}
+
 BITNET_API int bitnet_last_device_error(void) {
   int sms = 0;
   if (int st = check_device(&sms)) return st;

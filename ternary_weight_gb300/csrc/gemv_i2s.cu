@@ -1,4 +1,5 @@
-// gemv_i2s.cu -- decode GEMV (small M): i2_s packed ternary weights x int8 activations.
+// gemv_i2s.cu -- decode GEMV (small M > 1; M = 1 goes to gemv_m1.cu): i2_s packed ternary
+// weights x int8 activations.
 //
 // What it computes (per output (m, n)):
 //   raw = sum_k code[n][k] * xq[m][k]       codes 0/1/2 multiplied as stored
@@ -178,6 +179,16 @@ cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int3
                             float w_scale, float* out, int32_t* acc_out, int64_t M64, int64_t N64, int64_t K64,
                             int num_sms, cudaStream_t stream) {
   const int M = (int)M64, N = (int)N64, K = (int)K64;
+  if (M == 1 && gemv_m1_supported(K)) {
+    LinearSet set{};
+    set.wp[0] = wp;
+    set.out[0] = out;
+    set.acc[0] = acc_out;
+    set.w_scale[0] = w_scale;
+    set.N[0] = N;
+    set.count = 1;
+    return launch_gemv_m1(xq, 0, act_scale, rowsum, set, QuantOut{nullptr, nullptr, nullptr}, K, num_sms, stream);
+  }
   const int C = K >> 6;
   int log2G = 5;
   while (log2G > 1 && (C & ((1 << log2G) - 1)) != 0) --log2G;  // C is even, so G >= 2 divides it

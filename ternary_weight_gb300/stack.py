@@ -3,9 +3,9 @@
 A decode step of a BitNet b1.58 model applies, layer after layer, groups of ternary
 projections that share one activation row (q/k/v on the attention input, o on the attention
 output, gate/up on the FFN input, down on the FFN middle). ``TernaryStack`` keeps every
-projection's i2_s packed weights resident in HBM and runs, per group, one activation
-quantisation followed by one GEMV per projection -- all through the C ABI -- in a fixed
-order. The whole sequence is captured once into a CUDA graph, so a step is one graph
+projection's i2_s packed weights resident in HBM and runs, per group, the activation
+quantisation and one GEMV per projection -- all through the C ABI, by default as one fused
+launch per group -- in a fixed order. The whole sequence is captured once into a CUDA graph, so a step is one graph
 launch. Activations enter through one contiguous input buffer and results leave through
 one contiguous output buffer, so a host round trip is one copy each way.
 
@@ -53,8 +53,9 @@ class TernaryStack:
     """Groups of ternary projections executed in order, as one CUDA graph per step."""
 
     def __init__(self, groups: Sequence[Group], M: int = 1, act_dtype=torch.float32, device="cuda",
-                 algo: str = "auto"):
+                 algo: str = "auto", fused: bool = True):
         self.groups = list(groups)
+        self.fused = fused
         self.M = M
         self.act_dtype = act_dtype
         self.device = torch.device(device)
@@ -85,6 +86,8 @@ class TernaryStack:
 
     # ---- accounting ----
     def launches_per_step(self) -> int:
+        if self.fused and self.M == 1:
+            return len(self.groups)
         return sum(1 + len(g.linears) for g in self.groups)
 
     def gemv_launches_per_step(self) -> int:
@@ -105,8 +108,20 @@ class TernaryStack:
 
     # ---- execution ----
     def run(self, stream=None, gemv_only: bool = False):
-        """Enqueue one step (quantise each group's row, then its GEMVs) on the stream."""
+        """Enqueue one step (quantise each group's row, then its GEMVs) on the stream.
+
+        fused (default): one bitnet_w2a8_linear_group call per group -- quantisation and every
+        projection of the group in a single kernel when M == 1. Otherwise (or with gemv_only,
+        which leaves out the quantisation) one quantisation launch per group and one
+        bitnet_i2s_matmul launch per projection."""
         for gi, g in enumerate(self.groups):
+            if self.fused and not gemv_only:
+                single = self.M == 1
+                binding.linear_group(self.x[gi], [l.wp for l in g.linears], [l.w_scale for l in g.linears],
+                                     outs=self.out[gi], xq=None if single else self.xq[gi],
+                                     scale=None if single else self.s[gi], rowsum=None if single else self.rs[gi],
+                                     stream=stream)
+                continue
             if not gemv_only:
                 binding.quant_act(self.x[gi], self.xq[gi], self.s[gi], self.rs[gi], stream=stream)
             for li, l in enumerate(g.linears):

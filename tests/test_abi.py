@@ -110,3 +110,24 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         binding.lib()
+
+
+def _group(lib, x=FAKE, dtype=0, M=1, K=128, count=1, wp=(FAKE,), ws=(1.0,), N=(1,), out=(FAKE,), acc=None,
+           xq=None, s=None, rs=None):
+    wp_a = (ctypes.c_void_p * len(wp))(*wp) if wp is not None else None
+    out_a = (ctypes.c_void_p * len(out))(*out) if out is not None else None
+    acc_a = (ctypes.c_void_p * len(acc))(*acc) if acc is not None else None
+    ws_a = (ctypes.c_float * len(ws))(*ws)
+    n_a = (ctypes.c_int64 * len(N))(*N)
+    return lib.bitnet_w2a8_linear_group(x, dtype, M, K, count, wp_a, ws_a, n_a, out_a, acc_a, xq, s, rs, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), -1), (dict(dtype=5), -1), (dict(count=0), -1), (dict(count=9), -1), (dict(M=0), -1),
+    (dict(K=200), -1), (dict(wp=None), -1), (dict(out=None), -1), (dict(wp=(0,)), -1), (dict(N=(0,)), -1),
+    (dict(M=2), -1), (dict(K=16384), -1),                       # workspace required beyond one launch
+    (dict(x=FAKE + 4), -2), (dict(wp=(FAKE + 8,)), -2), (dict(out=(FAKE + 2,)), -2),
+    (dict(acc=(FAKE + 1,)), -2), (dict(xq=FAKE + 8), -2),
+])
+def test_linear_group_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _group(lib, **kw) == status

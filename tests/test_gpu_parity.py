@@ -249,3 +249,93 @@ def _sampled_full_size(case, algo="auto", n_rows=16, n_cols=384):
                          + workloads.prefill_cases() + workloads.large_cases(), ids=lambda c: c.name)
 def test_full_size_configs(case):
     _sampled_full_size(case)
+
+
+# ----------------------------------------------------------------------------- fused, grouped linear
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K,Ns", [(128, [1]), (384, [5, 17]), (2560, [2560, 640, 640]), (2560, [6912, 6912]),
+                                  (6912, [2560]), (8192, [3000, 1]), (10240, [300]), (1152, [77]),
+                                  (2560, [7, 64, 100, 33, 2, 640, 1, 257])])
+def test_linear_group_m1_fused(dtype, K, Ns):
+    """One launch: quantisation + up to 8 projections; every output, accumulator and the
+    published xq / s / rowsum against the oracle."""
+    x = workloads.activations(1, K, seed=800 + K, dtype=dtype, outlier_p=0.01)
+    ws = [workloads.ternary_weights(N, K, seed=801 + i) for i, N in enumerate(Ns)]
+    scales = [workloads.weight_scale(N, K, seed=830 + i) for i, N in enumerate(Ns)]
+    wps = [binding.pack_i2s(dev(w)) for w in ws]
+    accs = [torch.empty((1, N), dtype=torch.int32, device="cuda") for N in Ns]
+    xq = torch.empty((1, K), dtype=torch.int8, device="cuda")
+    s = torch.empty(1, dtype=torch.float32, device="cuda")
+    rs = torch.empty(1, dtype=torch.int32, device="cuda")
+    outs = binding.linear_group(x_device(x, dtype), wps, scales, accs=accs, xq=xq, scale=s, rowsum=rs)
+    torch.cuda.synchronize()
+    o_xq, o_s, o_rs = oracle.quant_act(x, dtype)
+    assert np.array_equal(host(xq), o_xq)
+    assert np.array_equal(host(s).view(np.uint32), o_s.view(np.uint32))
+    assert np.array_equal(host(rs), o_rs)
+    for w, sc, out, acc in zip(ws, scales, outs, accs):
+        o_out, o_acc = oracle.ternary_matmul(o_xq, o_s, oracle.pack_i2s(w)[0], sc, nthreads=NT)
+        assert np.array_equal(host(acc), o_acc)
+        assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32))
+
+
+def test_linear_group_m1_without_quant_outputs():
+    K, Ns = 2560, [2560, 640]
+    x = workloads.activations(1, K, seed=850, dtype="f32")
+    ws = [workloads.ternary_weights(N, K, seed=851 + i) for i, N in enumerate(Ns)]
+    outs = binding.linear_group(dev(x), [binding.pack_i2s(dev(w)) for w in ws], [0.02, 0.03])
+    torch.cuda.synchronize()
+    o_xq, o_s, _ = oracle.quant_act(x)
+    for w, sc, out in zip(ws, [0.02, 0.03], outs):
+        o_out, _ = oracle.ternary_matmul(o_xq, o_s, oracle.pack_i2s(w)[0], sc, nthreads=NT)
+        assert_out_close(host(out), o_out)
+
+
+@pytest.mark.parametrize("M,K", [(3, 2560), (130, 1024), (1, 16384)])
+def test_linear_group_two_launch_path(M, K):
+    """M > 1 (or K beyond the single-launch kernel): quantisation then one matmul per projection."""
+    x = workloads.activations(M, K, seed=860 + M, dtype="bf16")
+    Ns = [300, 129]
+    ws = [workloads.ternary_weights(N, K, seed=861 + i) for i, N in enumerate(Ns)]
+    xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    s = torch.empty(M, dtype=torch.float32, device="cuda")
+    rs = torch.empty(M, dtype=torch.int32, device="cuda")
+    accs = [torch.empty((M, N), dtype=torch.int32, device="cuda") for N in Ns]
+    outs = binding.linear_group(x_device(x, "bf16"), [binding.pack_i2s(dev(w)) for w in ws], [0.02, 0.03],
+                                accs=accs, xq=xq, scale=s, rowsum=rs)
+    torch.cuda.synchronize()
+    o_xq, o_s, _ = oracle.quant_act(x, "bf16")
+    assert np.array_equal(host(xq), o_xq)
+    for w, sc, out, acc in zip(ws, [0.02, 0.03], outs, accs):
+        o_out, o_acc = oracle.ternary_matmul(o_xq, o_s, oracle.pack_i2s(w)[0], sc, nthreads=NT)
+        assert np.array_equal(host(acc), o_acc)
+        assert_out_close(host(out), o_out)
+
+
+def test_linear_group_requires_workspace_beyond_single_launch():
+    x = torch.zeros((2, 256), device="cuda")
+    wp = torch.zeros((4, 64), dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.BitnetError) as e:
+        binding.linear_group(x, [wp], [1.0])
+    assert e.value.status == binding.BITNET_EINVAL
+
+
+def test_stack_fused_equals_unfused():
+    """The decode stack's fused step and its two-launch step give identical outputs."""
+    from ternary_weight_gb300.stack import Group, PackedLinear, TernaryStack
+
+    groups = []
+    for gi, (K, Ns) in enumerate([(2560, [2560, 640, 640]), (2560, [2560]), (2560, [6912, 6912]), (6912, [2560])]):
+        lins = [PackedLinear.from_ternary("p%d_%d" % (gi, i), dev(workloads.ternary_weights(N, K, 870 + 10 * gi + i)),
+                                          0.01 + 0.001 * i) for i, N in enumerate(Ns)]
+        groups.append(Group("g%d" % gi, K, lins))
+    outs = []
+    for fused in (True, False):
+        st = TernaryStack(groups, M=1, fused=fused)
+        xs = np.concatenate([workloads.activations_f32(1, g.K, 890 + i).ravel() for i, g in enumerate(groups)])
+        st.x_all.copy_(torch.from_numpy(xs))
+        st.step()
+        torch.cuda.synchronize()
+        outs.append(host(st.out_all))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
