@@ -162,6 +162,23 @@ BITNET_API int bitnet_w2a8_linear_group(const void *x, int dtype, int64_t M, int
                                         const int64_t *N, float *const *out, int32_t *const *acc_out,
                                         int8_t *xq, float *act_scale, int32_t *rowsum, void *stream);
 
+/*
+ * bitnet_w2a8_linear_group_ex -- bitnet_w2a8_linear_group plus an L2 prefetch hint: up to 8
+ * device byte ranges (16-byte aligned starts; a partial last 16 bytes is skipped) that the
+ * single-launch kernel pulls into L2 while it runs -- typically the packed weights of the
+ * next group, so that the next call finds them on chip. The hint never changes a result and
+ * is ignored on the two-launch path. prefetch_ptr / prefetch_bytes are HOST arrays.
+ * The single-launch kernel also allows the following kernel in the stream to start early
+ * (programmatic dependent launch); it reads x and writes its outputs only after the
+ * preceding kernel in the stream has completed.
+ */
+BITNET_API int bitnet_w2a8_linear_group_ex(const void *x, int dtype, int64_t M, int64_t K, int count,
+                                           const uint8_t *const *wp, const float *w_scale,
+                                           const int64_t *N, float *const *out, int32_t *const *acc_out,
+                                           int8_t *xq, float *act_scale, int32_t *rowsum,
+                                           int prefetch_count, const void *const *prefetch_ptr,
+                                           const int64_t *prefetch_bytes, void *stream);
+
 /* bitnet_w2a8_linear -- bitnet_w2a8_linear_group with a single projection. */
 BITNET_API int bitnet_w2a8_linear(const void *x, int dtype, int64_t M, int64_t K, const uint8_t *wp,
                                   float w_scale, int64_t N, float *out, int32_t *acc_out, int8_t *xq,

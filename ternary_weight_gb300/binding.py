@@ -38,6 +38,9 @@ SIGNATURES = {
         [_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P], ctypes.c_int),
     "bitnet_w2a8_linear_group": (
         [_P, ctypes.c_int, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "bitnet_w2a8_linear_group_ex": (
+        [_P, ctypes.c_int, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P],
+        ctypes.c_int),
     "bitnet_w2a8_linear": (
         [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_float, _I64, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "bitnet_last_device_error": ([], ctypes.c_int),
@@ -158,11 +161,13 @@ def _act_dtype(x):
     raise ValueError("x must be float32 or bfloat16")
 
 
-def linear_group(x, wps, w_scales, outs=None, accs=None, xq=None, scale=None, rowsum=None, stream=None):
+def linear_group(x, wps, w_scales, outs=None, accs=None, xq=None, scale=None, rowsum=None, prefetch=None,
+                 stream=None):
     """Quantise x (M x K fp32/bf16) and multiply it with up to 8 packed projections sharing it.
 
-    One kernel launch when M == 1 (and K <= 10240); xq/scale/rowsum are then optional outputs.
-    Returns the list of M x N_l fp32 outputs."""
+    One kernel launch when M == 1; xq/scale/rowsum are then optional outputs. ``prefetch`` is
+    an optional list of CUDA tensors (e.g. the next group's packed weights) to pull into L2
+    while the kernel runs. Returns the list of M x N_l fp32 outputs."""
     import torch
 
     dt = _act_dtype(x)
@@ -180,8 +185,12 @@ def linear_group(x, wps, w_scales, outs=None, accs=None, xq=None, scale=None, ro
     acc_arr = P(*[(a.data_ptr() if a is not None else None) for a in accs]) if accs is not None else None
     ws_arr = (ctypes.c_float * n)(*[float(v) for v in w_scales])
     n_arr = (ctypes.c_int64 * n)(*[int(w.shape[0]) for w in wps])
-    _check(lib().bitnet_w2a8_linear_group(_ptr(x), dt, M, K, n, wp_arr, ws_arr, n_arr, out_arr, acc_arr,
-                                          _ptr(xq), _ptr(scale), _ptr(rowsum), _stream(stream)),
+    pf = list(prefetch or [])
+    pf_ptr = (ctypes.c_void_p * max(1, len(pf)))(*[t.data_ptr() for t in pf])
+    pf_bytes = (ctypes.c_int64 * max(1, len(pf)))(*[t.numel() * t.element_size() for t in pf])
+    _check(lib().bitnet_w2a8_linear_group_ex(_ptr(x), dt, M, K, n, wp_arr, ws_arr, n_arr, out_arr, acc_arr,
+                                             _ptr(xq), _ptr(scale), _ptr(rowsum), len(pf), pf_ptr, pf_bytes,
+                                             _stream(stream)),
            "bitnet_w2a8_linear_group")
     return outs
 

@@ -205,15 +205,22 @@ struct QuantOut {  // optional outputs of a fused quantisation (each may be null
   float* scale;
   int32_t* rowsum;
 };
+constexpr int kMaxPrefetch = 8;
+struct Prefetch {  // byte ranges to pull into L2 (a hint; 16-byte aligned starts)
+  const void* ptr[kMaxPrefetch];
+  int64_t bytes[kMaxPrefetch];
+  int count;
+};
 
 // ---------------------------------------------------------------------------------------
 // Launchers (defined in the kernel translation units). All return cudaError_t of the launch.
 // ---------------------------------------------------------------------------------------
-// M = 1 GEMV over a LinearSet. fuse: 0 = x is xq (int8) with act_scale and rowsum; 1 = x is
-// fp32, 2 = x is bf16 (quantised in the kernel, qout optionally written).
-bool gemv_m1_supported(int64_t K);
-cudaError_t launch_gemv_m1(const void* x, int fuse, const float* act_scale, const int32_t* rowsum,
-                           const LinearSet& set, const QuantOut& qout, int64_t K, int num_sms, cudaStream_t stream);
+// Single-token group step (gemv_group.cu): quantise x (fp32, or bf16 if bf16) and run the
+// GEMVs of a LinearSet in one launch; qout optionally written; pf an L2 prefetch hint.
+// Launched with programmatic stream serialisation.
+bool gemv_group_supported(int64_t K);
+cudaError_t launch_gemv_group(const void* x, bool bf16, const LinearSet& set, const QuantOut& qout,
+                              const Prefetch& pf, int64_t K, int num_sms, cudaStream_t stream);
 cudaError_t launch_pack_i2s(const int8_t* w, uint8_t* wp, int64_t N, int64_t K, int32_t* invalid_count,
                             cudaStream_t stream);
 cudaError_t launch_quant_act(const void* x, int dtype, int64_t M, int64_t K, int8_t* xq, float* act_scale,

@@ -120,23 +120,32 @@ BITNET_API int bitnet_i2s_matmul(const int8_t* xq, const float* act_scale, const
                                 stream);
 }
 
-BITNET_API int bitnet_w2a8_linear_group(const void* x, int dtype, int64_t M, int64_t K, int count,
-                                        const uint8_t* const* wp, const float* w_scale, const int64_t* N,
-                                        float* const* out, int32_t* const* acc_out, int8_t* xq, float* act_scale,
-                                        int32_t* rowsum, void* stream) {
+BITNET_API int bitnet_w2a8_linear_group_ex(const void* x, int dtype, int64_t M, int64_t K, int count,
+                                           const uint8_t* const* wp, const float* w_scale, const int64_t* N,
+                                           float* const* out, int32_t* const* acc_out, int8_t* xq, float* act_scale,
+                                           int32_t* rowsum, int prefetch_count, const void* const* prefetch_ptr,
+                                           const int64_t* prefetch_bytes, void* stream) {
   if (!x || !wp || !w_scale || !N || !out) return BITNET_EINVAL;
   if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_EINVAL;
   if (count < 1 || count > kMaxGroupLinears) return BITNET_EINVAL;
   if (M < 1 || M > INT32_MAX || !valid_k(K)) return BITNET_EINVAL;
+  if (prefetch_count < 0 || prefetch_count > kMaxPrefetch) return BITNET_EINVAL;
+  if (prefetch_count > 0 && (!prefetch_ptr || !prefetch_bytes)) return BITNET_EINVAL;
   if (!aligned(x, 16)) return BITNET_EALIGN;
-  int64_t total_rows = 0;
   for (int l = 0; l < count; ++l) {
     if (!wp[l] || !out[l] || N[l] < 1 || N[l] > INT32_MAX) return BITNET_EINVAL;
     if (!aligned(wp[l], 16) || !aligned(out[l], 4) || (acc_out && acc_out[l] && !aligned(acc_out[l], 4)))
       return BITNET_EALIGN;
-    total_rows += N[l];
   }
-  const bool single_launch = (M == 1 && gemv_m1_supported(K) && total_rows <= INT32_MAX);
+  Prefetch pf{};
+  for (int p = 0; p < prefetch_count; ++p) {
+    if (!prefetch_ptr[p] || prefetch_bytes[p] < 0) return BITNET_EINVAL;
+    if (!aligned(prefetch_ptr[p], 16)) return BITNET_EALIGN;
+    pf.ptr[p] = prefetch_ptr[p];
+    pf.bytes[p] = prefetch_bytes[p];
+  }
+  pf.count = prefetch_count;
+  const bool single_launch = (M == 1 && gemv_group_supported(K));
   if (!single_launch && (!xq || !act_scale || !rowsum)) return BITNET_EINVAL;
   if ((xq && !aligned(xq, 16)) || (act_scale && !aligned(act_scale, 4)) || (rowsum && !aligned(rowsum, 4)))
     return BITNET_EALIGN;
@@ -153,8 +162,7 @@ BITNET_API int bitnet_w2a8_linear_group(const void* x, int dtype, int64_t M, int
       set.N[l] = (int)N[l];
     }
     set.count = count;
-    return status_of(launch_gemv_m1(x, dtype == BITNET_BF16 ? 2 : 1, nullptr, nullptr, set,
-                                    QuantOut{xq, act_scale, rowsum}, K, sms, s));
+    return status_of(launch_gemv_group(x, dtype == BITNET_BF16, set, QuantOut{xq, act_scale, rowsum}, pf, K, sms, s));
   }
   if (cudaError_t e = launch_quant_act(x, dtype, M, K, xq, act_scale, rowsum, s)) return status_of(e);
   for (int l = 0; l < count; ++l) {
@@ -163,6 +171,14 @@ BITNET_API int bitnet_w2a8_linear_group(const void* x, int dtype, int64_t M, int
     if (st != BITNET_OK) return st;
   }
   return BITNET_OK;
+}
+
+BITNET_API int bitnet_w2a8_linear_group(const void* x, int dtype, int64_t M, int64_t K, int count,
+                                        const uint8_t* const* wp, const float* w_scale, const int64_t* N,
+                                        float* const* out, int32_t* const* acc_out, int8_t* xq, float* act_scale,
+                                        int32_t* rowsum, void* stream) {
+  return bitnet_w2a8_linear_group_ex(x, dtype, M, K, count, wp, w_scale, N, out, acc_out, xq, act_scale, rowsum, 0,
+                                     nullptr, nullptr, stream);
 }
 
 BITNET_API int bitnet_w2a8_linear(const void* x, int dtype, int64_t M, int64_t K, const uint8_t* wp, float w_scale,

@@ -1,0 +1,438 @@
+// gemv_group.cu -- single-token (M = 1) decode step of one projection group: the per-token
+// activation quantisation fused with the GEMVs of up to 8 projections that share the row.
+//
+// What it computes, per projection l and output row n:
+//   xq = clamp(rne(x * s), -127, 127),  s = 127 / max(max|x|, 1e-5),  rowsum = sum_k xq[k]
+//   raw = sum_k code_l[n][k] * xq[k]          codes 0/1/2 multiplied as stored
+//   out_l[n] = ((raw - rowsum) / s) * w_scale_l
+// Sources: "BitNet 딥다이브" §4-5 (per-token quant_input), §4-2 (i2_s layout), §4-3 (_Nx1: one
+// decoded activation set reused across weight rows); "[분석/검증-3] BitNet.cpp ARM 커널 재작성" §3
+// and "[기술 분석 보고서] ... 추론 붕괴 원인 분석" §3.1-§4 (raw code dot over the 4x32-interleaved
+// bytes); "bitnet.rs" "8-bit Activation Quantisation", "Quantised Forward Pass".
+//
+// Design: latency first (a decode step is a chain of such groups). One CTA per SM, small
+// enough (160 threads, ~106 KB of shared memory) that the CTA of the next group's kernel fits
+// beside it, so with programmatic dependent launch the next kernel starts streaming its
+// weights while this one finishes.
+//  * The group's projections are concatenated into one row space; CTA b owns a contiguous
+//    slice of it, cut into tiles of whole rows (<= 12 KB, never across two projections).
+//  * Warp 4 is the producer: one lane issues cp.async.bulk copies of consecutive tiles into an
+//    8-slot x 12 KB shared-memory ring, each slot completing on its own mbarrier by
+//    transaction bytes; then it hands the L2 prefetch hint (the next group's weights) to
+//    cp.async.bulk.prefetch.L2.
+//  * Programmatic dependent launch: the kernel lets the next kernel in the stream launch as
+//    soon as it starts, and streams its weights (read-only model state) before it waits for
+//    the previous kernel (griddepcontrol.wait); the activations are read and every output is
+//    written only after that wait.
+//  * Warps 0-3 are consumers; tile i goes to warp i % 4 (the slot count is a multiple of 4,
+//    so each slot belongs to one warp). They read the row once (fp32 or bf16), reduce
+//    max|x|, quantise every element once into shared memory laid out [j][c][16], reduce the
+//    row sum, and load the 64 activation bytes of each of their chunk columns c = kl + G*t
+//    into registers. Per 16-byte weight chunk: one conflict-free LDS.128, then per 32-bit word
+//    four masks (0xC0.., 0x30.., 0x0C.., 0x03..) and four dp4a (unsigned codes x signed int8)
+//    into accumulators holding exact multiples of 64/16/4/1. A tile holds up to 8 row steps;
+//    their partials are reduced over the G lanes together with a transpose-reduce, so the
+//    epilogue (one IEEE divide per output) runs on up to 8 lanes at once. CTA 0 also writes
+//    xq, s and the row sum when asked.
+//  * Every wait is bounded; a timeout is recorded in the device error word and the kernel
+//    leaves after waiting (bounded) for the copies it issued.
+#include "bitnet_dev.cuh"
+
+#include <atomic>
+
+namespace bitnet {
+
+static_assert(kMaxGroupLinears == 8, "LinearSet layout");
+
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + producer warp
+constexpr int kSlots = 8;
+constexpr int kSlotBytes = 12288;
+constexpr int kRingBytes = kSlots * kSlotBytes;
+constexpr int kMaxT = 5;                 // chunks per lane per row
+constexpr int kMaxK = 64 * 32 * kMaxT;   // largest K this kernel takes (10240)
+// Tile i lives in slot i % kSlots and is consumed by warp i % kConsumerWarps. With the slot
+// count a multiple of the consumer-warp count, every slot is only ever waited on by one
+// warp, in order, so a parity wait can never see a stale phase of its slot.
+static_assert(kSlots % kConsumerWarps == 0, "each ring slot must belong to one consumer warp");
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+__device__ __forceinline__ int quant1(float x, float s) {
+  return max(-127, min(127, __float2int_rn(__fmul_rn(x, s))));
+}
+
+// Geometry shared by producer and consumers.
+struct Geo {
+  int64_t row_bytes;
+  int64_t cta_begin, cta_end;  // concatenated row range of this CTA
+  int TR;                      // rows per tile
+};
+
+// The idx-th tile of this CTA: projection l, first row n0 (within l), row count.
+__device__ __forceinline__ bool tile_at(const LinearSet& set, const Geo& g, int idx, int& l, int64_t& n0,
+                                        int& rows) {
+  int64_t off = 0;
+  for (int j = 0; j < set.count; ++j) {
+    const int64_t lo = max(off, g.cta_begin), hi = min(off + (int64_t)set.N[j], g.cta_end);
+    if (hi > lo) {
+      const int64_t cnt = (hi - lo + g.TR - 1) / g.TR;
+      if (idx < cnt) {
+        l = j;
+        n0 = lo - off + (int64_t)idx * g.TR;
+        rows = (int)min((int64_t)g.TR, hi - (lo + (int64_t)idx * g.TR));
+        return true;
+      }
+      idx -= (int)cnt;
+    }
+    off += set.N[j];
+  }
+  return false;
+}
+
+// BF16: x is bf16 (else fp32).
+template <int T, bool BF16>
+__global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __restrict__ xin, LinearSet set,
+                                                                 QuantOut qout, Prefetch pf, int K, int log2G,
+                                                                 int S) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;                      // kSlots x kSlotBytes
+  uint8_t* xq_s = smem + kRingBytes;         // K bytes, [j][c][16]
+  __shared__ __align__(8) uint64_t full_bar[kSlots];
+  __shared__ __align__(8) uint64_t empty_bar[kSlots];
+  __shared__ float red_f[kConsumerWarps];
+  __shared__ int red_i[kConsumerWarps];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = K >> 6;
+  Geo geo;
+  geo.row_bytes = K >> 2;
+  int64_t total = 0;
+  for (int j = 0; j < set.count; ++j) total += set.N[j];
+  geo.cta_begin = total * blockIdx.x / gridDim.x;
+  geo.cta_end = total * (blockIdx.x + 1) / gridDim.x;
+  geo.TR = S << (5 - log2G);  // rows per tile = steps x rows per step
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  bool abort = false;
+
+  if (warp == kConsumerWarps) {
+    // ================================ producer ================================
+    if (lane == 0) {
+      int issued = 0;
+      bool prefetched = false;
+      for (int i = 0;; ++i) {
+        int l, rows;
+        int64_t n0;
+        if (!tile_at(set, geo, i, l, n0, rows)) break;
+        const int slot = i % kSlots, use = i / kSlots;
+        if (use > 0 && !mbar_wait(&empty_bar[slot], (use - 1) & 1, &abort)) break;
+        const uint32_t bytes = (uint32_t)(rows * geo.row_bytes);
+        mbar_arrive_expect_tx(&full_bar[slot], bytes);
+        bulk_copy_g2s(ring + slot * kSlotBytes, set.wp[l] + n0 * geo.row_bytes, bytes, &full_bar[slot]);
+        issued = i + 1;
+        if (!prefetched && (i + 1 == kSlots || !tile_at(set, geo, i + 1, l, n0, rows))) {
+          // ring primed (or all issued): now the prefetch hint, CTA b taking slice b of each range
+          for (int p = 0; p < pf.count; ++p) {
+            const int64_t n16 = pf.bytes[p] >> 4;
+            int64_t lo = n16 * blockIdx.x / gridDim.x * 16, hi = n16 * (blockIdx.x + 1) / gridDim.x * 16;
+            const char* base = static_cast<const char*>(pf.ptr[p]);
+            while (lo < hi) {
+              const int64_t len = (hi - lo) < (1 << 16) ? (hi - lo) : (1 << 16);
+              prefetch_l2(base + lo, (uint32_t)len);
+              lo += len;
+            }
+          }
+          prefetched = true;
+        }
+      }
+      if (abort) {  // let every copy this CTA issued land before the CTA can exit
+        bool dummy = false;
+        for (int i = issued - kSlots > 0 ? issued - kSlots : 0; i < issued; ++i)
+          mbar_wait(&full_bar[i % kSlots], (i / kSlots) & 1, &dummy);
+      }
+    }
+    return;
+  }
+
+  // ================================ consumers ================================
+  const int G = 1 << log2G;
+  const int kl = lane & (G - 1);
+  const int rg = lane >> log2G;
+  const int rpw = 32 >> log2G;
+
+  uint32_t a[T][4][4];  // [t][j][word]: the 16 activation bytes paired with bit pair j of chunk t
+  float s_act;
+  int rs_total;
+  pdl_wait();  // the activations may be the previous kernel's output
+  {
+    constexpr int E = BF16 ? 8 : 4;  // elements per 16-byte vector
+    const uint4* xv = static_cast<const uint4*>(xin);
+    const int nvec = K / E;
+    float amax = 0.0f;
+    for (int v = threadIdx.x; v < nvec; v += kConsumers) {
+      const uint4 u = __ldg(xv + v);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if constexpr (BF16) {
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[i] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[i] & 0xFFFF0000u)));
+        } else {
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[i])));
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red_f[warp] = amax;
+    named_bar_sync(1, kConsumers);
+    amax = red_f[0];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, red_f[w]);
+    s_act = __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
+    // quantise every element once; element k goes to [j][c][16] with
+    // c = 2*(k/128) + (k%32)/16, j = (k%128)/32
+    const int plane = K >> 2;
+    int sum = 0;
+    const bool publish = blockIdx.x == 0 && qout.xq != nullptr;
+    for (int v = threadIdx.x; v < nvec; v += kConsumers) {
+      const uint4 u = __ldg(xv + v);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+      int q[E];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if constexpr (BF16) {
+          q[2 * i] = quant1(__uint_as_float(w4[i] << 16), s_act);
+          q[2 * i + 1] = quant1(__uint_as_float(w4[i] & 0xFFFF0000u), s_act);
+        } else {
+          q[i] = quant1(__uint_as_float(w4[i]), s_act);
+        }
+      }
+      const int k = v * E;
+      const int rem = k & 127;
+      const int off = (rem >> 5) * plane + (2 * (k >> 7) + ((rem & 31) >> 4)) * 16 + (rem & 15);
+      uint32_t word0 = 0, word1 = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        word0 |= (uint32_t)(q[b] & 0xFF) << (8 * b);
+        sum += q[b];
+      }
+      if constexpr (BF16) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          word1 |= (uint32_t)(q[4 + b] & 0xFF) << (8 * b);
+          sum += q[4 + b];
+        }
+        *reinterpret_cast<uint2*>(xq_s + off) = make_uint2(word0, word1);
+        if (publish) *reinterpret_cast<uint2*>(qout.xq + k) = make_uint2(word0, word1);
+      } else {
+        *reinterpret_cast<uint32_t*>(xq_s + off) = word0;
+        if (publish) *reinterpret_cast<uint32_t*>(qout.xq + k) = word0;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) red_i[warp] = sum;
+    named_bar_sync(1, kConsumers);
+    rs_total = 0;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) rs_total += red_i[w];
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      if (qout.scale) *qout.scale = s_act;
+      if (qout.rowsum) *qout.rowsum = rs_total;
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const int c = kl + (t << log2G);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (c < C) v = *reinterpret_cast<const uint4*>(xq_s + j * plane + c * 16);
+        a[t][j][0] = v.x;
+        a[t][j][1] = v.y;
+        a[t][j][2] = v.z;
+        a[t][j][3] = v.w;
+      }
+    }
+  }
+
+  // ---- consume this warp's tiles: a tile is S steps of rpw rows; step s of row group rg is
+  // row s*rpw + rg. Each lane keeps one partial per step; a transpose-reduce over the G lanes
+  // (three halving levels, then plain xor levels) leaves the total of step s in the lanes
+  // whose top three lane-in-group bits spell s, so the epilogue (one IEEE divide per output)
+  // runs for up to 8 rows in parallel. ----
+  const int hb = (G >= 8) ? log2G - 3 : 0;  // low lane bits left after the halving levels
+  for (int i = warp;; i += kConsumerWarps) {
+    int l, rows;
+    int64_t n0;
+    if (!tile_at(set, geo, i, l, n0, rows)) break;
+    const int slot = i % kSlots, use = i / kSlots;
+    if (!mbar_wait(&full_bar[slot], use & 1, &abort)) break;
+    const uint8_t* tile = ring + slot * kSlotBytes;
+    int v[8];
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      v[st] = 0;
+      if (st < S) {
+        const int rr = st * rpw + rg;
+        const bool rv = rr < rows;
+        const uint8_t* rowp = tile + (rv ? rr : 0) * geo.row_bytes;
+        int acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const int c = kl + (t << log2G);
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (rv && c < C) w = *reinterpret_cast<const uint4*>(rowp + c * 16);
+          const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc0 = dp4a_us(w4[q] & 0xC0C0C0C0u, a[t][0][q], acc0);
+            acc1 = dp4a_us(w4[q] & 0x30303030u, a[t][1][q], acc1);
+            acc2 = dp4a_us(w4[q] & 0x0C0C0C0Cu, a[t][2][q], acc2);
+            acc3 = dp4a_us(w4[q] & 0x03030303u, a[t][3][q], acc3);
+          }
+        }
+        v[st] = (acc0 >> 6) + (acc1 >> 4) + (acc2 >> 2) + acc3;
+      }
+    }
+    int mine_step = 0;
+    bool writer = kl == 0;
+    if (G >= 8) {
+      bool up = (kl >> (log2G - 1)) & 1;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int send = up ? v[k] : v[k + 4], keep = up ? v[k + 4] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, G >> 1);
+      }
+      const bool up2 = (kl >> (log2G - 2)) & 1;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int send = up2 ? v[k] : v[k + 2], keep = up2 ? v[k + 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, G >> 2);
+      }
+      const bool up3 = (kl >> (log2G - 3)) & 1;
+      {
+        const int send = up3 ? v[0] : v[1], keep = up3 ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, G >> 3);
+      }
+      for (int o = (G >> 4); o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+      mine_step = (up ? 4 : 0) + (up2 ? 2 : 0) + (up3 ? 1 : 0);
+      writer = (kl & ((1 << hb) - 1)) == 0;
+    } else {
+      for (int o = G >> 1; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+    const int rr = mine_step * rpw + rg;
+    if (writer && mine_step < S && rr < rows) {
+      const int64_t n = n0 + rr;
+      const int acc = v[0] - rs_total;
+      set.out[l][n] = __fmul_rn(__fdiv_rn(__int2float_rn(acc), s_act), set.w_scale[l]);
+      if (set.acc[l]) set.acc[l][n] = acc;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);
+  }
+}
+
+// lanes per row: the largest power of two <= 32 dividing C when that keeps T <= 5 chunks per
+// lane, else 32 lanes with a ragged last column (predicated).
+void choose_layout(int K, int& log2G, int& T) {
+  const int C = K >> 6;
+  log2G = 5;
+  while (log2G > 1 && (C & ((1 << log2G) - 1)) != 0) --log2G;
+  T = C >> log2G;
+  if (T > kMaxT) {
+    log2G = 5;
+    T = (C + 31) >> 5;
+  }
+}
+
+template <int T, bool BF16>
+cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
+                     int num_sms, cudaStream_t stream) {
+  auto kern = gemv_group_kernel<T, BF16>;
+  const int smem = kRingBytes + K;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes + kMaxK);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  int64_t total = 0;
+  for (int j = 0; j < set.count; ++j) total += set.N[j];
+  const int rpw = 32 >> log2G;
+  const int64_t step_bytes = (int64_t)(K >> 2) * rpw;
+  // steps per tile: at most 8 (one partial register each), the tile within one ring slot
+  // (K <= 10240 keeps one step within 2560 bytes), 1 when fewer than 8 lanes share a row, and
+  // no more than a consumer warp's share of the CTA's rows
+  int blocks = num_sms;
+  if (total < blocks) blocks = (int)total;
+  const int64_t per_cta = (total + blocks - 1) / blocks;
+  int64_t S = (log2G >= 3) ? kSlotBytes / step_bytes : 1;
+  if (S > 8) S = 8;
+  if (S < 1) S = 1;
+  const int64_t want = ((per_cta + kConsumerWarps - 1) / kConsumerWarps + rpw - 1) / rpw;
+  if (S > want) S = want < 1 ? 1 : want;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, x, set, q, pf, K, log2G, (int)S);
+}
+
+template <bool BF16>
+cudaError_t launch_dtype(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K,
+                         int num_sms, cudaStream_t stream) {
+  int log2G, T;
+  choose_layout(K, log2G, T);
+  switch (T) {
+    case 1: return launch_t<1, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
+    case 2: return launch_t<2, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
+    case 3: return launch_t<3, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
+    case 4: return launch_t<4, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
+    case 5: return launch_t<5, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool gemv_group_supported(int64_t K) {
+  if (K > kMaxK) return false;
+  int log2G, T;
+  choose_layout((int)K, log2G, T);
+  return T <= kMaxT;
+}
+
+cudaError_t launch_gemv_group(const void* x, bool bf16, const LinearSet& set, const QuantOut& qout,
+                              const Prefetch& pf, int64_t K, int num_sms, cudaStream_t stream) {
+  return bf16 ? launch_dtype<true>(x, set, qout, pf, (int)K, num_sms, stream)
+              : launch_dtype<false>(x, set, qout, pf, (int)K, num_sms, stream);
+}
+
+}  // namespace bitnet

@@ -1,5 +1,4 @@
-// gemv_i2s.cu -- decode GEMV (small M > 1; M = 1 goes to gemv_m1.cu): i2_s packed ternary
-// weights x int8 activations.
+// gemv_i2s.cu -- decode GEMV (small M): i2_s packed ternary weights x int8 activations.
 //
 // What it computes (per output (m, n)):
 //   raw = sum_k code[n][k] * xq[m][k]       codes 0/1/2 multiplied as stored
@@ -22,8 +21,9 @@
 //    [m][j][c][16 bytes] so that the 16 activation bytes paired with bit pair j of chunk c
 //    are one conflict-free 16-byte load, shared by the R weight rows a lane handles.
 //  * A warp works on a tile of (32/G)*R rows: G lanes per row group walk the row's chunks
-//    (c = lane_in_group + G*t; G is the largest power of two <= 32 dividing C, so no lane
-//    idles), each lane owning R rows. Weight chunks are streamed with 128-bit
+//    (c = lane_in_group + G*t; G is the largest power of two <= 32 dividing C while that keeps
+//    the walk at most 5 chunks, else 32 with a predicated ragged last chunk), each lane owning
+//    R rows. Weight chunks are streamed with 128-bit
 //    non-allocating loads, one chunk ahead (2*R loads in flight per lane). Partial sums
 //    are reduced with xor-shuffles inside the G-lane group.
 #include "bitnet_dev.cuh"
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
   const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
   if (tile * rows_per_tile >= N) return;  // warp-uniform; no block barrier follows
   const int64_t nbase = tile * rows_per_tile + (int64_t)rg * R;
-  const int T = C >> log2G;  // chunks per lane per row
+  const int T = (C + G - 1) >> log2G;  // chunks per lane per row (the last may be ragged)
 
   const uint4* wrow[R];
   bool rv[R];
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
 
   uint4 cur[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) cur[r] = rv[r] ? ldg_stream(wrow[r] + kl) : make_uint4(0u, 0u, 0u, 0u);
+  for (int r = 0; r < R; ++r) cur[r] = (rv[r] && kl < C) ? ldg_stream(wrow[r] + kl) : make_uint4(0u, 0u, 0u, 0u);
 
   for (int t = 0; t < T; ++t) {
     const int c = kl + (t << log2G);
@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
     if (t + 1 < T) {
 #pragma unroll
       for (int r = 0; r < R; ++r)
-        nxt[r] = rv[r] ? ldg_stream(wrow[r] + c + G) : make_uint4(0u, 0u, 0u, 0u);
+        nxt[r] = (rv[r] && c + G < C) ? ldg_stream(wrow[r] + c + G) : make_uint4(0u, 0u, 0u, 0u);
     }
+    if (c < C) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
 #pragma unroll
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
           acc[r][m][j] = s;
         }
       }
+    }
     }
     if (t + 1 < T) {
 #pragma unroll
@@ -179,19 +181,12 @@ cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int3
                             float w_scale, float* out, int32_t* acc_out, int64_t M64, int64_t N64, int64_t K64,
                             int num_sms, cudaStream_t stream) {
   const int M = (int)M64, N = (int)N64, K = (int)K64;
-  if (M == 1 && gemv_m1_supported(K)) {
-    LinearSet set{};
-    set.wp[0] = wp;
-    set.out[0] = out;
-    set.acc[0] = acc_out;
-    set.w_scale[0] = w_scale;
-    set.N[0] = N;
-    set.count = 1;
-    return launch_gemv_m1(xq, 0, act_scale, rowsum, set, QuantOut{nullptr, nullptr, nullptr}, K, num_sms, stream);
-  }
   const int C = K >> 6;
+  // lanes per row: the largest power of two <= 32 dividing C while that keeps at most 5 chunks
+  // per lane, else 32 lanes with a ragged (predicated) last chunk
   int log2G = 5;
   while (log2G > 1 && (C & ((1 << log2G) - 1)) != 0) --log2G;  // C is even, so G >= 2 divides it
+  if ((C >> log2G) > 5) log2G = 5;
   const int rpw = 32 >> log2G;
 
   // activation rows per CTA: next power of two >= M, at most 8, within the smem budget

@@ -53,9 +53,10 @@ class TernaryStack:
     """Groups of ternary projections executed in order, as one CUDA graph per step."""
 
     def __init__(self, groups: Sequence[Group], M: int = 1, act_dtype=torch.float32, device="cuda",
-                 algo: str = "auto", fused: bool = True):
+                 algo: str = "auto", fused: bool = True, prefetch_next: bool = True):
         self.groups = list(groups)
         self.fused = fused
+        self.prefetch_next = prefetch_next
         self.M = M
         self.act_dtype = act_dtype
         self.device = torch.device(device)
@@ -111,15 +112,19 @@ class TernaryStack:
         """Enqueue one step (quantise each group's row, then its GEMVs) on the stream.
 
         fused (default): one bitnet_w2a8_linear_group call per group -- quantisation and every
-        projection of the group in a single kernel when M == 1. Otherwise (or with gemv_only,
-        which leaves out the quantisation) one quantisation launch per group and one
-        bitnet_i2s_matmul launch per projection."""
+        projection of the group in a single kernel when M == 1 -- which also pulls the next
+        group's packed weights into L2 while it runs (prefetch_next; the last group prefetches
+        the first, for the next step). Otherwise (or with gemv_only, which leaves out the
+        quantisation) one quantisation launch per group and one bitnet_i2s_matmul launch per
+        projection."""
         for gi, g in enumerate(self.groups):
             if self.fused and not gemv_only:
                 single = self.M == 1
+                nxt = self.groups[(gi + 1) % len(self.groups)]
                 binding.linear_group(self.x[gi], [l.wp for l in g.linears], [l.w_scale for l in g.linears],
                                      outs=self.out[gi], xq=None if single else self.xq[gi],
                                      scale=None if single else self.s[gi], rowsum=None if single else self.rs[gi],
+                                     prefetch=[l.wp for l in nxt.linears] if self.prefetch_next else None,
                                      stream=stream)
                 continue
             if not gemv_only:

@@ -125,9 +125,26 @@ def _group(lib, x=FAKE, dtype=0, M=1, K=128, count=1, wp=(FAKE,), ws=(1.0,), N=(
 @pytest.mark.parametrize("kw,status", [
     (dict(x=None), -1), (dict(dtype=5), -1), (dict(count=0), -1), (dict(count=9), -1), (dict(M=0), -1),
     (dict(K=200), -1), (dict(wp=None), -1), (dict(out=None), -1), (dict(wp=(0,)), -1), (dict(N=(0,)), -1),
-    (dict(M=2), -1), (dict(K=16384), -1),                       # workspace required beyond one launch
+    (dict(M=2), -1),                                            # workspace required beyond one launch
     (dict(x=FAKE + 4), -2), (dict(wp=(FAKE + 8,)), -2), (dict(out=(FAKE + 2,)), -2),
     (dict(acc=(FAKE + 1,)), -2), (dict(xq=FAKE + 8), -2),
 ])
 def test_linear_group_rejects_bad_arguments_on_host(lib, kw, status):
     assert _group(lib, **kw) == status
+
+
+def test_linear_group_ex_rejects_bad_prefetch(lib):
+    wp = (ctypes.c_void_p * 1)(FAKE)
+    out = (ctypes.c_void_p * 1)(FAKE)
+    ws = (ctypes.c_float * 1)(1.0)
+    n = (ctypes.c_int64 * 1)(1)
+    call = lambda cnt, ptrs, sizes: lib.bitnet_w2a8_linear_group_ex(FAKE, 0, 1, 128, 1, wp, ws, n, out, None, None,
+                                                                    None, None, cnt, ptrs, sizes, None)
+    P = ctypes.c_void_p * 2
+    B = ctypes.c_int64 * 2
+    assert call(9, P(FAKE, FAKE), B(16, 16)) == -1
+    assert call(-1, P(FAKE, FAKE), B(16, 16)) == -1
+    assert call(1, None, B(16, 16)) == -1
+    assert call(1, P(0, 0), B(16, 16)) == -1
+    assert call(1, P(FAKE, 0), B(-16, 16)) == -1
+    assert call(1, P(FAKE + 4, 0), B(16, 16)) == -2

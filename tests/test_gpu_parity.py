@@ -339,3 +339,15 @@ def test_stack_fused_equals_unfused():
         torch.cuda.synchronize()
         outs.append(host(st.out_all))
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+def test_linear_group_prefetch_hint_changes_nothing():
+    K, Ns = 2560, [6912, 6912]
+    x = workloads.activations(1, K, seed=880, dtype="f32")
+    wps = [binding.pack_i2s(dev(workloads.ternary_weights(N, K, seed=881 + i))) for i, N in enumerate(Ns)]
+    other = [binding.pack_i2s(dev(workloads.ternary_weights(2560, 6912, seed=883)))]
+    a = binding.linear_group(dev(x), wps, [0.02, 0.03])
+    b = binding.linear_group(dev(x), wps, [0.02, 0.03], prefetch=other + wps)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert np.array_equal(host(u).view(np.uint32), host(v).view(np.uint32))
