@@ -11,12 +11,12 @@
 // bytes); "bitnet.rs" "8-bit Activation Quantisation", "Quantised Forward Pass".
 //
 // Design: latency first (a decode step is a chain of such groups). One CTA per SM, small
-// enough (160 threads, ~106 KB of shared memory) that the CTA of the next group's kernel fits
-// beside it, so with programmatic dependent launch the next kernel starts streaming its
-// weights while this one finishes.
+// enough (288 threads at <= 113 registers, ~106 KB of shared memory) that the CTA of the next
+// group's kernel fits beside it, so with programmatic dependent launch the next kernel starts
+// streaming its weights while this one finishes.
 //  * The group's projections are concatenated into one row space; CTA b owns a contiguous
 //    slice of it, cut into tiles of whole rows (<= 12 KB, never across two projections).
-//  * Warp 4 is the producer: one lane issues cp.async.bulk copies of consecutive tiles into an
+//  * Warp 8 is the producer: one lane issues cp.async.bulk copies of consecutive tiles into an
 //    8-slot x 12 KB shared-memory ring, each slot completing on its own mbarrier by
 //    transaction bytes; then it hands the L2 prefetch hint (the next group's weights) to
 //    cp.async.bulk.prefetch.L2.
@@ -24,16 +24,18 @@
 //    soon as it starts, and streams its weights (read-only model state) before it waits for
 //    the previous kernel (griddepcontrol.wait); the activations are read and every output is
 //    written only after that wait.
-//  * Warps 0-3 are consumers; tile i goes to warp i % 4 (the slot count is a multiple of 4,
-//    so each slot belongs to one warp). They read the row once (fp32 or bf16), reduce
-//    max|x|, quantise every element once into shared memory laid out [j][c][16], reduce the
-//    row sum, and load the 64 activation bytes of each of their chunk columns c = kl + G*t
-//    into registers. Per 16-byte weight chunk: one conflict-free LDS.128, then per 32-bit word
-//    four masks (0xC0.., 0x30.., 0x0C.., 0x03..) and four dp4a (unsigned codes x signed int8)
-//    into accumulators holding exact multiples of 64/16/4/1. A tile holds up to 8 row steps;
-//    their partials are reduced over the G lanes together with a transpose-reduce, so the
-//    epilogue (one IEEE divide per output) runs on up to 8 lanes at once. CTA 0 also writes
-//    xq, s and the row sum when asked.
+//  * Warps 0-7 are consumers; tile i goes to warp i % 8 (the slot count is a multiple of 8,
+//    so each slot belongs to one warp). They read the row once into registers (fp32 or bf16),
+//    reduce max|x|, quantise every element once into shared memory laid out [j][c][16] and
+//    reduce the row sum. Lane kl of a G-lane row group owns chunk columns c = kl + G*t; per
+//    column it loads the 64 paired activation bytes (four conflict-free LDS.128) and applies
+//    them to up to 8 row steps of the tile: per 16-byte weight chunk one LDS.128, then per
+//    32-bit word w four masked operands (w & 0xC0.., (w<<2) & 0xC0.., w & 0x0C..,
+//    (w<<2) & 0x0C..) and four dp4a (unsigned codes x signed int8) into two accumulators that
+//    hold exact multiples of 64 and 4. The steps' partials
+//    are reduced over the G lanes together with a transpose-reduce, so the epilogue (one IEEE
+//    divide per output) runs on up to 8 lanes at once. CTA 0 also writes xq, s and the row
+//    sum when asked.
 //  * Every wait is bounded; a timeout is recorded in the device error word and the kernel
 //    leaves after waiting (bounded) for the copies it issued.
 #include "bitnet_dev.cuh"
@@ -46,14 +48,18 @@ static_assert(kMaxGroupLinears == 8, "LinearSet layout");
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + producer warp
 constexpr int kSlots = 8;
 constexpr int kSlotBytes = 12288;
 constexpr int kRingBytes = kSlots * kSlotBytes;
-constexpr int kMaxT = 5;                 // chunks per lane per row
-constexpr int kMaxK = 64 * 32 * kMaxT;   // largest K this kernel takes (10240)
+constexpr int kMaxK = 10240;            // largest K this kernel takes
+// the activation row passes through the consumers as 16-byte vectors, at most
+// kMaxVecPerThread per thread; the first kRegVec of them stay in registers between the max
+// and the quantise pass (all of them for K <= 6144 fp32 / 12288 bf16), the rest are re-read
+constexpr int kMaxVecPerThread = kMaxK / 4 / (kConsumerWarps * 32);
+constexpr int kRegVec = 6;
 // Tile i lives in slot i % kSlots and is consumed by warp i % kConsumerWarps. With the slot
 // count a multiple of the consumer-warp count, every slot is only ever waited on by one
 // warp, in order, so a parity wait can never see a stale phase of its slot.
@@ -98,7 +104,7 @@ __device__ __forceinline__ bool tile_at(const LinearSet& set, const Geo& g, int 
 }
 
 // BF16: x is bf16 (else fp32).
-template <int T, bool BF16>
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __restrict__ xin, LinearSet set,
                                                                  QuantOut qout, Prefetch pf, int K, int log2G,
                                                                  int S) {
@@ -175,26 +181,32 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   const int kl = lane & (G - 1);
   const int rg = lane >> log2G;
   const int rpw = 32 >> log2G;
+  const int T = (C + G - 1) >> log2G;  // chunk columns per lane (the last may be ragged)
+  const int plane = K >> 2;
 
-  uint32_t a[T][4][4];  // [t][j][word]: the 16 activation bytes paired with bit pair j of chunk t
   float s_act;
   int rs_total;
   pdl_wait();  // the activations may be the previous kernel's output
   {
+    // the row is read once into registers: vector v = threadIdx.x + kConsumers * i
     constexpr int E = BF16 ? 8 : 4;  // elements per 16-byte vector
     const uint4* xv = static_cast<const uint4*>(xin);
     const int nvec = K / E;
+    uint4 xr[kRegVec];
     float amax = 0.0f;
-    for (int v = threadIdx.x; v < nvec; v += kConsumers) {
-      const uint4 u = __ldg(xv + v);
+#pragma unroll
+    for (int i = 0; i < kMaxVecPerThread; ++i) {
+      const int v = threadIdx.x + kConsumers * i;
+      const uint4 u = v < nvec ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+      if (i < kRegVec) xr[i] = u;
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int e = 0; e < 4; ++e) {
         if constexpr (BF16) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[i] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[i] & 0xFFFF0000u)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] & 0xFFFF0000u)));
         } else {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[i])));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[e])));
         }
       }
     }
@@ -206,50 +218,53 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
 #pragma unroll
     for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, red_f[w]);
     s_act = __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
-    // quantise every element once; element k goes to [j][c][16] with
+    // quantise each element once; element k goes to [j][c][16] with
     // c = 2*(k/128) + (k%32)/16, j = (k%128)/32
-    const int plane = K >> 2;
     int sum = 0;
     const bool publish = blockIdx.x == 0 && qout.xq != nullptr;
-    for (int v = threadIdx.x; v < nvec; v += kConsumers) {
-      const uint4 u = __ldg(xv + v);
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-      int q[E];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if constexpr (BF16) {
-          q[2 * i] = quant1(__uint_as_float(w4[i] << 16), s_act);
-          q[2 * i + 1] = quant1(__uint_as_float(w4[i] & 0xFFFF0000u), s_act);
-        } else {
-          q[i] = quant1(__uint_as_float(w4[i]), s_act);
+    for (int i = 0; i < kMaxVecPerThread; ++i) {
+      const int v = threadIdx.x + kConsumers * i;
+      if (v < nvec) {
+        const uint4 u = i < kRegVec ? xr[i] : __ldg(xv + v);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+        int q[E];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (BF16) {
+            q[2 * e] = quant1(__uint_as_float(w4[e] << 16), s_act);
+            q[2 * e + 1] = quant1(__uint_as_float(w4[e] & 0xFFFF0000u), s_act);
+          } else {
+            q[e] = quant1(__uint_as_float(w4[e]), s_act);
+          }
         }
-      }
-      const int k = v * E;
-      const int rem = k & 127;
-      const int off = (rem >> 5) * plane + (2 * (k >> 7) + ((rem & 31) >> 4)) * 16 + (rem & 15);
-      uint32_t word0 = 0, word1 = 0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        word0 |= (uint32_t)(q[b] & 0xFF) << (8 * b);
-        sum += q[b];
-      }
-      if constexpr (BF16) {
+        const int k = v * E;
+        const int rem = k & 127;
+        const int off = (rem >> 5) * plane + (2 * (k >> 7) + ((rem & 31) >> 4)) * 16 + (rem & 15);
+        uint32_t word0 = 0, word1 = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          word1 |= (uint32_t)(q[4 + b] & 0xFF) << (8 * b);
-          sum += q[4 + b];
+          word0 |= (uint32_t)(q[b] & 0xFF) << (8 * b);
+          sum += q[b];
         }
-        *reinterpret_cast<uint2*>(xq_s + off) = make_uint2(word0, word1);
-        if (publish) *reinterpret_cast<uint2*>(qout.xq + k) = make_uint2(word0, word1);
-      } else {
-        *reinterpret_cast<uint32_t*>(xq_s + off) = word0;
-        if (publish) *reinterpret_cast<uint32_t*>(qout.xq + k) = word0;
+        if constexpr (BF16) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            word1 |= (uint32_t)(q[4 + b] & 0xFF) << (8 * b);
+            sum += q[4 + b];
+          }
+          *reinterpret_cast<uint2*>(xq_s + off) = make_uint2(word0, word1);
+          if (publish) *reinterpret_cast<uint2*>(qout.xq + k) = make_uint2(word0, word1);
+        } else {
+          *reinterpret_cast<uint32_t*>(xq_s + off) = word0;
+          if (publish) *reinterpret_cast<uint32_t*>(qout.xq + k) = word0;
+        }
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) red_i[warp] = sum;
-    named_bar_sync(1, kConsumers);
+    named_bar_sync(1, kConsumers);  // also orders the shared activation writes before the reads
     rs_total = 0;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) rs_total += red_i[w];
@@ -257,26 +272,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
       if (qout.scale) *qout.scale = s_act;
       if (qout.rowsum) *qout.rowsum = rs_total;
     }
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const int c = kl + (t << log2G);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c < C) v = *reinterpret_cast<const uint4*>(xq_s + j * plane + c * 16);
-        a[t][j][0] = v.x;
-        a[t][j][1] = v.y;
-        a[t][j][2] = v.z;
-        a[t][j][3] = v.w;
-      }
-    }
   }
 
-  // ---- consume this warp's tiles: a tile is S steps of rpw rows; step s of row group rg is
-  // row s*rpw + rg. Each lane keeps one partial per step; a transpose-reduce over the G lanes
-  // (three halving levels, then plain xor levels) leaves the total of step s in the lanes
-  // whose top three lane-in-group bits spell s, so the epilogue (one IEEE divide per output)
-  // runs for up to 8 rows in parallel. ----
+  // ---- consume this warp's tiles: a tile is S steps of rpw rows; step st of row group rg is
+  // row st*rpw + rg. For each chunk column the lane loads the 64 paired activation bytes from
+  // shared memory once and applies them to all S steps, keeping four bit-pair accumulators
+  // per step. A transpose-reduce over the G lanes (three halving levels, then plain xor
+  // levels) leaves the total of step st in the lanes whose top three lane-in-group bits spell
+  // st, so the epilogue (one IEEE divide per output) runs for up to 8 rows in parallel. ----
   const int hb = (G >= 8) ? log2G - 3 : 0;  // low lane bits left after the halving levels
   for (int i = warp;; i += kConsumerWarps) {
     int l, rows;
@@ -285,36 +288,46 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     const int slot = i % kSlots, use = i / kSlots;
     if (!mbar_wait(&full_bar[slot], use & 1, &abort)) break;
     const uint8_t* tile = ring + slot * kSlotBytes;
-    int v[8];
+    // per step: hi = 64 * (sum of bit pairs 0 and 1), lo = 4 * (sum of bit pairs 2 and 3);
+    // shifting the weight word left by 2 puts pair 1 under pair 0's mask and pair 3 under
+    // pair 2's, so one accumulator serves two pairs at the same scale
+    int acc[8][2];
 #pragma unroll
-    for (int st = 0; st < 8; ++st) {
-      v[st] = 0;
-      if (st < S) {
+    for (int st = 0; st < 8; ++st) acc[st][0] = acc[st][1] = 0;
+    for (int t = 0; t < T; ++t) {
+      const int c = kl + (t << log2G);
+      if (c >= C) continue;
+      uint4 a[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const uint4*>(xq_s + j * plane + c * 16);
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
         const int rr = st * rpw + rg;
-        const bool rv = rr < rows;
-        const uint8_t* rowp = tile + (rv ? rr : 0) * geo.row_bytes;
-        int acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          const int c = kl + (t << log2G);
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (rv && c < C) w = *reinterpret_cast<const uint4*>(rowp + c * 16);
+        if (st < S && rr < rows) {
+          const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * geo.row_bytes + c * 16);
           const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+          const uint32_t a0[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
+          const uint32_t a1[4] = {a[1].x, a[1].y, a[1].z, a[1].w};
+          const uint32_t a2[4] = {a[2].x, a[2].y, a[2].z, a[2].w};
+          const uint32_t a3[4] = {a[3].x, a[3].y, a[3].z, a[3].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            acc0 = dp4a_us(w4[q] & 0xC0C0C0C0u, a[t][0][q], acc0);
-            acc1 = dp4a_us(w4[q] & 0x30303030u, a[t][1][q], acc1);
-            acc2 = dp4a_us(w4[q] & 0x0C0C0C0Cu, a[t][2][q], acc2);
-            acc3 = dp4a_us(w4[q] & 0x03030303u, a[t][3][q], acc3);
+            const uint32_t sh = w4[q] << 2;
+            acc[st][0] = dp4a_us(w4[q] & 0xC0C0C0C0u, a0[q], acc[st][0]);
+            acc[st][0] = dp4a_us(sh & 0xC0C0C0C0u, a1[q], acc[st][0]);
+            acc[st][1] = dp4a_us(w4[q] & 0x0C0C0C0Cu, a2[q], acc[st][1]);
+            acc[st][1] = dp4a_us(sh & 0x0C0C0C0Cu, a3[q], acc[st][1]);
           }
         }
-        v[st] = (acc0 >> 6) + (acc1 >> 4) + (acc2 >> 2) + acc3;
       }
     }
+    int v[8];
+#pragma unroll
+    for (int st = 0; st < 8; ++st) v[st] = (acc[st][0] >> 6) + (acc[st][1] >> 2);
     int mine_step = 0;
     bool writer = kl == 0;
     if (G >= 8) {
-      bool up = (kl >> (log2G - 1)) & 1;
+      const bool up = (kl >> (log2G - 1)) & 1;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int send = up ? v[k] : v[k + 4], keep = up ? v[k + 4] : v[k];
@@ -340,32 +353,29 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     const int rr = mine_step * rpw + rg;
     if (writer && mine_step < S && rr < rows) {
       const int64_t n = n0 + rr;
-      const int acc = v[0] - rs_total;
-      set.out[l][n] = __fmul_rn(__fdiv_rn(__int2float_rn(acc), s_act), set.w_scale[l]);
-      if (set.acc[l]) set.acc[l][n] = acc;
+      const int a = v[0] - rs_total;
+      set.out[l][n] = __fmul_rn(__fdiv_rn(__int2float_rn(a), s_act), set.w_scale[l]);
+      if (set.acc[l]) set.acc[l][n] = a;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);
   }
 }
 
-// lanes per row: the largest power of two <= 32 dividing C when that keeps T <= 5 chunks per
-// lane, else 32 lanes with a ragged last column (predicated).
-void choose_layout(int K, int& log2G, int& T) {
+// lanes per row: the largest power of two <= 32 dividing C when that keeps at most 5 chunk
+// columns per lane, else 32 lanes with a ragged last column (predicated)
+int choose_log2g(int K) {
   const int C = K >> 6;
-  log2G = 5;
+  int log2G = 5;
   while (log2G > 1 && (C & ((1 << log2G) - 1)) != 0) --log2G;
-  T = C >> log2G;
-  if (T > kMaxT) {
-    log2G = 5;
-    T = (C + 31) >> 5;
-  }
+  if ((C >> log2G) > 5) log2G = 5;
+  return log2G;
 }
 
-template <int T, bool BF16>
+template <bool BF16>
 cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
                      int num_sms, cudaStream_t stream) {
-  auto kern = gemv_group_kernel<T, BF16>;
+  auto kern = gemv_group_kernel<BF16>;
   const int smem = kRingBytes + K;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -405,34 +415,15 @@ cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, con
   return cudaLaunchKernelEx(&cfg, kern, x, set, q, pf, K, log2G, (int)S);
 }
 
-template <bool BF16>
-cudaError_t launch_dtype(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K,
-                         int num_sms, cudaStream_t stream) {
-  int log2G, T;
-  choose_layout(K, log2G, T);
-  switch (T) {
-    case 1: return launch_t<1, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
-    case 2: return launch_t<2, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
-    case 3: return launch_t<3, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
-    case 4: return launch_t<4, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
-    case 5: return launch_t<5, BF16>(x, set, q, pf, K, log2G, num_sms, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 }  // namespace
 
-bool gemv_group_supported(int64_t K) {
-  if (K > kMaxK) return false;
-  int log2G, T;
-  choose_layout((int)K, log2G, T);
-  return T <= kMaxT;
-}
+bool gemv_group_supported(int64_t K) { return K <= kMaxK; }
 
 cudaError_t launch_gemv_group(const void* x, bool bf16, const LinearSet& set, const QuantOut& qout,
                               const Prefetch& pf, int64_t K, int num_sms, cudaStream_t stream) {
-  return bf16 ? launch_dtype<true>(x, set, qout, pf, (int)K, num_sms, stream)
-              : launch_dtype<false>(x, set, qout, pf, (int)K, num_sms, stream);
+  const int log2G = choose_log2g((int)K);
+  return bf16 ? launch_t<true>(x, set, qout, pf, (int)K, log2G, num_sms, stream)
+              : launch_t<false>(x, set, qout, pf, (int)K, log2G, num_sms, stream);
 }
 
 }  // namespace bitnet

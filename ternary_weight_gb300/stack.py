@@ -53,7 +53,7 @@ class TernaryStack:
     """Groups of ternary projections executed in order, as one CUDA graph per step."""
 
     def __init__(self, groups: Sequence[Group], M: int = 1, act_dtype=torch.float32, device="cuda",
-                 algo: str = "auto", fused: bool = True, prefetch_next: bool = True):
+                 algo: str = "auto", fused: bool = True, prefetch_next: bool = False):
         self.groups = list(groups)
         self.fused = fused
         self.prefetch_next = prefetch_next
