@@ -104,10 +104,11 @@ __device__ __forceinline__ bool tile_at(const LinearSet& set, const Geo& g, int 
 }
 
 // BF16: x is bf16 (else fp32).
-template <bool BF16>
+// S: row steps per tile (1..8), a compile-time constant so the step loops carry no
+// predicated dead steps.
+template <bool BF16, int S>
 __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __restrict__ xin, LinearSet set,
-                                                                 QuantOut qout, Prefetch pf, int K, int log2G,
-                                                                 int S) {
+                                                                 QuantOut qout, Prefetch pf, int K, int log2G) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;                      // kSlots x kSlotBytes
   uint8_t* xq_s = smem + kRingBytes;         // K bytes, [j][c][16]
@@ -291,9 +292,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     // per step: hi = 64 * (sum of bit pairs 0 and 1), lo = 4 * (sum of bit pairs 2 and 3);
     // shifting the weight word left by 2 puts pair 1 under pair 0's mask and pair 3 under
     // pair 2's, so one accumulator serves two pairs at the same scale
-    int acc[8][2];
+    int acc[S][2];
 #pragma unroll
-    for (int st = 0; st < 8; ++st) acc[st][0] = acc[st][1] = 0;
+    for (int st = 0; st < S; ++st) acc[st][0] = acc[st][1] = 0;
     for (int t = 0; t < T; ++t) {
       const int c = kl + (t << log2G);
       if (c >= C) continue;
@@ -301,9 +302,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
 #pragma unroll
       for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const uint4*>(xq_s + j * plane + c * 16);
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
+      for (int st = 0; st < S; ++st) {
         const int rr = st * rpw + rg;
-        if (st < S && rr < rows) {
+        if (rr < rows) {
           const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * geo.row_bytes + c * 16);
           const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
           const uint32_t a0[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     }
     int v[8];
 #pragma unroll
-    for (int st = 0; st < 8; ++st) v[st] = (acc[st][0] >> 6) + (acc[st][1] >> 2);
+    for (int st = 0; st < 8; ++st) v[st] = st < S ? (acc[st < S ? st : 0][0] >> 6) + (acc[st < S ? st : 0][1] >> 2) : 0;
     int mine_step = 0;
     bool writer = kl == 0;
     if (G >= 8) {
@@ -372,10 +373,10 @@ int choose_log2g(int K) {
   return log2G;
 }
 
-template <bool BF16>
-cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
-                     int num_sms, cudaStream_t stream) {
-  auto kern = gemv_group_kernel<BF16>;
+template <bool BF16, int S>
+cudaError_t launch_s(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
+                     int blocks, cudaStream_t stream) {
+  auto kern = gemv_group_kernel<BF16, S>;
   const int smem = kRingBytes + K;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -387,6 +388,22 @@ cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, con
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, x, set, q, pf, K, log2G);
+}
+
+template <bool BF16>
+cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
+                     int num_sms, cudaStream_t stream) {
   int64_t total = 0;
   for (int j = 0; j < set.count; ++j) total += set.N[j];
   const int rpw = 32 >> log2G;
@@ -402,17 +419,16 @@ cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, con
   if (S < 1) S = 1;
   const int64_t want = ((per_cta + kConsumerWarps - 1) / kConsumerWarps + rpw - 1) / rpw;
   if (S > want) S = want < 1 ? 1 : want;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, set, q, pf, K, log2G, (int)S);
+  switch (S) {
+    case 1: return launch_s<BF16, 1>(x, set, q, pf, K, log2G, blocks, stream);
+    case 2: return launch_s<BF16, 2>(x, set, q, pf, K, log2G, blocks, stream);
+    case 3: return launch_s<BF16, 3>(x, set, q, pf, K, log2G, blocks, stream);
+    case 4: return launch_s<BF16, 4>(x, set, q, pf, K, log2G, blocks, stream);
+    case 5: return launch_s<BF16, 5>(x, set, q, pf, K, log2G, blocks, stream);
+    case 6: return launch_s<BF16, 6>(x, set, q, pf, K, log2G, blocks, stream);
+    case 7: return launch_s<BF16, 7>(x, set, q, pf, K, log2G, blocks, stream);
+    default: return launch_s<BF16, 8>(x, set, q, pf, K, log2G, blocks, stream);
+  }
 }
 
 }  // namespace
