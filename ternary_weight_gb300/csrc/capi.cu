@@ -145,7 +145,9 @@ BITNET_API int bitnet_w2a8_linear_group_ex(const void* x, int dtype, int64_t M, 
     pf.bytes[p] = prefetch_bytes[p];
   }
   pf.count = prefetch_count;
-  const bool single_launch = (M == 1 && gemv_group_supported(K));
+  int64_t total_rows = 0;
+  for (int l = 0; l < count; ++l) total_rows += N[l];
+  const bool single_launch = (M == 1 && gemv_group_supported(K) && total_rows <= INT32_MAX);
   if (!single_launch && (!xq || !act_scale || !rowsum)) return BITNET_EINVAL;
   if ((xq && !aligned(xq, 16)) || (act_scale && !aligned(act_scale, 4)) || (rowsum && !aligned(rowsum, 4)))
     return BITNET_EALIGN;

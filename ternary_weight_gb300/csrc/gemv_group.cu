@@ -71,36 +71,34 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// The L2 prefetch hint: CTA b hands slice b of every range to cp.async.bulk.prefetch.L2.
+__device__ __forceinline__ void issue_prefetch(const Prefetch& pf) {
+  for (int p = 0; p < pf.count; ++p) {
+    const int64_t n16 = pf.bytes[p] >> 4;
+    int64_t lo = n16 * blockIdx.x / gridDim.x * 16, hi = n16 * (blockIdx.x + 1) / gridDim.x * 16;
+    const char* base = static_cast<const char*>(pf.ptr[p]);
+    while (lo < hi) {
+      const int64_t len = (hi - lo) < (1 << 16) ? (hi - lo) : (1 << 16);
+      prefetch_l2(base + lo, (uint32_t)len);
+      lo += len;
+    }
+  }
+}
+
 __device__ __forceinline__ int quant1(float x, float s) {
   return max(-127, min(127, __float2int_rn(__fmul_rn(x, s))));
 }
 
-// Geometry shared by producer and consumers.
-struct Geo {
-  int64_t row_bytes;
-  int64_t cta_begin, cta_end;  // concatenated row range of this CTA
-  int TR;                      // rows per tile
-};
-
-// The idx-th tile of this CTA: projection l, first row n0 (within l), row count.
-__device__ __forceinline__ bool tile_at(const LinearSet& set, const Geo& g, int idx, int& l, int64_t& n0,
-                                        int& rows) {
-  int64_t off = 0;
+// Number of tiles (whole-row runs of at most TR rows, never across two projections) in the
+// concatenated row range [begin, end) of the group.
+__device__ __forceinline__ int count_tiles(const LinearSet& set, int begin, int end, int TR) {
+  int n = 0, off = 0;
   for (int j = 0; j < set.count; ++j) {
-    const int64_t lo = max(off, g.cta_begin), hi = min(off + (int64_t)set.N[j], g.cta_end);
-    if (hi > lo) {
-      const int64_t cnt = (hi - lo + g.TR - 1) / g.TR;
-      if (idx < cnt) {
-        l = j;
-        n0 = lo - off + (int64_t)idx * g.TR;
-        rows = (int)min((int64_t)g.TR, hi - (lo + (int64_t)idx * g.TR));
-        return true;
-      }
-      idx -= (int)cnt;
-    }
+    const int lo = max(off, begin), hi = min(off + set.N[j], end);
+    if (hi > lo) n += (hi - lo + TR - 1) / TR;
     off += set.N[j];
   }
-  return false;
+  return n;
 }
 
 // BF16: x is bf16 (else fp32).
@@ -116,16 +114,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
   __shared__ float red_f[kConsumerWarps];
   __shared__ int red_i[kConsumerWarps];
+  // the tile held by each ring slot (written by the producer before its release-arrive on
+  // the slot's full barrier, read by the consumer after its acquire-wait)
+  __shared__ int slot_l[kSlots], slot_n0[kSlots], slot_rows[kSlots];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = K >> 6;
-  Geo geo;
-  geo.row_bytes = K >> 2;
-  int64_t total = 0;
+  const int row_bytes = K >> 2;
+  int total = 0;  // rows of the group (the host keeps this below 2^31)
   for (int j = 0; j < set.count; ++j) total += set.N[j];
-  geo.cta_begin = total * blockIdx.x / gridDim.x;
-  geo.cta_end = total * (blockIdx.x + 1) / gridDim.x;
-  geo.TR = S << (5 - log2G);  // rows per tile = steps x rows per step
+  const int cta_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int cta_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  const int TR = S << (5 - log2G);  // rows per tile = steps x rows per step
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
@@ -141,33 +141,31 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   if (warp == kConsumerWarps) {
     // ================================ producer ================================
     if (lane == 0) {
-      int issued = 0;
-      bool prefetched = false;
+      // walk this CTA's tiles in order: projection j, rows [r, hi) of it left to cover
+      int issued = 0, j = -1, off = 0, r = 0, hi = 0, prev_n = 0;
       for (int i = 0;; ++i) {
-        int l, rows;
-        int64_t n0;
-        if (!tile_at(set, geo, i, l, n0, rows)) break;
+        while (r >= hi) {  // next projection that intersects [cta_begin, cta_end)
+          off += prev_n;
+          if (++j >= set.count) break;
+          prev_n = set.N[j];
+          r = max(off, cta_begin);
+          hi = min(off + prev_n, cta_end);
+        }
+        if (j >= set.count) break;
+        const int rows = min(TR, hi - r);
         const int slot = i % kSlots, use = i / kSlots;
         if (use > 0 && !mbar_wait(&empty_bar[slot], (use - 1) & 1, &abort)) break;
-        const uint32_t bytes = (uint32_t)(rows * geo.row_bytes);
+        slot_l[slot] = j;
+        slot_n0[slot] = r - off;
+        slot_rows[slot] = rows;
+        const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
         mbar_arrive_expect_tx(&full_bar[slot], bytes);
-        bulk_copy_g2s(ring + slot * kSlotBytes, set.wp[l] + n0 * geo.row_bytes, bytes, &full_bar[slot]);
+        bulk_copy_g2s(ring + slot * kSlotBytes, set.wp[j] + (int64_t)(r - off) * row_bytes, bytes, &full_bar[slot]);
+        r += rows;
         issued = i + 1;
-        if (!prefetched && (i + 1 == kSlots || !tile_at(set, geo, i + 1, l, n0, rows))) {
-          // ring primed (or all issued): now the prefetch hint, CTA b taking slice b of each range
-          for (int p = 0; p < pf.count; ++p) {
-            const int64_t n16 = pf.bytes[p] >> 4;
-            int64_t lo = n16 * blockIdx.x / gridDim.x * 16, hi = n16 * (blockIdx.x + 1) / gridDim.x * 16;
-            const char* base = static_cast<const char*>(pf.ptr[p]);
-            while (lo < hi) {
-              const int64_t len = (hi - lo) < (1 << 16) ? (hi - lo) : (1 << 16);
-              prefetch_l2(base + lo, (uint32_t)len);
-              lo += len;
-            }
-          }
-          prefetched = true;
-        }
+        if (issued == kSlots) issue_prefetch(pf);  // ring primed: now the L2 prefetch hint
       }
+      if (issued < kSlots) issue_prefetch(pf);
       if (abort) {  // let every copy this CTA issued land before the CTA can exit
         bool dummy = false;
         for (int i = issued - kSlots > 0 ? issued - kSlots : 0; i < issued; ++i)
@@ -282,12 +280,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   // levels) leaves the total of step st in the lanes whose top three lane-in-group bits spell
   // st, so the epilogue (one IEEE divide per output) runs for up to 8 rows in parallel. ----
   const int hb = (G >= 8) ? log2G - 3 : 0;  // low lane bits left after the halving levels
-  for (int i = warp;; i += kConsumerWarps) {
-    int l, rows;
-    int64_t n0;
-    if (!tile_at(set, geo, i, l, n0, rows)) break;
+  const int n_tiles = count_tiles(set, cta_begin, cta_end, TR);
+  for (int i = warp; i < n_tiles; i += kConsumerWarps) {
     const int slot = i % kSlots, use = i / kSlots;
     if (!mbar_wait(&full_bar[slot], use & 1, &abort)) break;
+    const int l = slot_l[slot], n0 = slot_n0[slot], rows = slot_rows[slot];
     const uint8_t* tile = ring + slot * kSlotBytes;
     // per step: hi = 64 * (sum of bit pairs 0 and 1), lo = 4 * (sum of bit pairs 2 and 3);
     // shifting the weight word left by 2 puts pair 1 under pair 0's mask and pair 3 under
@@ -305,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
       for (int st = 0; st < S; ++st) {
         const int rr = st * rpw + rg;
         if (rr < rows) {
-          const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * geo.row_bytes + c * 16);
+          const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * row_bytes + c * 16);
           const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
           const uint32_t a0[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
           const uint32_t a1[4] = {a[1].x, a[1].y, a[1].z, a[1].w};
@@ -353,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     }
     const int rr = mine_step * rpw + rg;
     if (writer && mine_step < S && rr < rows) {
-      const int64_t n = n0 + rr;
+      const int n = n0 + rr;
       const int a = v[0] - rs_total;
       set.out[l][n] = __fmul_rn(__fdiv_rn(__int2float_rn(a), s_act), set.w_scale[l]);
       if (set.acc[l]) set.acc[l][n] = a;
