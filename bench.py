@@ -453,9 +453,9 @@ def run_ours(args):
     achieved = (bytes_step / n_launch) / (t_step / args.steps / n_launch) / 1e9
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": recorded_traffic("gemv_m1.cu"),
+                "traffic": recorded_traffic("gemv_group.cu"),
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                "kernel": "gemv_m1_kernel<T,FUSE> (fused quantisation + grouped GEMV), avg over the step's "
+                "kernel": "gemv_group_kernel (fused quantisation + grouped GEMV), avg over the step's "
                           "%d launches; algorithmic bytes per launch %.0f" % (n_launch, bytes_step / n_launch)}
 
     # ---- e2e: pinned host activations in, every projection's output back, each step ----
