@@ -131,6 +131,23 @@ BITNET_API int bitnet_i2s_matmul(const int8_t *xq, const float *act_scale, const
                                  const uint8_t *wp, float w_scale, float *out, int32_t *acc_out,
                                  int64_t M, int64_t N, int64_t K, void *stream);
 
+/*
+ * bitnet_i2s_matmul_ws -- the same result as bitnet_i2s_matmul, computed the prefill way with a
+ * caller-provided device workspace: the codes are expanded once to fp16 (N x K) and the int8
+ * activations converted once to fp16 (M x K) -- both exact -- and a TMA-fed tcgen05 GEMM runs
+ * on them (fp32 accumulation of integers below 2^24, hence exact). "BitNet 딥다이브" §4-5: the
+ * reference GPU path runs prefill with fp16 weights.
+ *   workspace       : device memory, 256-byte aligned, at least
+ *                     bitnet_i2s_matmul_workspace_size(M, N, K) bytes; contents overwritten.
+ *   workspace_bytes : its size (BITNET_EINVAL if too small).
+ *   Other arguments as bitnet_i2s_matmul; K <= 32768. Three launches on `stream`.
+ */
+BITNET_API int64_t bitnet_i2s_matmul_workspace_size(int64_t M, int64_t N, int64_t K);
+BITNET_API int bitnet_i2s_matmul_ws(const int8_t *xq, const float *act_scale, const int32_t *rowsum,
+                                    const uint8_t *wp, float w_scale, float *out, int32_t *acc_out,
+                                    int64_t M, int64_t N, int64_t K, void *workspace,
+                                    int64_t workspace_bytes, void *stream);
+
 /* Same as bitnet_i2s_matmul with an explicit kernel choice (BITNET_ALGO_*). */
 BITNET_API int bitnet_i2s_matmul_algo(const int8_t *xq, const float *act_scale,
                                       const int32_t *rowsum, const uint8_t *wp, float w_scale,

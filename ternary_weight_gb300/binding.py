@@ -43,6 +43,9 @@ SIGNATURES = {
         ctypes.c_int),
     "bitnet_w2a8_linear": (
         [_P, ctypes.c_int, _I64, _I64, _P, ctypes.c_float, _I64, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "bitnet_i2s_matmul_workspace_size": ([_I64, _I64, _I64], _I64),
+    "bitnet_i2s_matmul_ws": (
+        [_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "bitnet_last_device_error": ([], ctypes.c_int),
 }
 
@@ -159,6 +162,33 @@ def _act_dtype(x):
     if x.dtype == torch.bfloat16:
         return BITNET_BF16
     raise ValueError("x must be float32 or bfloat16")
+
+
+def workspace_size(M, N, K) -> int:
+    n = lib().bitnet_i2s_matmul_workspace_size(M, N, K)
+    if n < 0:
+        raise BitnetError(int(n), "bitnet_i2s_matmul_workspace_size")
+    return int(n)
+
+
+def i2s_matmul_ws(xq, scale, rowsum, wp, w_scale, workspace=None, out=None, acc_out=None, stream=None):
+    """The prefill path with a device workspace (allocated here from torch if not given)."""
+    import torch
+
+    M, K = xq.shape
+    N = wp.shape[0]
+    if wp.shape[1] * 4 != K:
+        raise ValueError("wp must be N x K/4")
+    need = workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+    out = torch.empty((M, N), dtype=torch.float32, device=xq.device) if out is None else out
+    _require_cuda(xq, scale, rowsum, wp, out, acc_out, workspace)
+    _check(lib().bitnet_i2s_matmul_ws(_ptr(xq), _ptr(scale), _ptr(rowsum), _ptr(wp), float(w_scale), _ptr(out),
+                                      _ptr(acc_out), M, N, K, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "bitnet_i2s_matmul_ws")
+    return out
 
 
 def linear_group(x, wps, w_scales, outs=None, accs=None, xq=None, scale=None, rowsum=None, prefetch=None,

@@ -228,8 +228,16 @@ cudaError_t launch_quant_act(const void* x, int dtype, int64_t M, int64_t K, int
 cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
                             float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
                             int num_sms, cudaStream_t stream);
-// Reads and clears the GEMM translation unit's device error word (synchronous).
+// Read and clear the device error word of each translation unit that waits (synchronous).
 cudaError_t read_clear_device_error_gemm(int* value);
+cudaError_t read_clear_device_error_gemm_ws(int* value);
+cudaError_t read_clear_device_error_gemv_group(int* value);
+
+// Expand-then-GEMM path (gemm_tc_ws.cu): workspace bytes, and the launch (K <= 32768).
+int64_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_tc_ws(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
+                              float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
+                              void* workspace, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_i2s_tc(const int8_t* xq, const float* act_scale, const int32_t* rowsum,
                                const uint8_t* wp, float w_scale, float* out, int32_t* acc_out, int64_t M,
                                int64_t N, int64_t K, int num_sms, cudaStream_t stream);

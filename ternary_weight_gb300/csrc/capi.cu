@@ -113,6 +113,26 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
   return status_of(e);
 }
 
+BITNET_API int64_t bitnet_i2s_matmul_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || M > INT32_MAX || N < 1 || N > INT32_MAX || !valid_k(K) || K > kMaxKTensorCore) return BITNET_EINVAL;
+  return gemm_ws_bytes(M, N, K);
+}
+
+BITNET_API int bitnet_i2s_matmul_ws(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
+                                    float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
+                                    void* workspace, int64_t workspace_bytes, void* stream) {
+  if (!xq || !act_scale || !rowsum || !wp || !out || !workspace) return BITNET_EINVAL;
+  if (M < 1 || M > INT32_MAX || N < 1 || N > INT32_MAX || !valid_k(K) || K > kMaxKTensorCore) return BITNET_EINVAL;
+  if (workspace_bytes < gemm_ws_bytes(M, N, K)) return BITNET_EINVAL;
+  if (!aligned(xq, 16) || !aligned(wp, 16) || !aligned(act_scale, 4) || !aligned(rowsum, 4) || !aligned(out, 4) ||
+      (acc_out && !aligned(acc_out, 4)) || !aligned(workspace, 256))
+    return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  return status_of(launch_gemm_tc_ws(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, workspace, sms,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 BITNET_API int bitnet_i2s_matmul(const int8_t* xq, const float* act_scale, const int32_t* rowsum,
                                  const uint8_t* wp, float w_scale, float* out, int32_t* acc_out, int64_t M,
                                  int64_t N, int64_t K, void* stream) {
@@ -194,9 +214,15 @@ BITNET_API int bitnet_last_device_error(void) {
   int sms = 0;
   if (int st = check_device(&sms)) return st;
   if (cudaDeviceSynchronize() != cudaSuccess) return BITNET_ECUDA;
-  int v = 0;
-  if (read_clear_device_error_gemm(&v) != cudaSuccess) return BITNET_ECUDA;
-  return v == 0 ? BITNET_OK : v;
+  int status = BITNET_OK;
+  cudaError_t (*readers[])(int*) = {read_clear_device_error_gemm, read_clear_device_error_gemm_ws,
+                                    read_clear_device_error_gemv_group};
+  for (auto rd : readers) {
+    int v = 0;
+    if (rd(&v) != cudaSuccess) return BITNET_ECUDA;
+    if (v != 0 && status == BITNET_OK) status = v;
+  }
+  return status;
 }
 
 }  // extern "C"

@@ -430,6 +430,13 @@ cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, con
 
 }  // namespace
 
+cudaError_t read_clear_device_error_gemv_group(int* value) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+}
+
 bool gemv_group_supported(int64_t K) { return K <= kMaxK; }
 
 cudaError_t launch_gemv_group(const void* x, bool bf16, const LinearSet& set, const QuantOut& qout,

@@ -148,3 +148,18 @@ def test_linear_group_ex_rejects_bad_prefetch(lib):
     assert call(1, P(0, 0), B(16, 16)) == -1
     assert call(1, P(FAKE, 0), B(-16, 16)) == -1
     assert call(1, P(FAKE + 4, 0), B(16, 16)) == -2
+
+
+def test_workspace_size_and_ws_validation(lib):
+    up = lambda v: (v + 255) // 256 * 256
+    for M, N, K in ((2, 3, 128), (4096, 2560, 6912), (1, 1, 32768)):
+        assert lib.bitnet_i2s_matmul_workspace_size(M, N, K) == up(M * K * 2) + up(N * K * 2)
+    assert lib.bitnet_i2s_matmul_workspace_size(1, 1, 65536) == -1  # beyond the exact-accumulation K
+    assert lib.bitnet_i2s_matmul_workspace_size(0, 1, 128) == -1
+    need = lib.bitnet_i2s_matmul_workspace_size(1, 1, 128)
+    ws = lambda **kw: lib.bitnet_i2s_matmul_ws(kw.get("xq", FAKE), FAKE, FAKE, FAKE, 1.0, FAKE, None, 1, 1, 128,
+                                               kw.get("w", FAKE), kw.get("n", need), None)
+    assert ws(w=None) == -1
+    assert ws(n=need - 1) == -1
+    assert ws(w=FAKE + 16) == -2   # the workspace must be 256-byte aligned
+    assert ws(xq=FAKE + 8) == -2

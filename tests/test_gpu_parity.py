@@ -351,3 +351,53 @@ def test_linear_group_prefetch_hint_changes_nothing():
     torch.cuda.synchronize()
     for u, v in zip(a, b):
         assert np.array_equal(host(u).view(np.uint32), host(v).view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- prefill with workspace
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (65, 300, 2560), (128, 256, 2560), (129, 513, 1024),
+                                   (200, 1000, 6912), (512, 2560, 6912), (300, 6912, 2560), (256, 640, 8192)])
+def test_matmul_ws_parity(M, N, K):
+    x = workloads.activations(M, K, seed=900 + M, dtype="bf16")
+    w = workloads.ternary_weights(N, K, seed=901 + N)
+    ws = workloads.weight_scale(N, K, 902)
+    g_wp = binding.pack_i2s(dev(w))
+    g_xq, g_s, g_rs = binding.quant_act(x_device(x, "bf16"))
+    g_acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    g_out = binding.i2s_matmul_ws(g_xq, g_s, g_rs, g_wp, ws, acc_out=g_acc)
+    torch.cuda.synchronize()
+    o_xq, o_s, _ = oracle.quant_act(x, "bf16")
+    o_out, o_acc = oracle.ternary_matmul(o_xq, o_s, oracle.pack_i2s(w)[0], ws, nthreads=NT)
+    assert np.array_equal(host(g_acc), o_acc)
+    assert np.array_equal(host(g_out).view(np.uint32), o_out.view(np.uint32))
+
+
+def test_matmul_ws_random_bytes_and_max_magnitude():
+    M, N, K = 130, 300, 8192
+    xq = workloads.random_int8(M, K, seed=910)
+    xq[0, :] = 127
+    xq[1, :] = -127
+    wp = workloads.random_packed_bytes(N, K, seed=911)
+    wp[0, :] = 0xAA  # all codes 2: acc = 127*K and -127*K in rows 0 and 1
+    s = np.full(M, 0.75, np.float32)
+    rs = xq.astype(np.int64).sum(axis=1).astype(np.int32)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    out = binding.i2s_matmul_ws(dev(xq), dev(s), dev(rs), dev(wp), 0.013, acc_out=acc)
+    torch.cuda.synchronize()
+    o_out, o_acc = oracle.ternary_matmul(xq, s, wp, 0.013, nthreads=NT)
+    assert np.array_equal(host(acc), o_acc) and o_acc[0, 0] == 127 * K and o_acc[1, 0] == -127 * K
+    assert_out_close(host(out), o_out)
+
+
+def test_matmul_ws_two_calls_reuse_workspace():
+    M, N, K = 256, 512, 2560
+    wsbuf = torch.empty(binding.workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+    for seed in (920, 921):
+        xq = workloads.random_int8(M, K, seed=seed)
+        wp, _ = oracle.pack_i2s(workloads.ternary_weights(N, K, seed + 5))
+        s = np.full(M, 1.25, np.float32)
+        rs = xq.astype(np.int64).sum(axis=1).astype(np.int32)
+        out = binding.i2s_matmul_ws(dev(xq), dev(s), dev(rs), dev(wp), 0.02, workspace=wsbuf)
+        torch.cuda.synchronize()
+        o_out, _ = oracle.ternary_matmul(xq, s, wp, 0.02, nthreads=NT)
+        assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32))
