@@ -148,6 +148,27 @@ BITNET_API int bitnet_i2s_matmul_ws(const int8_t *xq, const float *act_scale, co
                                     int64_t M, int64_t N, int64_t K, void *workspace,
                                     int64_t workspace_bytes, void *stream);
 
+/*
+ * bitnet_i2s_matmul_noalloc -- bitnet_i2s_matmul_ws for callers that cannot allocate device
+ * memory (for example a plugin whose host framework owns all device memory and forbids
+ * cudaMalloc, or a loop where a cudaMalloc/cudaFree would synchronise the device). No page
+ * describes such an entry point; it exists for those callers only.
+ *   It uses no caller workspace and allocates nothing: the workspace is a fixed 64 MiB
+ *   scratch array in the library's device image, which every GPU that loads the library
+ *   holds until the process exits. Problems whose workspace
+ *   (bitnet_i2s_matmul_workspace_size) exceeds 64 MiB are refused with BITNET_EINVAL before
+ *   any GPU work.
+ *   The first call on each device (with that device current) looks up the array's device
+ *   address; make that first call before any stream capture.
+ *   All calls share the array: calls that overlap on the GPU race on it. Each call overwrites
+ *   what it uses, so nothing has to be cleared between calls.
+ *   Other arguments, results and errors as bitnet_i2s_matmul_ws.
+ */
+BITNET_API int bitnet_i2s_matmul_noalloc(const int8_t *xq, const float *act_scale,
+                                         const int32_t *rowsum, const uint8_t *wp, float w_scale,
+                                         float *out, int32_t *acc_out, int64_t M, int64_t N,
+                                         int64_t K, void *stream);
+
 /* Same as bitnet_i2s_matmul with an explicit kernel choice (BITNET_ALGO_*). */
 BITNET_API int bitnet_i2s_matmul_algo(const int8_t *xq, const float *act_scale,
                                       const int32_t *rowsum, const uint8_t *wp, float w_scale,

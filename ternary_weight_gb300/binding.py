@@ -46,6 +46,7 @@ SIGNATURES = {
     "bitnet_i2s_matmul_workspace_size": ([_I64, _I64, _I64], _I64),
     "bitnet_i2s_matmul_ws": (
         [_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "bitnet_i2s_matmul_noalloc": ([_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "bitnet_last_device_error": ([], ctypes.c_int),
 }
 
@@ -188,6 +189,25 @@ def i2s_matmul_ws(xq, scale, rowsum, wp, w_scale, workspace=None, out=None, acc_
                                       _ptr(acc_out), M, N, K, _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)),
            "bitnet_i2s_matmul_ws")
+    return out
+
+
+def i2s_matmul_noalloc(xq, scale, rowsum, wp, w_scale, out=None, acc_out=None, stream=None):
+    """The prefill matmul without any workspace: for callers that must not allocate device memory.
+
+    The library's own 64 MiB device scratch array stands in for the workspace (problems that
+    need more are refused); the output tensor is allocated here only if ``out`` is not given."""
+    import torch
+
+    M, K = xq.shape
+    N = wp.shape[0]
+    if wp.shape[1] * 4 != K:
+        raise ValueError("wp must be N x K/4")
+    out = torch.empty((M, N), dtype=torch.float32, device=xq.device) if out is None else out
+    _require_cuda(xq, scale, rowsum, wp, out, acc_out)
+    _check(lib().bitnet_i2s_matmul_noalloc(_ptr(xq), _ptr(scale), _ptr(rowsum), _ptr(wp), float(w_scale), _ptr(out),
+                                           _ptr(acc_out), M, N, K, _stream(stream)),
+           "bitnet_i2s_matmul_noalloc")
     return out
 
 
