@@ -23,11 +23,16 @@
 //  * Programmatic dependent launch: the kernel lets the next kernel in the stream launch as
 //    soon as it starts, and streams its weights (read-only model state) before it waits for
 //    the previous kernel (griddepcontrol.wait); the activations are read and every output is
-//    written only after that wait.
+//    written only after that wait. In a chain of such kernels the time per kernel is the
+//    release latency plus what follows the wait, so everything that does not need the
+//    activations happens before it: the kernel parameters are copied to shared memory (a
+//    parameter's first read misses the constant cache), the tile count is computed, the
+//    row gets an L2 prefetch and each consumer warp waits for its first tile.
 //  * Warps 0-7 are consumers; tile i goes to warp i % 8 (the slot count is a multiple of 8,
 //    so each slot belongs to one warp). They read the row once into registers (fp32 or bf16),
-//    reduce max|x|, quantise every element once into shared memory laid out [j][c][16] and
-//    reduce the row sum. Lane kl of a G-lane row group owns chunk columns c = kl + G*t; per
+//    reduce max|x| (redux.sync on the bits of the non-negative maxima), quantise every
+//    element once into shared memory laid out [j][c][16] (rounding by the fp32
+//    add-1.5*2^23 identity) and reduce the row sum. Lane kl of a G-lane row group owns chunk columns c = kl + G*t; per
 //    column it loads the 64 paired activation bytes (four conflict-free LDS.128) and applies
 //    them to up to 8 row steps of the tile: per 16-byte weight chunk one LDS.128, then per
 //    32-bit word w four masked operands (w & 0xC0.., (w<<2) & 0xC0.., w & 0x0C..,
@@ -60,6 +65,9 @@ constexpr int kMaxK = 10240;            // largest K this kernel takes
 // and the quantise pass (all of them for K <= 6144 fp32 / 12288 bf16), the rest are re-read
 constexpr int kMaxVecPerThread = kMaxK / 4 / (kConsumerWarps * 32);
 constexpr int kRegVec = 6;
+// chunk columns per lane: the lane layout keeps C/G <= 5, or G = 32 with C <= kMaxK/64 = 160
+constexpr int kMaxColsPerLane = 5;
+static_assert(kMaxK / 64 <= 32 * kMaxColsPerLane, "column loop bound");
 // Tile i lives in slot i % kSlots and is consumed by warp i % kConsumerWarps. With the slot
 // count a multiple of the consumer-warp count, every slot is only ever waited on by one
 // warp, in order, so a parity wait can never see a stale phase of its slot.
@@ -85,18 +93,26 @@ __device__ __forceinline__ void issue_prefetch(const Prefetch& pf) {
   }
 }
 
-__device__ __forceinline__ int quant1(float x, float s) {
-  return max(-127, min(127, __float2int_rn(__fmul_rn(x, s))));
+// x * s rounded to the nearest integer, ties to even, returned as the bits of the fp32 sum
+// x*s + 1.5*2^23: for |x*s| < 2^22 the sum lies in [2^23, 2^24), where fp32 steps by exactly 1,
+// so the round-to-nearest-even add performs the integer rounding (1.5*2^23 is even, so ties
+// go the same way), and bits - 0x4B400000 is the integer; its low byte is the int8 code.
+// The clamp to [-127, 127] is never active: s = fl(127/a) with a >= max|x| gives
+// |fl(x*s)| <= 127 (1 + 2^-24)^2 < 127.5, so the rounded value is at most 127 in magnitude.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+__device__ __forceinline__ uint32_t quant_bits(float x, float s) {
+  return __float_as_uint(__fadd_rn(__fmul_rn(x, s), kRoundMagic));
 }
 
 // Number of tiles (whole-row runs of at most TR rows, never across two projections) in the
-// concatenated row range [begin, end) of the group.
-__device__ __forceinline__ int count_tiles(const LinearSet& set, int begin, int end, int TR) {
+// concatenated row range [begin, end) of the group's count projections of N[j] rows.
+__device__ __forceinline__ int count_tiles(const int* N, int count, int begin, int end, int TR) {
   int n = 0, off = 0;
-  for (int j = 0; j < set.count; ++j) {
-    const int lo = max(off, begin), hi = min(off + set.N[j], end);
+  for (int j = 0; j < count; ++j) {
+    const int lo = max(off, begin), hi = min(off + N[j], end);
     if (hi > lo) n += (hi - lo + TR - 1) / TR;
-    off += set.N[j];
+    off += N[j];
   }
   return n;
 }
@@ -116,15 +132,26 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   __shared__ int red_i[kConsumerWarps];
   // the tile held by each ring slot (written by the producer before its release-arrive on
   // the slot's full barrier, read by the consumer after its acquire-wait)
-  __shared__ int slot_l[kSlots], slot_n0[kSlots], slot_rows[kSlots];
+  __shared__ int slot_rows[kSlots];
+  __shared__ float* slot_out[kSlots];    // output row of the tile's first row
+  __shared__ int32_t* slot_acc[kSlots];  // same for the optional accumulators (or null)
+  __shared__ float slot_ws[kSlots];      // weight scale of the tile's projection
+  // The kernel parameters, copied to shared memory at the start. The first read of a
+  // parameter in a launch misses the constant cache (about half a microsecond); staged here,
+  // those misses are paid before the dependency wait instead of after it, where every
+  // nanosecond lengthens the decode chain.
+  __shared__ const uint8_t* p_wp[kMaxGroupLinears];
+  __shared__ float* p_out[kMaxGroupLinears];
+  __shared__ int32_t* p_acc[kMaxGroupLinears];
+  __shared__ float p_ws[kMaxGroupLinears];
+  __shared__ int p_N[kMaxGroupLinears];
+  __shared__ int p_count;
+  __shared__ const void* p_x;
+  __shared__ QuantOut p_q;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = K >> 6;
   const int row_bytes = K >> 2;
-  int total = 0;  // rows of the group (the host keeps this below 2^31)
-  for (int j = 0; j < set.count; ++j) total += set.N[j];
-  const int cta_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
-  const int cta_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   const int TR = S << (5 - log2G);  // rows per tile = steps x rows per step
 
   if (threadIdx.x == 0) {
@@ -134,8 +161,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     }
     fence_mbar_init();
   }
+  if (warp == 1 && lane < kMaxGroupLinears) {
+    p_wp[lane] = set.wp[lane];
+    p_out[lane] = set.out[lane];
+    p_acc[lane] = set.acc[lane];
+    p_ws[lane] = set.w_scale[lane];
+    p_N[lane] = set.N[lane];
+    if (lane == 0) {
+      p_count = set.count;
+      p_x = xin;
+      p_q = qout;
+    }
+  }
   __syncthreads();
   pdl_launch_dependents();
+  const int count = p_count;
+  int total = 0;  // rows of the group (the host keeps this below 2^31)
+  for (int j = 0; j < count; ++j) total += p_N[j];
+  const int cta_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int cta_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   bool abort = false;
 
   if (warp == kConsumerWarps) {
@@ -146,21 +190,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
       for (int i = 0;; ++i) {
         while (r >= hi) {  // next projection that intersects [cta_begin, cta_end)
           off += prev_n;
-          if (++j >= set.count) break;
-          prev_n = set.N[j];
+          if (++j >= count) break;
+          prev_n = p_N[j];
           r = max(off, cta_begin);
           hi = min(off + prev_n, cta_end);
         }
-        if (j >= set.count) break;
+        if (j >= count) break;
         const int rows = min(TR, hi - r);
         const int slot = i % kSlots, use = i / kSlots;
         if (use > 0 && !mbar_wait(&empty_bar[slot], (use - 1) & 1, &abort)) break;
-        slot_l[slot] = j;
-        slot_n0[slot] = r - off;
+        slot_out[slot] = p_out[j] + (r - off);
+        slot_acc[slot] = p_acc[j] ? p_acc[j] + (r - off) : nullptr;
+        slot_ws[slot] = p_ws[j];
         slot_rows[slot] = rows;
         const uint32_t bytes = (uint32_t)rows * (uint32_t)row_bytes;
         mbar_arrive_expect_tx(&full_bar[slot], bytes);
-        bulk_copy_g2s(ring + slot * kSlotBytes, set.wp[j] + (int64_t)(r - off) * row_bytes, bytes, &full_bar[slot]);
+        bulk_copy_g2s(ring + slot * kSlotBytes, p_wp[j] + (int64_t)(r - off) * row_bytes, bytes, &full_bar[slot]);
         r += rows;
         issued = i + 1;
         if (issued == kSlots) issue_prefetch(pf);  // ring primed: now the L2 prefetch hint
@@ -183,13 +228,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   const int T = (C + G - 1) >> log2G;  // chunk columns per lane (the last may be ragged)
   const int plane = K >> 2;
 
+  // everything that does not depend on the activations is done before the wait: the tile
+  // count, the L2 prefetch of the row and the wait for this warp's first tile
+  const int n_tiles = count_tiles(p_N, count, cta_begin, cta_end, TR);
+  const QuantOut q_out = p_q;
+  const uint4* xv = static_cast<const uint4*>(p_x);
+  // an L2 prefetch of the row is safe before the wait: it returns no data, and a write by
+  // the previous kernel lands in L2 all the same
+  if (threadIdx.x == 0) prefetch_l2(xv, (uint32_t)K * (BF16 ? 2u : 4u));
+  if (warp < n_tiles) mbar_wait(&full_bar[warp], 0, &abort);  // tile `warp`: slot warp, use 0
   float s_act;
   int rs_total;
   pdl_wait();  // the activations may be the previous kernel's output
   {
     // the row is read once into registers: vector v = threadIdx.x + kConsumers * i
     constexpr int E = BF16 ? 8 : 4;  // elements per 16-byte vector
-    const uint4* xv = static_cast<const uint4*>(xin);
     const int nvec = K / E;
     uint4 xr[kRegVec];
     float amax = 0.0f;
@@ -209,82 +262,94 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) red_f[warp] = amax;
+    // amax is a non-negative float (fmaxf drops NaN), so its bits order like unsigned ints
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
+    if (lane == 0) red_f[warp] = __uint_as_float(wmax);
     named_bar_sync(1, kConsumers);
-    amax = red_f[0];
-#pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, red_f[w]);
+    {
+      const float4 r0 = *reinterpret_cast<const float4*>(&red_f[0]);
+      const float4 r1 = *reinterpret_cast<const float4*>(&red_f[4]);
+      amax = fmaxf(fmaxf(fmaxf(r0.x, r0.y), fmaxf(r0.z, r0.w)), fmaxf(fmaxf(r1.x, r1.y), fmaxf(r1.z, r1.w)));
+    }
     s_act = __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
     // quantise each element once; element k goes to [j][c][16] with
-    // c = 2*(k/128) + (k%32)/16, j = (k%128)/32
-    int sum = 0;
-    const bool publish = blockIdx.x == 0 && qout.xq != nullptr;
+    // c = 2*(k/128) + (k%32)/16, j = (k%128)/32. The row sum is accumulated on the biased
+    // bits (each q + 0x4B400000) and unbiased at the end, modulo 2^32.
+    uint32_t bsum = 0;
+    int nel = 0;
+    const bool publish = blockIdx.x == 0 && q_out.xq != nullptr;
 #pragma unroll
     for (int i = 0; i < kMaxVecPerThread; ++i) {
       const int v = threadIdx.x + kConsumers * i;
       if (v < nvec) {
         const uint4 u = i < kRegVec ? xr[i] : __ldg(xv + v);
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-        int q[E];
+        uint32_t qb[E];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if constexpr (BF16) {
-            q[2 * e] = quant1(__uint_as_float(w4[e] << 16), s_act);
-            q[2 * e + 1] = quant1(__uint_as_float(w4[e] & 0xFFFF0000u), s_act);
+            qb[2 * e] = quant_bits(__uint_as_float(w4[e] << 16), s_act);
+            qb[2 * e + 1] = quant_bits(__uint_as_float(w4[e] & 0xFFFF0000u), s_act);
           } else {
-            q[e] = quant1(__uint_as_float(w4[e]), s_act);
+            qb[e] = quant_bits(__uint_as_float(w4[e]), s_act);
           }
         }
+#pragma unroll
+        for (int e = 0; e < E; ++e) bsum += qb[e];
+        nel += E;
         const int k = v * E;
         const int rem = k & 127;
         const int off = (rem >> 5) * plane + (2 * (k >> 7) + ((rem & 31) >> 4)) * 16 + (rem & 15);
-        uint32_t word0 = 0, word1 = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          word0 |= (uint32_t)(q[b] & 0xFF) << (8 * b);
-          sum += q[b];
-        }
+        // low bytes of four words -> one word
+        const uint32_t word0 = __byte_perm(__byte_perm(qb[0], qb[1], 0x0040), __byte_perm(qb[2], qb[3], 0x0040), 0x5410);
         if constexpr (BF16) {
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            word1 |= (uint32_t)(q[4 + b] & 0xFF) << (8 * b);
-            sum += q[4 + b];
-          }
+          const uint32_t word1 =
+              __byte_perm(__byte_perm(qb[4], qb[5], 0x0040), __byte_perm(qb[6], qb[7], 0x0040), 0x5410);
           *reinterpret_cast<uint2*>(xq_s + off) = make_uint2(word0, word1);
-          if (publish) *reinterpret_cast<uint2*>(qout.xq + k) = make_uint2(word0, word1);
+          if (publish) *reinterpret_cast<uint2*>(q_out.xq + k) = make_uint2(word0, word1);
         } else {
           *reinterpret_cast<uint32_t*>(xq_s + off) = word0;
-          if (publish) *reinterpret_cast<uint32_t*>(qout.xq + k) = word0;
+          if (publish) *reinterpret_cast<uint32_t*>(q_out.xq + k) = word0;
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) red_i[warp] = sum;
+    const int sum = (int)(bsum - (uint32_t)nel * kRoundMagicBits);
+    const int wsum = __reduce_add_sync(0xffffffffu, sum);
+    if (lane == 0) red_i[warp] = wsum;
     named_bar_sync(1, kConsumers);  // also orders the shared activation writes before the reads
-    rs_total = 0;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) rs_total += red_i[w];
+    {
+      const int4 r0 = *reinterpret_cast<const int4*>(&red_i[0]);
+      const int4 r1 = *reinterpret_cast<const int4*>(&red_i[4]);
+      rs_total = ((r0.x + r0.y) + (r0.z + r0.w)) + ((r1.x + r1.y) + (r1.z + r1.w));
+    }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-      if (qout.scale) *qout.scale = s_act;
-      if (qout.rowsum) *qout.rowsum = rs_total;
+      if (q_out.scale) *q_out.scale = s_act;
+      if (q_out.rowsum) *q_out.rowsum = rs_total;
     }
   }
 
   // ---- consume this warp's tiles: a tile is S steps of rpw rows; step st of row group rg is
   // row st*rpw + rg. For each chunk column the lane loads the 64 paired activation bytes from
-  // shared memory once and applies them to all S steps, keeping four bit-pair accumulators
-  // per step. A transpose-reduce over the G lanes (three halving levels, then plain xor
-  // levels) leaves the total of step st in the lanes whose top three lane-in-group bits spell
-  // st, so the epilogue (one IEEE divide per output) runs for up to 8 rows in parallel. ----
+  // shared memory once and applies them to all S steps, keeping two accumulators per step.
+  // The column loop is unrolled over its bound of 5 (the lane layout keeps C/G <= 5 for
+  // K <= 10240) with every load unconditional, so loads of the next column overlap the
+  // arithmetic of this one: a column past the row's end, or a row past the tile's end, reads
+  // bytes inside the ring slot and the activation buffer and has its weight word zeroed.
+  // A transpose-reduce over the G lanes (three halving levels, then plain xor levels) leaves
+  // the total of step st in the lanes whose top three lane-in-group bits spell st, so the
+  // epilogue (one IEEE divide per output) runs for up to 8 rows in parallel. ----
   const int hb = (G >= 8) ? log2G - 3 : 0;  // low lane bits left after the halving levels
-  const int n_tiles = count_tiles(set, cta_begin, cta_end, TR);
   for (int i = warp; i < n_tiles; i += kConsumerWarps) {
     const int slot = i % kSlots, use = i / kSlots;
-    if (!mbar_wait(&full_bar[slot], use & 1, &abort)) break;
-    const int l = slot_l[slot], n0 = slot_n0[slot], rows = slot_rows[slot];
+    if (i != warp) {
+      if (!mbar_wait(&full_bar[slot], use & 1, &abort)) break;
+    } else if (abort) {
+      break;
+    }
+    const int rows = slot_rows[slot];
+    float* const out_row = slot_out[slot];
+    int32_t* const acc_row = slot_acc[slot];
+    const float ws = slot_ws[slot];
     const uint8_t* tile = ring + slot * kSlotBytes;
     // per step: hi = 64 * (sum of bit pairs 0 and 1), lo = 4 * (sum of bit pairs 2 and 3);
     // shifting the weight word left by 2 puts pair 1 under pair 0's mask and pair 3 under
@@ -292,30 +357,33 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     int acc[S][2];
 #pragma unroll
     for (int st = 0; st < S; ++st) acc[st][0] = acc[st][1] = 0;
+    // (fully unrolled up to 4 steps; beyond that the registers of a second column would spill)
+    constexpr int kUnrollCols = S <= 4 ? kMaxColsPerLane : 1;
+#pragma unroll kUnrollCols
     for (int t = 0; t < T; ++t) {
       const int c = kl + (t << log2G);
-      if (c >= C) continue;
+      const bool col_ok = c < C;
+      const int cc = col_ok ? c : C - 1;
       uint4 a[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const uint4*>(xq_s + j * plane + c * 16);
+      for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const uint4*>(xq_s + j * plane + cc * 16);
 #pragma unroll
       for (int st = 0; st < S; ++st) {
         const int rr = st * rpw + rg;
-        if (rr < rows) {
-          const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * row_bytes + c * 16);
-          const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-          const uint32_t a0[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
-          const uint32_t a1[4] = {a[1].x, a[1].y, a[1].z, a[1].w};
-          const uint32_t a2[4] = {a[2].x, a[2].y, a[2].z, a[2].w};
-          const uint32_t a3[4] = {a[3].x, a[3].y, a[3].z, a[3].w};
+        uint4 w = *reinterpret_cast<const uint4*>(tile + rr * row_bytes + cc * 16);
+        if (!col_ok || rr >= rows) w = make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t a0[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
+        const uint32_t a1[4] = {a[1].x, a[1].y, a[1].z, a[1].w};
+        const uint32_t a2[4] = {a[2].x, a[2].y, a[2].z, a[2].w};
+        const uint32_t a3[4] = {a[3].x, a[3].y, a[3].z, a[3].w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t sh = w4[q] << 2;
-            acc[st][0] = dp4a_us(w4[q] & 0xC0C0C0C0u, a0[q], acc[st][0]);
-            acc[st][0] = dp4a_us(sh & 0xC0C0C0C0u, a1[q], acc[st][0]);
-            acc[st][1] = dp4a_us(w4[q] & 0x0C0C0C0Cu, a2[q], acc[st][1]);
-            acc[st][1] = dp4a_us(sh & 0x0C0C0C0Cu, a3[q], acc[st][1]);
-          }
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t sh = w4[q] << 2;
+          acc[st][0] = dp4a_us(w4[q] & 0xC0C0C0C0u, a0[q], acc[st][0]);
+          acc[st][0] = dp4a_us(sh & 0xC0C0C0C0u, a1[q], acc[st][0]);
+          acc[st][1] = dp4a_us(w4[q] & 0x0C0C0C0Cu, a2[q], acc[st][1]);
+          acc[st][1] = dp4a_us(sh & 0x0C0C0C0Cu, a3[q], acc[st][1]);
         }
       }
     }
@@ -350,10 +418,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     }
     const int rr = mine_step * rpw + rg;
     if (writer && mine_step < S && rr < rows) {
-      const int n = n0 + rr;
       const int a = v[0] - rs_total;
-      set.out[l][n] = __fmul_rn(__fdiv_rn(__int2float_rn(a), s_act), set.w_scale[l]);
-      if (set.acc[l]) set.acc[l][n] = a;
+      out_row[rr] = __fmul_rn(__fdiv_rn(__int2float_rn(a), s_act), ws);
+      if (acc_row) acc_row[rr] = a;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);

@@ -280,6 +280,38 @@ def test_linear_group_m1_fused(dtype, K, Ns):
         assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_linear_group_m1_rounding_ties(dtype):
+    """max|x| = 127 makes s = 1 exactly, so every x = k + 0.5 is a rounding tie: the fused
+    quantisation must round each to the even neighbour, as the oracle does."""
+    K = 2560
+    rng = np.random.default_rng(870)
+    halves = (rng.integers(-126, 126, size=K) + 0.5).astype(np.float32)
+    ints = rng.integers(-127, 128, size=K).astype(np.float32)
+    x = np.where(rng.random(K) < 0.7, halves, ints).astype(np.float32)
+    x[17] = 127.0
+    x = x.reshape(1, K)
+    tie = np.abs(x - np.trunc(x)) == 0.5  # every such value is exact in bf16 too (|x| < 128)
+    if dtype == "bf16":
+        x = workloads.to_bf16_bits(x)
+    ws = [workloads.ternary_weights(N, K, seed=871 + i) for i, N in enumerate([640, 2560])]
+    wps = [binding.pack_i2s(dev(w)) for w in ws]
+    accs = [torch.empty((1, w.shape[0]), dtype=torch.int32, device="cuda") for w in ws]
+    xq = torch.empty((1, K), dtype=torch.int8, device="cuda")
+    s = torch.empty(1, dtype=torch.float32, device="cuda")
+    rs = torch.empty(1, dtype=torch.int32, device="cuda")
+    outs = binding.linear_group(x_device(x, dtype), wps, [0.02, 0.03], accs=accs, xq=xq, scale=s, rowsum=rs)
+    torch.cuda.synchronize()
+    o_xq, o_s, o_rs = oracle.quant_act(x, dtype)
+    assert o_s[0] == 1.0 and tie.sum() > K // 2 and np.all(o_xq[tie] % 2 == 0)  # ties went to even codes
+    assert np.array_equal(host(xq), o_xq)
+    assert np.array_equal(host(rs), o_rs)
+    for w, sc, out, acc in zip(ws, [0.02, 0.03], outs, accs):
+        o_out, o_acc = oracle.ternary_matmul(o_xq, o_s, oracle.pack_i2s(w)[0], sc, nthreads=NT)
+        assert np.array_equal(host(acc), o_acc)
+        assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32))
+
+
 def test_linear_group_m1_without_quant_outputs():
     K, Ns = 2560, [2560, 640]
     x = workloads.activations(1, K, seed=850, dtype="f32")
