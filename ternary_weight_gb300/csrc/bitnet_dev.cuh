@@ -90,6 +90,14 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src, u
       : "memory");
 }
 
+// 16-byte load from shared memory by its 32-bit shared-window address (always an LDS, never a
+// generic load that the compiler could not prove to be shared)
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 // Named barrier over a subset of the CTA's warps (id 1..15; count a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

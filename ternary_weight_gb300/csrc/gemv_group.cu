@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
                                                                  QuantOut qout, Prefetch pf, int K, int log2G) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;                      // kSlots x kSlotBytes
-  uint8_t* xq_s = smem + kRingBytes;         // K bytes, [j][c][16]
+  uint8_t* xq_s = smem + kRingBytes;         // K + 64 bytes, [j][c][16] (c = C is zero)
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
   __shared__ float red_f[kConsumerWarps];
@@ -226,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   const int rg = lane >> log2G;
   const int rpw = 32 >> log2G;
   const int T = (C + G - 1) >> log2G;  // chunk columns per lane (the last may be ragged)
-  const int plane = K >> 2;
+  // activation plane j holds the C chunk columns plus one zero column (index C) that the
+  // ragged lanes of a 32-lane layout read instead of a column past the row's end
+  const int plane = (C + 1) * 16;
 
   // everything that does not depend on the activations is done before the wait: the tile
   // count, the L2 prefetch of the row and the wait for this warp's first tile
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     // amax is a non-negative float (fmaxf drops NaN), so its bits order like unsigned ints
     const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
     if (lane == 0) red_f[warp] = __uint_as_float(wmax);
+    if (threadIdx.x < 4) *reinterpret_cast<uint4*>(xq_s + threadIdx.x * plane + C * 16) = make_uint4(0u, 0u, 0u, 0u);
     named_bar_sync(1, kConsumers);
     {
       const float4 r0 = *reinterpret_cast<const float4*>(&red_f[0]);
@@ -339,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   // the total of step st in the lanes whose top three lane-in-group bits spell st, so the
   // epilogue (one IEEE divide per output) runs for up to 8 rows in parallel. ----
   const int hb = (G >= 8) ? log2G - 3 : 0;  // low lane bits left after the halving levels
+  const uint32_t xq_u = smem_u32(xq_s);
+  const int step_stride = rpw * row_bytes;
   for (int i = warp; i < n_tiles; i += kConsumerWarps) {
     const int slot = i % kSlots, use = i / kSlots;
     if (i != warp) {
@@ -350,28 +355,35 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     float* const out_row = slot_out[slot];
     int32_t* const acc_row = slot_acc[slot];
     const float ws = slot_ws[slot];
-    const uint8_t* tile = ring + slot * kSlotBytes;
+    // this lane's row of step 0; step st is st * step_stride bytes further
+    const uint32_t tile_lane = smem_u32(ring + slot * kSlotBytes) + (uint32_t)(rg * row_bytes);
     // per step: hi = 64 * (sum of bit pairs 0 and 1), lo = 4 * (sum of bit pairs 2 and 3);
     // shifting the weight word left by 2 puts pair 1 under pair 0's mask and pair 3 under
     // pair 2's, so one accumulator serves two pairs at the same scale
     int acc[S][2];
 #pragma unroll
     for (int st = 0; st < S; ++st) acc[st][0] = acc[st][1] = 0;
-    // (fully unrolled up to 4 steps; beyond that the registers of a second column would spill)
-    constexpr int kUnrollCols = S <= 4 ? kMaxColsPerLane : 1;
+    // (fully unrolled up to 6 steps; beyond that the registers of a second column would spill)
+    constexpr int kUnrollCols = S <= 6 ? kMaxColsPerLane : 1;
 #pragma unroll kUnrollCols
     for (int t = 0; t < T; ++t) {
+      // A ragged column past the row's end multiplies the row's last column by the zero
+      // activation column: it adds nothing. Rows past the tile's end (a short last tile)
+      // hold stale bytes; their sums are never written.
       const int c = kl + (t << log2G);
-      const bool col_ok = c < C;
-      const int cc = col_ok ? c : C - 1;
+      const uint32_t w_off = (uint32_t)(min(c, C - 1) * 16);
+      const uint32_t a_off = (uint32_t)((c < C ? c : C) * 16);
+      // all of the column's shared-memory loads first: the S weight vectors, then the
+      // activations
+      uint4 wv[S];
+#pragma unroll
+      for (int st = 0; st < S; ++st) wv[st] = lds128(tile_lane + (uint32_t)(st * step_stride) + w_off);
       uint4 a[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const uint4*>(xq_s + j * plane + cc * 16);
+      for (int j = 0; j < 4; ++j) a[j] = lds128(xq_u + (uint32_t)(j * plane) + a_off);
 #pragma unroll
       for (int st = 0; st < S; ++st) {
-        const int rr = st * rpw + rg;
-        uint4 w = *reinterpret_cast<const uint4*>(tile + rr * row_bytes + cc * 16);
-        if (!col_ok || rr >= rows) w = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 w = wv[st];
         const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
         const uint32_t a0[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
         const uint32_t a1[4] = {a[1].x, a[1].y, a[1].z, a[1].w};
@@ -441,14 +453,14 @@ template <bool BF16, int S>
 cudaError_t launch_s(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
                      int blocks, cudaStream_t stream) {
   auto kern = gemv_group_kernel<BF16, S>;
-  const int smem = kRingBytes + K;
+  const int smem = kRingBytes + K + 64;  // ring, activations + one zero column per plane
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes + kMaxK);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes + kMaxK + 64);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }

@@ -26,6 +26,12 @@
 //    R rows. Weight chunks are streamed with 128-bit
 //    non-allocating loads, one chunk ahead (2*R loads in flight per lane). Partial sums
 //    are reduced with xor-shuffles inside the G-lane group.
+//  * Programmatic dependent launch: the kernel lets the next kernel in the stream launch as
+//    soon as it starts and issues its first weight loads before it waits for the previous
+//    kernel (griddepcontrol.wait), so back-to-back GEMVs keep HBM busy across the kernel
+//    boundary. The activations, scales and row sums are read, and outputs written, only
+//    after the wait. A previous kernel that does not trigger early (any kernel but this
+//    library's GEMV and group kernels) still completes before this one starts.
 #include "bitnet_dev.cuh"
 
 #include <atomic>
@@ -36,6 +42,11 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxActSmem = 64 * 1024;  // bytes of staged activations per CTA
+constexpr int kColBlock = 5;            // chunk columns a lane loads at once (the lane layout keeps
+                                        // a row's walk at 5 columns when K <= 10240)
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   uint4 v;
@@ -56,6 +67,40 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
   const int m0 = blockIdx.y * MT;
   const int C = K >> 6;
   const int plane = K >> 2;  // bytes per j-plane of one staged row
+  pdl_launch_dependents();
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = 1 << log2G;
+  const int kl = lane & (G - 1);
+  const int rg = lane >> log2G;
+  const int rows_per_tile = (32 >> log2G) * R;
+  const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
+  const bool live = tile * rows_per_tile < N;  // warp-uniform
+  const int64_t nbase = tile * rows_per_tile + (int64_t)rg * R;
+  const int T = (C + G - 1) >> log2G;  // chunks per lane per row (the last may be ragged)
+
+  const uint4* wrow[R];
+  bool rv[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    rv[r] = live && (nbase + r) < N;
+    wrow[r] = reinterpret_cast<const uint4*>(wp + (rv[r] ? (nbase + r) : 0) * (int64_t)(K >> 2));
+  }
+  // Weight chunks are loaded kColBlock columns x R rows at a time, all issued before any is
+  // used (up to 320 bytes in flight per lane: HBM needs on the order of 100 KB in flight per
+  // SM). The first block is loaded before the wait for the previous kernel in the stream:
+  // the packed weights are read-only model state, the activations may be that kernel's output.
+  uint4 w[kColBlock][R];
+  auto load_block = [&](int t0) {
+#pragma unroll
+    for (int u = 0; u < kColBlock; ++u) {
+      const int c = kl + ((t0 + u) << log2G);
+#pragma unroll
+      for (int r = 0; r < R; ++r) w[u][r] = (rv[r] && c < C) ? ldg_stream(wrow[r] + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load_block(0);
+  pdl_wait();
 
   // ---- stage MT activation rows (rows past M read as zero) ----
   {
@@ -69,24 +114,7 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
     }
   }
   __syncthreads();
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int G = 1 << log2G;
-  const int kl = lane & (G - 1);
-  const int rg = lane >> log2G;
-  const int rows_per_tile = (32 >> log2G) * R;
-  const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
-  if (tile * rows_per_tile >= N) return;  // warp-uniform; no block barrier follows
-  const int64_t nbase = tile * rows_per_tile + (int64_t)rg * R;
-  const int T = (C + G - 1) >> log2G;  // chunks per lane per row (the last may be ragged)
-
-  const uint4* wrow[R];
-  bool rv[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    rv[r] = (nbase + r) < N;
-    wrow[r] = reinterpret_cast<const uint4*>(wp + (rv[r] ? (nbase + r) : 0) * (int64_t)(K >> 2));
-  }
+  if (!live) return;  // warp-uniform; no block barrier follows
 
   int acc[R][MT][4];
 #pragma unroll
@@ -96,40 +124,31 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[r][m][j] = 0;
 
-  uint4 cur[R];
+  for (int t0 = 0; t0 < T; t0 += kColBlock) {
+    if (t0 > 0) load_block(t0);
 #pragma unroll
-  for (int r = 0; r < R; ++r) cur[r] = (rv[r] && kl < C) ? ldg_stream(wrow[r] + kl) : make_uint4(0u, 0u, 0u, 0u);
-
-  for (int t = 0; t < T; ++t) {
-    const int c = kl + (t << log2G);
-    uint4 nxt[R];
-    if (t + 1 < T) {
+    for (int u = 0; u < kColBlock; ++u) {
+      if (t0 + u >= T) break;  // uniform: the walk is shorter than the block
+      // a ragged last column past the row's end has zero weights (it adds nothing); its
+      // activation load is clamped into the staged row
+      const int c = min(kl + ((t0 + u) << log2G), C - 1);
 #pragma unroll
-      for (int r = 0; r < R; ++r)
-        nxt[r] = (rv[r] && c + G < C) ? ldg_stream(wrow[r] + c + G) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (c < C) {
+      for (int m = 0; m < MT; ++m) {
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
+        for (int j = 0; j < 4; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(act + m * K + j * plane + c * 16);
+          const uint32_t mask = 0xC0C0C0C0u >> (2 * j);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 a = *reinterpret_cast<const uint4*>(act + m * K + j * plane + c * 16);
-        const uint32_t mask = 0xC0C0C0C0u >> (2 * j);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          int s = acc[r][m][j];
-          s = dp4a_us(cur[r].x & mask, a.x, s);
-          s = dp4a_us(cur[r].y & mask, a.y, s);
-          s = dp4a_us(cur[r].z & mask, a.z, s);
-          s = dp4a_us(cur[r].w & mask, a.w, s);
-          acc[r][m][j] = s;
+          for (int r = 0; r < R; ++r) {
+            int s = acc[r][m][j];
+            s = dp4a_us(w[u][r].x & mask, a.x, s);
+            s = dp4a_us(w[u][r].y & mask, a.y, s);
+            s = dp4a_us(w[u][r].z & mask, a.z, s);
+            s = dp4a_us(w[u][r].w & mask, a.w, s);
+            acc[r][m][j] = s;
+          }
         }
       }
-    }
-    }
-    if (t + 1 < T) {
-#pragma unroll
-      for (int r = 0; r < R; ++r) cur[r] = nxt[r];
     }
   }
 
@@ -148,6 +167,144 @@ __global__ void __launch_bounds__(kThreads) gemv_i2s_kernel(const int8_t* __rest
       }
     }
   }
+}
+
+
+// ---------------------------------------------------------------------------------------
+// M = 1, K <= 10240: persistent kernel with a register double buffer.
+// Warp w of the grid takes warp tiles w, w + W, w + 2W, ... (W = warps in the grid); a warp
+// tile is rpw row groups x R rows, and each lane owns the TB chunk columns c = kl + G*u of its
+// R rows (TB = the walk length, at most 5). While the lane computes one tile, the loads of its
+// next tile are in flight: 4 or 5 16-byte chunks per lane, with four CTAs (32 warps) per SM
+// about 64 KB per SM, which keeps HBM streaming without any shared-memory staging of the
+// weights. The activation row is
+// staged once per CTA in shared memory ([j][c][16] plus a zero column at c = C that the
+// ragged lanes of a 32-lane layout read).
+// ---------------------------------------------------------------------------------------
+template <int R, int TB, int LB>
+__global__ void __launch_bounds__(kThreads, LB) gemv_m1_kernel(const int8_t* __restrict__ xq,
+                                                              const float* __restrict__ act_scale,
+                                                              const int32_t* __restrict__ rowsum,
+                                                              const uint8_t* __restrict__ wp, float w_scale,
+                                                              float* __restrict__ out, int32_t* __restrict__ acc_out,
+                                                              int N, int K, int log2G) {
+  extern __shared__ __align__(16) uint8_t act[];  // 4 planes x (C + 1) x 16 bytes
+  const int C = K >> 6;
+  const int plane = (C + 1) * 16;
+  pdl_launch_dependents();
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = 1 << log2G;
+  const int kl = lane & (G - 1);
+  const int rg = lane >> log2G;
+  const int rows_per_tile = (32 >> log2G) * R;
+  const int n_tiles = (N + rows_per_tile - 1) / rows_per_tile;
+  const int stride = gridDim.x * kWarps;
+  const int row_chunks = C;  // 16-byte chunks per packed row (K/4 bytes)
+  const uint4* wbase = reinterpret_cast<const uint4*>(wp);
+
+  // chunk (u, r) of warp tile `tile` for this lane, or zero past the matrix
+  auto load_tile = [&](int tile, uint4 (&buf)[TB][R]) {
+    const int n0 = tile * rows_per_tile + rg * R;
+#pragma unroll
+    for (int u = 0; u < TB; ++u) {
+      const int c = kl + (u << log2G);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const bool ok = tile < n_tiles && n0 + r < N && c < C;
+        buf[u][r] = ok ? ldg_stream(wbase + (int64_t)(n0 + r) * row_chunks + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+
+  uint4 bufA[TB][R], bufB[TB][R];
+  int tile = blockIdx.x * kWarps + warp;
+  // the first tile is loaded before the wait for the previous kernel in the stream: the
+  // packed weights are read-only model state, the activations may be that kernel's output
+  load_tile(tile, bufA);
+  pdl_wait();
+  {
+    const int pieces = K >> 4;  // piece p covers k = 16p..16p+15
+    for (int p = threadIdx.x; p < pieces; p += kThreads) {
+      const int i = p >> 3, j = (p >> 1) & 3, h = p & 1;
+      *reinterpret_cast<uint4*>(act + j * plane + (2 * i + h) * 16) = __ldg(reinterpret_cast<const uint4*>(xq) + p);
+    }
+    if (threadIdx.x < 4) *reinterpret_cast<uint4*>(act + threadIdx.x * plane + C * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int rs = __ldg(rowsum);
+  const float sx = __ldg(act_scale);
+  __syncthreads();
+
+  auto compute_store = [&](int t, const uint4 (&buf)[TB][R]) {
+    int acc[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[r][j] = 0;
+#pragma unroll
+    for (int u = 0; u < TB; ++u) {
+      const int c = kl + (u << log2G);
+      const int ca = c < C ? c : C;  // a ragged column reads the zero column
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 a = *reinterpret_cast<const uint4*>(act + j * plane + ca * 16);
+        const uint32_t mask = 0xC0C0C0C0u >> (2 * j);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          int v = acc[r][j];
+          v = dp4a_us(buf[u][r].x & mask, a.x, v);
+          v = dp4a_us(buf[u][r].y & mask, a.y, v);
+          v = dp4a_us(buf[u][r].z & mask, a.z, v);
+          v = dp4a_us(buf[u][r].w & mask, a.w, v);
+          acc[r][j] = v;
+        }
+      }
+    }
+    const int n0 = t * rows_per_tile + rg * R;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      int raw = (acc[r][0] >> 6) + (acc[r][1] >> 4) + (acc[r][2] >> 2) + acc[r][3];
+      for (int o = G >> 1; o > 0; o >>= 1) raw += __shfl_xor_sync(0xffffffffu, raw, o);
+      if (kl == 0 && n0 + r < N) {
+        const int a = raw - rs;
+        out[n0 + r] = __fmul_rn(__fdiv_rn(__int2float_rn(a), sx), w_scale);
+        if (acc_out) acc_out[n0 + r] = a;
+      }
+    }
+  };
+
+  // two tiles per trip, so the buffers swap roles without copies; tile < n_tiles is
+  // warp-uniform, so the shuffles in compute_store see full warps
+  for (; tile < n_tiles; tile += 2 * stride) {
+    load_tile(tile + stride, bufB);
+    compute_store(tile, bufA);
+    if (tile + stride >= n_tiles) break;
+    load_tile(tile + 2 * stride, bufA);
+    compute_store(tile + stride, bufB);
+  }
+}
+
+template <int R, int TB, int LB>
+cudaError_t launch_m1(const int8_t* xq, const float* s, const int32_t* rs, const uint8_t* wp, float w_scale,
+                      float* out, int32_t* acc_out, int N, int K, int log2G, int num_sms, cudaStream_t stream) {
+  auto kern = gemv_m1_kernel<R, TB, LB>;
+  const int smem = K + 64;
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;  // K <= 10240 keeps it under 48 KB
+  const int rows_per_tile = (32 >> log2G) * R;
+  const int64_t tiles = ((int64_t)N + rows_per_tile - 1) / rows_per_tile;
+  int64_t blocks = (tiles + kWarps - 1) / kWarps;
+  if (blocks > (int64_t)LB * num_sms) blocks = (int64_t)LB * num_sms;  // persistent: LB CTAs per SM
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, xq, s, rs, wp, w_scale, out, acc_out, N, K, log2G);
 }
 
 template <int MT, int R>
@@ -170,9 +327,17 @@ cudaError_t launch_cfg(const int8_t* xq, const float* s, const int32_t* rs, cons
   }
   const int rows_per_tile = (32 >> log2G) * R;
   const int64_t tiles = ((int64_t)N + rows_per_tile - 1) / rows_per_tile;
-  dim3 grid((unsigned)((tiles + kWarps - 1) / kWarps), (unsigned)((M + MT - 1) / MT));
-  kern<<<grid, kThreads, smem, stream>>>(xq, s, rs, wp, w_scale, out, acc_out, M, N, K, log2G);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((tiles + kWarps - 1) / kWarps), (unsigned)((M + MT - 1) / MT));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, xq, s, rs, wp, w_scale, out, acc_out, M, N, K, log2G);
 }
 
 }  // namespace
@@ -188,6 +353,37 @@ cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int3
   while (log2G > 1 && (C & ((1 << log2G) - 1)) != 0) --log2G;  // C is even, so G >= 2 divides it
   if ((C >> log2G) > 5) log2G = 5;
   const int rpw = 32 >> log2G;
+
+  if (M == 1 && K <= 10240) {
+    // walk length T <= 5 (the lane layout above). Large matrices (at least two tiles per
+    // warp at four CTAs per SM): tiles of 2 to 5 chunks per lane, so the double buffer fits
+    // in 64 registers and four CTAs (32 warps, about 64 KB of loads in flight) share an SM.
+    // Smaller ones: two CTAs per SM and tiles of 5 to 8 chunks per lane (measured: 5 beats
+    // 10 for the 8-lane K = 2560 layouts).
+    const int T = (C + (1 << log2G) - 1) >> log2G;
+    const int rpw1 = 32 >> log2G;
+    const int64_t tiles_r1 = ((int64_t)N + rpw1 - 1) / rpw1;
+    const bool large = tiles_r1 >= 2LL * 4 * kWarps * num_sms;
+#define BITNET_M1(R_, TB_, LB_) \
+  launch_m1<R_, TB_, LB_>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, N, K, log2G, num_sms, stream)
+    if (large) {
+      switch (T) {
+        case 1: return BITNET_M1(2, 1, 4);
+        case 2: return BITNET_M1(2, 2, 4);
+        case 3: return BITNET_M1(1, 3, 4);
+        case 4: return BITNET_M1(1, 4, 4);
+        default: return BITNET_M1(1, 5, 4);
+      }
+    }
+    switch (T) {
+      case 1: return BITNET_M1(8, 1, 2);
+      case 2: return BITNET_M1(4, 2, 2);
+      case 3: return BITNET_M1(2, 3, 2);
+      case 4: return BITNET_M1(2, 4, 2);
+      default: return BITNET_M1(1, 5, 2);
+    }
+#undef BITNET_M1
+  }
 
   // activation rows per CTA: next power of two >= M, at most 8, within the smem budget
   int MT = 1;

@@ -146,6 +146,17 @@ def test_chain_parity_gemv(M, N, K, dtype):
     assert_chain_equal(g, o)
 
 
+# M = 1 matrices large enough for the persistent GEMV's many-CTA configuration (at least two
+# warp tiles per warp with four CTAs per SM on 152 SMs), 32-lane (ragged and not) and 8-lane
+# layouts; every output is compared.
+@pytest.mark.parametrize("N,K", [(10000, 8192), (9800, 6912), (9729, 10240), (38920, 2560)])
+def test_chain_parity_gemv_m1_large(N, K):
+    x = workloads.activations(1, K, seed=310 + K, dtype="bf16", outlier_p=0.01)
+    w = workloads.ternary_weights(N, K, seed=311 + N)
+    g, o = run_chain(x, "bf16", w, workloads.weight_scale(N, K, 312))
+    assert_chain_equal(g, o)
+
+
 GEMM_CHAIN = [
     (1, 256, 128, "f32"), (65, 300, 2560, "bf16"), (127, 257, 384, "bf16"), (128, 256, 2560, "bf16"),
     (129, 513, 1024, "f32"), (200, 1000, 6912, "bf16"), (300, 700, 2560, "bf16"), (256, 640, 8192, "bf16"),
