@@ -37,17 +37,30 @@ namespace bitnet {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;  // one 128-byte swizzle row of fp16
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 4;
 constexpr int THREADS = (2 + EPI_WARPS) * 32;  // producer, MMA, 4 epilogue warps
-constexpr uint32_t TMEM_COLS = 512;             // two 256-column fp32 accumulators
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
-constexpr uint32_t IDESC = make_idesc_f16_f32(BM, BN);
+constexpr uint32_t TMEM_COLS = 512;             // two accumulators of BN <= 256 fp32 columns
+constexpr int kSmemBudget = 227 * 1024;
+// epilogue staging: one 32 x 33 fp32 block per epilogue warp (the padding column keeps both the
+// row-wise writes and the column-wise reads free of bank conflicts)
+constexpr int EPI_PITCH = 33;
+constexpr int EPI_SMEM = EPI_WARPS * 32 * EPI_PITCH * 4;
+
+// Tile width BN (the MMA's N) is chosen per problem; the ring takes as many stages as fit.
+template <int BN>
+struct TileCfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int RING_BUDGET = kSmemBudget - 1024 - 1024 - EPI_SMEM;
+  static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 6 ? RING_BUDGET / STAGE_BYTES : 6;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + EPI_SMEM;
+  static constexpr uint32_t IDESC = make_idesc_f16_f32(BM, BN);
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "MMA N and the 32-column epilogue steps");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzle atoms");
+  static_assert(STAGES >= 3, "pipeline depth");
+};
 
 // ---------------------------------------------------------------------------- expansion
 __device__ __forceinline__ uint2 codes4_to_f16(uint32_t codes) {  // 4 codes (one per byte) -> 4 fp16
@@ -105,12 +118,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1) gemm_f16_ws_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                  const __grid_constant__ CUtensorMap tmB,
                                                                  const float* __restrict__ act_scale,
                                                                  const int32_t* __restrict__ rowsum, float w_scale,
                                                                  float* __restrict__ out, int32_t* __restrict__ acc_out,
                                                                  int M, int N, int K) {
+  using Cfg = TileCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES, STAGE_BYTES = Cfg::STAGE_BYTES;
+  constexpr uint32_t IDESC = Cfg::IDESC;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
@@ -122,6 +139,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_f16_ws_kernel(const __grid_co
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);  // 1024-byte aligned atoms
   const uint32_t ring_addr = smem_u32(ring);
+  float* epi_stage = reinterpret_cast<float*>(ring + STAGES * STAGE_BYTES);  // EPI_SMEM bytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
   const int tiles = num_m * num_n;
@@ -195,34 +213,53 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_f16_ws_kernel(const __grid_co
     }
   } else {
     // ================================ epilogue (warps 2-5) ================================
+    // Warp q reads accumulator lanes 32q..32q+31 (rows m0 + 32q + lane) 32 columns at a time,
+    // finishes them in registers, and writes them through its 32 x 33 staging block so that
+    // each store instruction covers 32 consecutive columns of one row (128 contiguous bytes).
     const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    float* blk = epi_stage + (warp - 2) * 32 * EPI_PITCH;
+    int* blk_i = reinterpret_cast<int*>(blk);
     int lt = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
       const int acc = lt & 1, ua = lt >> 1;
       if (!mbar_wait(&tfull_bar[acc], ua & 1, &abort)) break;
       tc_fence_after();
       const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
-      const int m = m0 + q * 32 + lane;
-      const bool mv = m < M;
-      const int rs = mv ? __ldg(rowsum + m) : 0;
-      const float sc = mv ? __ldg(act_scale + m) : 1.0f;
-      const int64_t rowoff = (int64_t)m * N;
+      const int mrow = m0 + q * 32 + lane;  // this lane's accumulator row
+      const bool mv = mrow < M;
+      const int rs = mv ? __ldg(rowsum + mrow) : 0;
+      const float sc = mv ? __ldg(act_scale + mrow) : 1.0f;
 #pragma unroll 1
       for (int cb = 0; cb < BN; cb += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + cb), v);
         tmem_ld_wait();
-        if (mv) {
+        const int n = n0 + cb + lane;  // the column this lane stores
+        // pass 1: acc = raw - rowsum, staged row-wise (lane = row)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int n = n0 + cb + e;
-            if (n < N) {
-              const int a = __float2int_rn(__uint_as_float(v[e])) - rs;
-              out[rowoff + n] = __fmul_rn(__fdiv_rn(__int2float_rn(a), sc), w_scale);
-              if (acc_out) acc_out[rowoff + n] = a;
-            }
+        for (int e = 0; e < 32; ++e) blk_i[lane * EPI_PITCH + e] = __float2int_rn(__uint_as_float(v[e])) - rs;
+        __syncwarp();
+        if (acc_out) {
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r) {
+            const int m = m0 + q * 32 + r;
+            if (m < M && n < N) acc_out[(int64_t)m * N + n] = blk_i[r * EPI_PITCH + lane];
           }
         }
+        __syncwarp();
+        // pass 2: out = (acc / s) * w_scale, in the row's own lane, then stored column-wise
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int a = blk_i[lane * EPI_PITCH + e];
+          blk[lane * EPI_PITCH + e] = __fmul_rn(__fdiv_rn(__int2float_rn(a), sc), w_scale);
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+          const int m = m0 + q * 32 + r;
+          if (m < M && n < N) out[(int64_t)m * N + n] = blk[r * EPI_PITCH + lane];
+        }
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
@@ -270,6 +307,30 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int b
 
 int64_t align256(int64_t v) { return (v + 255) & ~(int64_t)255; }
 
+template <int BN>
+cudaError_t launch_ws_gemm(const uint16_t* x16, const uint16_t* w16, const float* act_scale, const int32_t* rowsum,
+                           float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int num_sms,
+                           cudaStream_t stream) {
+  using Cfg = TileCfg<BN>;
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, x16, M, K, BM) || !make_map(&mB, w16, N, K, BN)) return cudaErrorInvalidValue;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gemm_f16_ws_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  gemm_f16_ws_kernel<BN><<<grid, THREADS, Cfg::SMEM_BYTES, stream>>>(mA, mB, act_scale, rowsum, w_scale, out, acc_out,
+                                                                     (int)M, (int)N, (int)K);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t read_clear_device_error_gemm_ws(int* value) {
@@ -295,24 +356,26 @@ cudaError_t launch_gemm_tc_ws(const int8_t* xq, const float* act_scale, const in
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mA, mB;
-  if (!make_map(&mA, x16, M, K, BM) || !make_map(&mB, w16, N, K, BN)) return cudaErrorInvalidValue;
-
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(gemm_f16_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+  // Tile width: the persistent CTAs run the tiles in rounds of num_sms, and a tile's time
+  // grows with BN plus a fixed part (operand A's loads and per-step overheads, taken as 32
+  // columns' worth), so pick the BN with the least rounds x (BN + 32), ties to the wider.
+  // For M = 4096, N = 2560: BN = 256 needs 3 rounds of 320 tiles (2.1 waves), BN = 192 needs
+  // 3 rounds of 448 (2.95 waves) at about 0.78 of the time per tile.
+  const int64_t num_m = (M + BM - 1) / BM;
+  auto cost = [&](int bn) {
+    const int64_t tiles = num_m * ((N + bn - 1) / bn);
+    return ((tiles + num_sms - 1) / num_sms) * (bn + 32);
+  };
+  int bn = 256;
+  for (int cand : {224, 192, 160, 128})
+    if (cost(cand) < cost(bn)) bn = cand;
+  switch (bn) {
+    case 224: return launch_ws_gemm<224>(x16, w16, act_scale, rowsum, w_scale, out, acc_out, M, N, K, num_sms, stream);
+    case 192: return launch_ws_gemm<192>(x16, w16, act_scale, rowsum, w_scale, out, acc_out, M, N, K, num_sms, stream);
+    case 160: return launch_ws_gemm<160>(x16, w16, act_scale, rowsum, w_scale, out, acc_out, M, N, K, num_sms, stream);
+    case 128: return launch_ws_gemm<128>(x16, w16, act_scale, rowsum, w_scale, out, acc_out, M, N, K, num_sms, stream);
+    default: return launch_ws_gemm<256>(x16, w16, act_scale, rowsum, w_scale, out, acc_out, M, N, K, num_sms, stream);
   }
-  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  gemm_f16_ws_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mA, mB, act_scale, rowsum, w_scale, out, acc_out, (int)M,
-                                                            (int)N, (int)K);
-  return cudaGetLastError();
 }
 
 }  // namespace bitnet
