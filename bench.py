@@ -53,6 +53,7 @@ def parse_args(argv=None):
     p.add_argument("--layers", type=int, default=N_LAYERS)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-gemv-leg", action="store_true", help="skip the 100B-class GEMV leg of the default line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill"], default="decode_sweep",
                    help="decode_sweep (default, the headline) or one single-kernel leg")
@@ -489,6 +490,7 @@ def run_ours(args):
     e2e_bps, _ = aggregate([r[0] for r in per_rank_e2e], [r[1] for r in per_rank_e2e])
 
     prefill = None if args.no_prefill else kernel_leg("prefill", device, peaks)
+    gemv_100b = None if args.no_gemv_leg else kernel_leg("gemv_100b", device, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -516,6 +518,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": stack.out_elems * 4,
                 "note": "pinned host activations -> device, graph step, all projection outputs -> host, each step"},
         "prefill": prefill,
+        "gemv_100b": gemv_100b,
         "cpu_baseline": cpu,
     }
     if rank == 0:
