@@ -62,9 +62,10 @@ extern "C" {
 #define BITNET_BF16 1
 
 /* ---- matmul kernel selection (bitnet_i2s_matmul_algo) ---- */
-#define BITNET_ALGO_AUTO 0   /* decode GEMV for M <= 64, tensor-core GEMM otherwise */
+#define BITNET_ALGO_AUTO 0   /* GEMV M <= 16, few-token kernel M <= 64, GEMM beyond */
 #define BITNET_ALGO_GEMV 1   /* force the dp4a decode GEMV (any M)                   */
 #define BITNET_ALGO_GEMM 2   /* force the tcgen05 tensor-core GEMM (any M)           */
+#define BITNET_ALGO_SMALLM 3 /* force the few-token tensor-core kernel (M <= 64)     */
 
 /* Library ABI version (major*100 + minor). */
 BITNET_API int bitnet_version(void);
@@ -118,14 +119,17 @@ BITNET_API int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, 
  *   w_scale   : per-tensor weight scale alpha_W = mean|W| of the source weights
  *   out       : M x N fp32, out[m][n] = ((float)acc[m][n] / s[m]) * w_scale  (device, written)
  *   acc_out   : optional (may be NULL) M x N int32, acc[m][n] = sum_k (code-1)*xq (written)
- *   M, N >= 1; M, N <= 2^31 - 1; K >= 128, K % 128 == 0, K <= 65536. The tensor-core GEMM
- *   takes K <= 32768 (BITNET_EINVAL if forced beyond); auto dispatch then uses the GEMV.
+ *   M, N >= 1; M, N <= 2^31 - 1; K >= 128, K % 128 == 0, K <= 65536. The tensor-core kernels
+ *   take K <= 32768 (BITNET_EINVAL if forced beyond); auto dispatch then uses the GEMV.
  *   xq and wp must be 16-byte aligned; out and acc_out 4-byte aligned.
  *   The 2-bit field value 3 never comes out of bitnet_pack_i2s; if present it is used
  *   arithmetically (3 - 1 = +2), the same rule as the unpacking of [DeepDive] §8.
- *   For M <= 64 a dp4a GEMV streams the packed weights; for larger M a tcgen05 tensor-core
- *   GEMM expands the codes in shared memory (exact: every partial sum is an integer
- *   below 2^24 accumulated in fp32). Both give bit-identical results.
+ *   Kernel choice: for M <= 16 a dp4a GEMV streams the packed weights. For 17 <= M <= 64
+ *   a few-token tcgen05 kernel decodes each weight once into fp16 for all token rows
+ *   (weights as the MMA's M, K split over a thread-block cluster). For larger M a tcgen05
+ *   tile GEMM expands the codes in shared memory. The tensor-core paths are exact: every
+ *   partial sum is an integer below 2^24 accumulated in fp32. All give bit-identical
+ *   results.
  */
 BITNET_API int bitnet_i2s_matmul(const int8_t *xq, const float *act_scale, const int32_t *rowsum,
                                  const uint8_t *wp, float w_scale, float *out, int32_t *acc_out,

@@ -23,7 +23,7 @@ BITNET_ETIMEOUT = -5
 BITNET_F32 = 0
 BITNET_BF16 = 1
 
-ALGO = {"auto": 0, "gemv": 1, "gemm": 2}
+ALGO = {"auto": 0, "gemv": 1, "gemm": 2, "smallm": 3}
 
 # every entry point of include/bitnet.h with its ctypes signature
 _P = ctypes.c_void_p

@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap and its enums (the encoder itself comes from the runtime)
 #include <cuda_runtime.h>
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030)
@@ -98,6 +99,18 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, L2 only); src_bytes 0 writes zeros
+// and reads nothing. dst and src 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// One arrival on the mbarrier once every cp.async this thread issued so far has completed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Named barrier over a subset of the CTA's warps (id 1..15; count a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -160,7 +173,44 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 8 consecutive 32-bit columns (same lane mapping as the x32 form).
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------
+// Thread-block clusters: rank, barrier, and loads from a peer CTA's shared memory
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives, then waits; shared-memory writes before
+// the arrive are visible to the cluster's CTAs after the wait.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t smem_addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
 
 // Shared-memory matrix descriptor (tcgen05 format), K-major operand with the 128-byte
 // swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked along M/N.
@@ -236,10 +286,22 @@ cudaError_t launch_quant_act(const void* x, int dtype, int64_t M, int64_t K, int
 cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
                             float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
                             int num_sms, cudaStream_t stream);
+// Few-token tensor-core matmul (gemm_smallm.cu): 1 <= M <= 64, K <= 32768.
+bool gemm_smallm_supported(int64_t M, int64_t K);
+cudaError_t launch_gemm_smallm(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
+                               float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
+                               int num_sms, cudaStream_t stream);
+cudaError_t read_clear_device_error_smallm(int* value);
 // Read and clear the device error word of each translation unit that waits (synchronous).
 cudaError_t read_clear_device_error_gemm(int* value);
 cudaError_t read_clear_device_error_gemm_ws(int* value);
 cudaError_t read_clear_device_error_gemv_group(int* value);
+
+// Host: encode a 2-D tiled TMA tensor map over a row-major [rows][inner] array
+// (gemm_tc_ws.cu). False if the driver entry point is missing or the encoder refuses.
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner_elems,
+                   uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle);
 
 // Expand-then-GEMM path (gemm_tc_ws.cu): workspace bytes, and the launch (K <= 32768).
 int64_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K);

@@ -15,7 +15,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxK = 1 << 16;          // staged activation rows must fit shared memory
 constexpr int64_t kMaxKTensorCore = 1 << 15; // exact fp32 accumulation bound of the GEMM
-constexpr int64_t kGemvMaxM = 64;           // auto dispatch: GEMV up to here, GEMM above
+constexpr int64_t kGemvMaxM = 64;           // auto dispatch: GEMV or few-token kernel up to here, GEMM above
+constexpr int64_t kSmallmMinM = 17;         // auto dispatch: the few-token tensor-core kernel from here
 
 // per-device: 0 = unchecked, 1 = sm_103 ok, -1 = unsupported; and SM count
 std::atomic<int> g_dev_state[kMaxDevices];
@@ -97,19 +98,38 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
                                       int64_t N, int64_t K, int algo, void* stream) {
   if (!xq || !act_scale || !rowsum || !wp || !out) return BITNET_EINVAL;
   if (M < 1 || M > INT32_MAX || N < 1 || N > INT32_MAX || !valid_k(K)) return BITNET_EINVAL;
-  if (algo < BITNET_ALGO_AUTO || algo > BITNET_ALGO_GEMM) return BITNET_EINVAL;
+  if (algo < BITNET_ALGO_AUTO || algo > BITNET_ALGO_SMALLM) return BITNET_EINVAL;
   if (!aligned(xq, 16) || !aligned(wp, 16) || !aligned(act_scale, 4) || !aligned(rowsum, 4) || !aligned(out, 4) ||
       (acc_out && !aligned(acc_out, 4)))
     return BITNET_EALIGN;
-  if (algo == BITNET_ALGO_AUTO) algo = (M <= kGemvMaxM || K > kMaxKTensorCore) ? BITNET_ALGO_GEMV : BITNET_ALGO_GEMM;
+  if (algo == BITNET_ALGO_AUTO) {
+    // dp4a GEMV up to 16 tokens (it decodes each weight word once per token row, cheap while
+    // the rows are few); the few-token tensor-core kernel from 17 to 64 (each weight decoded
+    // once for all rows); the tile GEMM beyond
+    if (K > kMaxKTensorCore || M <= kSmallmMinM - 1)
+      algo = BITNET_ALGO_GEMV;
+    else if (M <= kGemvMaxM)
+      algo = BITNET_ALGO_SMALLM;
+    else
+      algo = BITNET_ALGO_GEMM;
+  }
   if (algo == BITNET_ALGO_GEMM && (K > kMaxKTensorCore || M > 65535LL * 128)) return BITNET_EINVAL;
   if (algo == BITNET_ALGO_GEMV && M > 65535LL * 8) return BITNET_EINVAL;
+  if (algo == BITNET_ALGO_SMALLM && !gemm_smallm_supported(M, K)) return BITNET_EINVAL;
   int sms = 0;
   if (int st = check_device(&sms)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (algo == BITNET_ALGO_GEMV)
-                      ? launch_gemv_i2s(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s)
-                      : launch_gemm_i2s_tc(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
+  cudaError_t e;
+  switch (algo) {
+    case BITNET_ALGO_GEMV:
+      e = launch_gemv_i2s(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
+      break;
+    case BITNET_ALGO_SMALLM:
+      e = launch_gemm_smallm(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
+      break;
+    default:
+      e = launch_gemm_i2s_tc(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
+  }
   return status_of(e);
 }
 
@@ -216,7 +236,7 @@ BITNET_API int bitnet_last_device_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return BITNET_ECUDA;
   int status = BITNET_OK;
   cudaError_t (*readers[])(int*) = {read_clear_device_error_gemm, read_clear_device_error_gemm_ws,
-                                    read_clear_device_error_gemv_group};
+                                    read_clear_device_error_gemv_group, read_clear_device_error_smallm};
   for (auto rd : readers) {
     int v = 0;
     if (rd(&v) != cudaSuccess) return BITNET_ECUDA;

@@ -27,7 +27,6 @@
 // Every wait is bounded; a timeout is recorded in the device error word.
 #include "bitnet_dev.cuh"
 
-#include <cuda.h>  // CUtensorMap and its enums only; the encoder is fetched from the runtime
 #include <cuda_fp16.h>
 
 #include <atomic>
@@ -294,15 +293,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D fp16 tensor [rows][K] (K contiguous), box BK x box_rows, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
-  auto encode = tensor_map_encoder();
-  if (!encode) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, (uint64_t)K, (uint64_t)rows, (uint64_t)K * 2, BK,
+                       (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int64_t align256(int64_t v) { return (v + 255) & ~(int64_t)255; }
@@ -332,6 +324,19 @@ cudaError_t launch_ws_gemm(const uint16_t* x16, const uint16_t* w16, const float
 }
 
 }  // namespace
+
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner_elems,
+                   uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner_elems, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t read_clear_device_error_gemm_ws(int* value) {
   int zero = 0;

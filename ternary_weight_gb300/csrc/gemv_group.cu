@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   uint8_t* xq_s = smem + kRingBytes;         // K + 64 bytes, [j][c][16] (c = C is zero)
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
-  __shared__ float red_f[kConsumerWarps];
-  __shared__ int red_i[kConsumerWarps];
+  __shared__ __align__(16) float red_f[kConsumerWarps];  // read back as float4
+  __shared__ __align__(16) int red_i[kConsumerWarps];    // read back as int4
   // the tile held by each ring slot (written by the producer before its release-arrive on
   // the slot's full barrier, read by the consumer after its acquire-wait)
   __shared__ int slot_rows[kSlots];

@@ -146,6 +146,42 @@ def test_chain_parity_gemv(M, N, K, dtype):
     assert_chain_equal(g, o)
 
 
+# The few-token tensor-core kernel, forced: every MMA width (16/32/48/64 tokens), ragged N (a
+# partial last 128-row tile), K with a half last 256-k stage, K splits over clusters of 1 to 8
+# CTAs, M = 1, and the decode shapes at M = 4 / 16 / 64.
+SMALLM_CHAIN = [
+    (1, 256, 128, "f32"), (2, 300, 2560, "bf16"), (4, 6912, 2560, "bf16"), (8, 1000, 8192, "bf16"),
+    (16, 2560, 6912, "bf16"), (17, 700, 384, "f32"), (33, 129, 1024, "bf16"), (48, 2560, 2560, "f32"),
+    (63, 513, 10240, "bf16"), (64, 6912, 2560, "bf16"), (64, 2560, 6912, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype", SMALLM_CHAIN)
+def test_chain_parity_smallm(M, N, K, dtype):
+    x = workloads.activations(M, K, seed=320 + M, dtype=dtype, outlier_p=0.01)
+    w = workloads.ternary_weights(N, K, seed=321 + N)
+    g, o = run_chain(x, dtype, w, workloads.weight_scale(N, K, 322), algo="smallm")
+    assert_chain_equal(g, o)
+    assert binding.last_device_error() == 0
+
+
+def test_smallm_code3_and_max_magnitude():
+    """Bytes with code 3 (weight +2) and activations at +-127 everywhere: the largest exact
+    accumulators the kernel can see, through the few-token path."""
+    M, N, K = 16, 384, 6912
+    xq = np.where(np.arange(M * K).reshape(M, K) % 3 == 0, -127, 127).astype(np.int8)
+    s = np.full(M, 1.0, dtype=np.float32)
+    rs = xq.astype(np.int64).sum(axis=1).astype(np.int32)
+    wp = workloads.random_packed_bytes(N, K, seed=323)
+    g_out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    g_acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    binding.i2s_matmul(dev(xq), dev(s), dev(rs), dev(wp), 0.5, out=g_out, acc_out=g_acc, algo="smallm")
+    torch.cuda.synchronize()
+    o_out, o_acc = oracle.ternary_matmul(xq, s, wp, 0.5, nthreads=NT)
+    assert np.array_equal(host(g_acc), o_acc)
+    assert np.array_equal(host(g_out).view(np.uint32), o_out.view(np.uint32))
+
+
 # M = 1 matrices large enough for the persistent GEMV's many-CTA configuration (at least two
 # warp tiles per warp with four CTAs per SM on 152 SMs), 32-lane (ragged and not) and 8-lane
 # layouts; every output is compared.
