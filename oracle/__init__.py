@@ -64,6 +64,9 @@ def _load():
     lib.oracle_ternary_matmul.restype = ctypes.c_int
     lib.oracle_raw_code_dot.argtypes = [P, P, P, I64, I64, I64]
     lib.oracle_raw_code_dot.restype = ctypes.c_int
+    for fn in (lib.oracle_quant_weight_f32, lib.oracle_quant_weight_bf16):
+        fn.argtypes = [P, I64, I64, ctypes.c_int, P, P]
+        fn.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -152,6 +155,34 @@ def raw_code_dot(xq: np.ndarray, wp: np.ndarray) -> np.ndarray:
     if _load().oracle_raw_code_dot(_ptr(xq), _ptr(wp), _ptr(raw), M, N, K) != 0:
         raise RuntimeError("oracle_raw_code_dot failed")
     return raw
+
+
+QUANT_WEIGHT_MODES = {"absmean": 0, "sign": 1}
+
+
+def quant_weight(w: np.ndarray, dtype: str = "f32", mode: str = "absmean"):
+    """Weight ternarisation of an N x K matrix (float32, or uint16 bf16 bit patterns).
+
+    Returns (q int8 N x K in {-1, 0, +1}, scale float32): AbsMean (scale = max(mean|w|, 1e-5),
+    q = clip(rne(w / scale), -1, 1)) or the sign rule (q = 0 where |w| < 1e-6, else sign(w);
+    scale = max|w|).
+    """
+    lib = _load()
+    if dtype == "f32":
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        fn = lib.oracle_quant_weight_f32
+    elif dtype == "bf16":
+        w = np.ascontiguousarray(w, dtype=np.uint16)
+        fn = lib.oracle_quant_weight_bf16
+    else:
+        raise ValueError(dtype)
+    N, K = w.shape
+    q = np.empty((N, K), dtype=np.int8)
+    scale = np.empty(1, dtype=np.float32)
+    rc = fn(_ptr(w), N, K, QUANT_WEIGHT_MODES[mode], _ptr(q), _ptr(scale))
+    if rc != 0:
+        raise RuntimeError("oracle quant_weight failed: %d" % rc)
+    return q, scale[0]
 
 
 def default_threads() -> int:

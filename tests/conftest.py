@@ -14,7 +14,8 @@ def pytest_configure(config):
 
 
 def read_golden(name):
-    """Parse a tests/golden/*.txt fixture: 'key = v1 v2 ...' lines, '#' comments."""
+    """Parse a tests/golden/*.txt fixture: 'key = v1 v2 ...' lines (ints, or floats where written
+    with a point or exponent), '#' comments."""
     out = {}
     with open(os.path.join(ROOT, "tests", "golden", name)) as f:
         for line in f:
@@ -22,5 +23,5 @@ def read_golden(name):
             if not line or line.startswith("#"):
                 continue
             key, _, val = line.partition("=")
-            out[key.strip()] = [int(v) for v in val.split()]
+            out[key.strip()] = [float(v) if any(c in v for c in ".eE") else int(v) for v in val.split()]
     return out

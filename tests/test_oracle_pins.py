@@ -7,6 +7,8 @@ an invariant, or brute force on tiny inputs. A plausible mistake in the oracle -
 reversed bit order, a linear instead of 4x32 interleave, a dropped -1, a wrong scale
 direction, round-half-away instead of round-half-even -- fails at least one of them.
 """
+from fractions import Fraction
+
 import numpy as np
 import pytest
 import torch
@@ -336,3 +338,74 @@ def test_quant_uses_multiply_form_of_scale():
     xq, s_or, _ = oracle.quant_act(row)
     assert s_or[0] == s
     assert np.array_equal(xq[0, : len(xs)].astype(np.float64), np.array(expect))
+
+
+# ----------------------------------------------------------------------------- weight ternarisation
+
+def test_absmean_page_example():
+    """[DeepDive] §6-2: mean|w| = 0.4 and w / 0.4 = [-1.5, -0.5, 0.5, 1.5] as printed; with
+    round-half-to-even (numpy's round, the reading taken) the codes are [-1, 0, 0, 1], where
+    rounding half away from zero would give [-1, -1, 1, 1]."""
+    g = read_golden("absmean_example.txt")
+    w = np.array([g["w"]], dtype=np.float32)
+    q, scale = oracle.quant_weight(w)
+    assert scale == np.float32(g["mean"][0])
+    assert np.array_equal(w / np.float32(scale), np.array([g["ratio"]], dtype=np.float32))
+    assert q.tolist() == [[-1, 0, 0, 1]]
+
+
+def test_absmean_rounding_ties_go_to_even():
+    # mean|w| = 1 exactly, so w / scale is w: +-0.5 round to 0, +-1.5 to +-2 (clipped to +-1)
+    w = np.array([[0.5, -0.5, 1.5, -1.5], [1.0, -1.0, 0.5, 1.5]], dtype=np.float32)
+    q, scale = oracle.quant_weight(w)
+    assert scale == 1.0
+    assert q.tolist() == [[0, 0, 1, -1], [1, -1, 0, 1]]
+
+
+def test_absmean_all_zero_uses_the_floor():
+    q, scale = oracle.quant_weight(np.zeros((3, 256), dtype=np.float32))
+    assert scale == np.float32(1e-5) and not q.any()
+
+
+@pytest.mark.parametrize("c", [0.25, -3.0, 2.0 ** -10, -0.015625])
+def test_absmean_constant_matrix(c):
+    # N*K = 2^10 copies of |c| sum exactly in fp64, so the mean is |c| and every code is sign(c)
+    w = np.full((8, 128), c, dtype=np.float32)
+    q, scale = oracle.quant_weight(w)
+    assert scale == np.float32(abs(c))
+    assert np.all(q == np.sign(c))
+
+
+@pytest.mark.parametrize("N,K,seed", [(7, 384, 0), (64, 2560, 1), (33, 1000, 2)])
+def test_absmean_scale_is_the_correctly_rounded_mean(N, K, seed):
+    """The fixed fp64 reduction order is a reading; whatever the order, the fp32 scale must be
+    the exact mean rounded once to fp32 (checked with an exact rational sum)."""
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    q, scale = oracle.quant_weight(w)
+    exact = sum(Fraction(float(v)) for v in np.abs(w).ravel()) / (N * K)
+    assert scale == np.float32(float(exact))
+    # and the codes are numpy's round-half-to-even of the fp32 quotient, clipped
+    ref = np.clip(np.round(w / np.float32(scale)), -1, 1).astype(np.int8)
+    assert np.array_equal(q, ref)
+
+
+def test_absmean_bf16_is_the_widened_fp32():
+    rng = np.random.default_rng(5)
+    wf = (rng.standard_normal((9, 256)) * 0.02).astype(np.float32)
+    wb = workloads.to_bf16_bits(wf)
+    widened = np.array([[oracle.bf16_to_f32(int(b)) for b in row] for row in wb], dtype=np.float32)
+    qb, sb = oracle.quant_weight(wb, dtype="bf16")
+    qf, sf = oracle.quant_weight(widened)
+    assert sb == sf and np.array_equal(qb, qf)
+
+
+def test_sign_rule_threshold_and_scale():
+    """[DeepDive] §4-2: |w| < 1e-6 codes as 0 (the comparison in double, so 1e-6f itself is
+    0), anything else by its sign; the scale kept is max|w|."""
+    t = np.float32(1e-6)
+    above = np.nextafter(t, np.float32(1), dtype=np.float32)
+    w = np.array([[t, -t, above, -above, 0.0, -0.0, 5.0, -7.5]], dtype=np.float32)
+    q, scale = oracle.quant_weight(w, mode="sign")
+    assert q.tolist() == [[0, 0, 1, -1, 0, 0, 1, -1]]
+    assert scale == np.float32(7.5)
