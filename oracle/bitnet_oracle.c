@@ -243,31 +243,23 @@ int oracle_raw_code_dot(const int8_t *xq, const uint8_t *wp, int32_t *raw,
  * -1, 1), the stored scale is abs_mean; [bitnet.rs] "Ternary Weight Quantisation" gives the
  * same without the floor). The pages compute the mean with a float library reduction in an
  * unstated order. A code decided by w / scale must come out the same on every
- * implementation, so the scale must be bit-identical, so the order of the fp64 reduction
- * is fixed here (a reading):
- *   row sum r_n: 32 partial sums p_l = sum over k = l, l+32, l+64, ... (ascending) of |w|,
- *                then combined by the butterfly below;
- *   total S:     32 partial sums t_l = sum over n = l, l+32, ... (ascending) of r_n, then the
- *                same butterfly;
- *   butterfly:   for off = 16, 8, 4, 2, 1: every p_l becomes p_l + p_(l xor off); the result
- *                is the common value.
- * mean = (float)(S / (N * K)) (the division and the conversion each round to nearest),
- * scale = max(mean, 1e-5f). "round" is round-half-to-even as in numpy (the page's example,
- * w = [-0.6, -0.2, 0.2, 0.6], asks which rule: with it the codes are [-1, 0, 0, 1]).
+ * implementation, so the scale must be bit-identical; the mean is therefore defined through
+ * an exact integer sum (a reading):
+ *   S    = sum over all weights of floor(|w| * 2^74), an exact unsigned integer (each term is
+ *          |w| to 74 fractional bits; |w| must be below 2^12, and N*K at most 2^40, so that
+ *          S fits in 128 bits);
+ *   mean = (float)((double)S * 2^-74 / (N * K)): the conversion of S to double, the
+ *          division and the conversion to float each round to nearest (the scaling by 2^-74
+ *          is exact);
+ *   scale = max(mean, 1e-5f).
+ * No summation order enters: any order of an exact integer sum gives S. "round" is
+ * round-half-to-even as in numpy (the page's example, w = [-0.6, -0.2, 0.2, 0.6], asks which
+ * rule: with it the codes are [-1, 0, 0, 1]).
  *
  * Sign rule ([DeepDive] §4-2, quantize_i2_s on float weights that are already ternary): a
  * value with |w| < 1e-6 (the comparison taken in double, as the C++ expression promotes
  * it) is 0, any other value its sign; the scale kept is the largest |w|.
  * --------------------------------------------------------------------------------------- */
-static double butterfly32(double *p) {
-    double t[32];
-    for (int off = 16; off >= 1; off >>= 1) {
-        for (int l = 0; l < 32; ++l) t[l] = p[l] + p[l ^ off];
-        memcpy(p, t, sizeof(t));
-    }
-    return p[0];
-}
-
 static int quant_weight(const float *wf, const uint16_t *wb, int64_t N, int64_t K, int mode, int8_t *q,
                         float *scale) {
     if ((!wf && !wb) || !q || !scale || N < 1 || K < 1 || (mode != 0 && mode != 1)) return -1;
@@ -275,14 +267,14 @@ static int quant_weight(const float *wf, const uint16_t *wb, int64_t N, int64_t 
 #define W_AT(i) (wf ? wf[(i)] : oracle_bf16_to_f32(wb[(i)]))
     float sc;
     if (mode == 0) {
-        double t[32] = {0};
-        for (int64_t n = 0; n < N; ++n) {
-            double p[32] = {0};
-            for (int64_t k = 0; k < K; ++k) p[k % 32] += (double)fabsf(W_AT(n * K + k));
-            t[n % 32] += butterfly32(p);
+        if ((double)N * (double)K > 1099511627776.0 /* 2^40 */) return -4;
+        unsigned __int128 S = 0;
+        for (int64_t i = 0; i < N * K; ++i) {
+            const float a = fabsf(W_AT(i));
+            if (!(a < 4096.0f)) return -4;                      /* |w| >= 2^12, or NaN */
+            S += (unsigned __int128)(a * 0x1p74f);  /* a * 2^74 is exact; the conversion truncates */
         }
-        const double S = butterfly32(t);
-        const float mean = (float)(S / ((double)N * (double)K));
+        const float mean = (float)((double)S * 0x1p-74 / ((double)N * (double)K));
         sc = fmaxf(mean, 1e-5f);
         for (int64_t i = 0; i < N * K; ++i) {
             float r = nearbyintf(W_AT(i) / sc);  /* one fp32 division, then round half to even */

@@ -57,10 +57,11 @@ int oracle_raw_code_dot(const int8_t *xq, const uint8_t *wp, int32_t *raw,
 
 /* Weight ternarisation (the step before packing). mode 0, AbsMean ([DeepDive] §6-2,
  * [bitnet.rs] "Ternary Weight Quantisation"): scale = max(mean|w|, 1e-5) with the mean
- * reduced in fp64 in the fixed order described in bitnet_oracle.c, q = clip(rne(w / scale),
- * -1, 1) in fp32. mode 1, the sign rule of quantize_i2_s ([DeepDive] §4-2): q = 0 where
- * |w| < 1e-6, else sign(w); scale = max|w|. q is N x K int8; *scale one float.
- * Returns 0, or -1 on bad arguments, -2 if the rounding mode is not round-to-nearest-even. */
+ * taken through the exact integer sum of floor(|w| * 2^74) described in bitnet_oracle.c,
+ * q = clip(rne(w / scale), -1, 1) in fp32. mode 1, the sign rule of quantize_i2_s
+ * ([DeepDive] §4-2): q = 0 where |w| < 1e-6, else sign(w); scale = max|w|. q is N x K int8;
+ * *scale one float. Returns 0, or -1 on bad arguments, -2 if the rounding mode is not
+ * round-to-nearest-even, -4 if AbsMean meets |w| >= 2^12 (or NaN) or N*K > 2^40. */
 int oracle_quant_weight_f32(const float *w, int64_t N, int64_t K, int mode, int8_t *q, float *scale);
 int oracle_quant_weight_bf16(const uint16_t *w, int64_t N, int64_t K, int mode, int8_t *q, float *scale);
 

@@ -378,16 +378,30 @@ def test_absmean_constant_matrix(c):
 
 @pytest.mark.parametrize("N,K,seed", [(7, 384, 0), (64, 2560, 1), (33, 1000, 2)])
 def test_absmean_scale_is_the_correctly_rounded_mean(N, K, seed):
-    """The fixed fp64 reduction order is a reading; whatever the order, the fp32 scale must be
-    the exact mean rounded once to fp32 (checked with an exact rational sum)."""
+    """The scale is the exact mean rounded to fp32 (checked with an exact rational sum), and it
+    is the integer-sum definition recomputed with Python integers:
+    S = sum floor(|w| 2^74), mean = fp32(fp64(S) 2^-74 / (N K))."""
     rng = np.random.default_rng(seed)
     w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
     q, scale = oracle.quant_weight(w)
-    exact = sum(Fraction(float(v)) for v in np.abs(w).ravel()) / (N * K)
+    absw = [Fraction(float(v)) for v in np.abs(w).ravel()]
+    exact = sum(absw) / (N * K)
     assert scale == np.float32(float(exact))
+    S = sum(int(a * 2 ** 74) for a in absw)  # int() of a positive Fraction floors
+    assert scale == np.float32(float(S) * 2.0 ** -74 / (N * K))
     # and the codes are numpy's round-half-to-even of the fp32 quotient, clipped
     ref = np.clip(np.round(w / np.float32(scale)), -1, 1).astype(np.int8)
     assert np.array_equal(q, ref)
+
+
+def test_absmean_rejects_weights_outside_the_exact_sum_range():
+    w = np.zeros((1, 128), dtype=np.float32)
+    w[0, 5] = 4096.0
+    with pytest.raises(RuntimeError):
+        oracle.quant_weight(w)
+    w[0, 5] = np.nextafter(np.float32(4096.0), np.float32(0))  # largest allowed magnitude
+    q, scale = oracle.quant_weight(w)
+    assert scale == np.float32(float(w[0, 5]) / 128) and q[0, 5] == 1
 
 
 def test_absmean_bf16_is_the_widened_fp32():
