@@ -56,10 +56,16 @@ extern "C" {
 #define BITNET_EUNSUPPORTED (-4)  /* current device is not sm_103, or no device                 */
 #define BITNET_ETIMEOUT (-5)      /* a device-side bounded wait gave up (reported by the next call
                                      to bitnet_last_device_error); the result is not valid      */
+#define BITNET_ERANGE (-6)        /* an input value outside the operation's range, found on the
+                                     device (reported by bitnet_last_device_error)              */
 
 /* ---- activation dtypes (bitnet_quant_act) ---- */
 #define BITNET_F32 0
 #define BITNET_BF16 1
+
+/* ---- weight ternarisation modes (bitnet_quant_weight) ---- */
+#define BITNET_QW_ABSMEAN 0 /* scale = max(mean|w|, 1e-5), q = clip(rne(w / scale), -1, 1) */
+#define BITNET_QW_SIGN 1    /* q = 0 where |w| < 1e-6, else sign(w); scale = max|w|       */
 
 /* ---- matmul kernel selection (bitnet_i2s_matmul_algo) ---- */
 #define BITNET_ALGO_AUTO 0   /* GEMV M <= 16, few-token kernel M <= 64, GEMM beyond */
@@ -180,6 +186,32 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t *xq, const float *act_scale,
                                       int64_t K, int algo, void *stream);
 
 /*
+ * bitnet_quant_weight -- ternarise full-precision weights and pack them into i2_s, the step
+ * before the matmul path (three kernels on `stream`, no workspace).
+ *   BITNET_QW_ABSMEAN: "BitNet 딥다이브" §6-2 (abs_mean = max(mean(abs(w)), 1e-5), codes
+ *   clip(round(w / abs_mean), -1, 1), stored scale abs_mean) and "bitnet.rs" "Ternary Weight
+ *   Quantisation". "round" is round-half-to-even of the fp32 quotient. The mean is defined
+ *   through an exact integer so that the scale, and every code it decides, is the same bit for
+ *   bit whatever the summation order: S = sum over all N*K weights of floor(|w| * 2^74) (128-bit,
+ *   exact), mean = fp32(fp64(S) * 2^-74 / (N*K)), each conversion and the division rounding to
+ *   nearest. This needs |w| < 2^12: a weight at or above it, infinite or NaN sets
+ *   BITNET_ERANGE in the device error word (read by bitnet_last_device_error); w_scale is then
+ *   NaN and wp is unspecified.
+ *   BITNET_QW_SIGN: quantize_i2_s of "BitNet 딥다이브" §4-2, for weights that are already
+ *   ternary: |w| < 1e-6 (compared in double) codes as 0, other values by sign (NaN as -1);
+ *   scale max|w| (NaN ignored).
+ *
+ *   w       : N x K fp32 or bf16 (dtype BITNET_F32 / BITNET_BF16), row-major (device, read)
+ *   wp      : N x K/4 uint8, i2_s packed codes (device, written; also used as scratch before
+ *             the codes are written). Must not overlap w.
+ *   w_scale : 1 fp32, the scale above (device, written)
+ *   N >= 1; K >= 128, K % 128 == 0, K <= 65536; N * K <= 2^40.
+ *   w and wp 16-byte aligned, w_scale 4-byte aligned. Host-side errors as bitnet_pack_i2s.
+ */
+BITNET_API int bitnet_quant_weight(const void *w, int dtype, int mode, int64_t N, int64_t K,
+                                   uint8_t *wp, float *w_scale, void *stream);
+
+/*
  * bitnet_w2a8_linear_group -- per-token activation quantisation fused with the ternary
  * matmuls of up to 8 projections that consume the same activation rows (e.g. q/k/v, or
  * gate/up). Computes, for l = 0..count-1, exactly what bitnet_quant_act followed by
@@ -229,8 +261,9 @@ BITNET_API int bitnet_w2a8_linear(const void *x, int dtype, int64_t M, int64_t K
 /*
  * bitnet_last_device_error -- read and clear the device-side error word of the current
  * device. Kernels that wait on an mbarrier give up after a bounded number of polls and
- * record BITNET_ETIMEOUT there instead of hanging. Synchronises the device.
- * Returns BITNET_OK, BITNET_ETIMEOUT or BITNET_ECUDA.
+ * record BITNET_ETIMEOUT there instead of hanging; bitnet_quant_weight records BITNET_ERANGE
+ * for weights outside its range. Synchronises the device.
+ * Returns BITNET_OK, BITNET_ETIMEOUT, BITNET_ERANGE or BITNET_ECUDA.
  */
 BITNET_API int bitnet_last_device_error(void);
 

@@ -19,6 +19,7 @@ BITNET_EALIGN = -2
 BITNET_ECUDA = -3
 BITNET_EUNSUPPORTED = -4
 BITNET_ETIMEOUT = -5
+BITNET_ERANGE = -6
 
 BITNET_F32 = 0
 BITNET_BF16 = 1
@@ -48,6 +49,7 @@ SIGNATURES = {
         [_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "bitnet_i2s_matmul_noalloc": ([_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "bitnet_last_device_error": ([], ctypes.c_int),
+    "bitnet_quant_weight": ([_P, ctypes.c_int, ctypes.c_int, _I64, _I64, _P, _P, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -116,6 +118,28 @@ def pack_i2s(w, out=None, invalid_count=None, stream=None):
     _check(lib().bitnet_pack_i2s(_ptr(w), _ptr(out), N, K, _ptr(invalid_count), _stream(stream)),
            "bitnet_pack_i2s")
     return out
+
+
+QUANT_WEIGHT_MODES = {"absmean": 0, "sign": 1}
+
+
+def quant_weight(w, mode="absmean", out=None, scale=None, stream=None):
+    """fp32 or bf16 weights (N x K, CUDA) -> (i2_s packed uint8 N x K/4, fp32 scale tensor of 1)."""
+    import torch
+
+    if w.dtype == torch.float32:
+        dt = BITNET_F32
+    elif w.dtype == torch.bfloat16:
+        dt = BITNET_BF16
+    else:
+        raise ValueError("w must be float32 or bfloat16")
+    N, K = w.shape
+    out = torch.empty((N, K // 4), dtype=torch.uint8, device=w.device) if out is None else out
+    scale = torch.empty(1, dtype=torch.float32, device=w.device) if scale is None else scale
+    _require_cuda(w, out, scale)
+    _check(lib().bitnet_quant_weight(_ptr(w), dt, QUANT_WEIGHT_MODES[mode], N, K, _ptr(out), _ptr(scale),
+                                     _stream(stream)), "bitnet_quant_weight")
+    return out, scale
 
 
 def quant_act(x, xq=None, scale=None, rowsum=None, stream=None):

@@ -286,12 +286,17 @@ cudaError_t launch_quant_act(const void* x, int dtype, int64_t M, int64_t K, int
 cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
                             float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
                             int num_sms, cudaStream_t stream);
+// Weight ternarisation + i2_s packing (quant_weight.cu); mode 0 AbsMean, 1 the sign rule.
+cudaError_t launch_quant_weight(const void* w, bool bf16, int64_t N, int64_t K, int mode, uint8_t* wp, float* w_scale,
+                                int num_sms, cudaStream_t stream);
+
 // Few-token tensor-core matmul (gemm_smallm.cu): 1 <= M <= 64, K <= 32768.
 bool gemm_smallm_supported(int64_t M, int64_t K);
 cudaError_t launch_gemm_smallm(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
                                float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
                                int num_sms, cudaStream_t stream);
 cudaError_t read_clear_device_error_smallm(int* value);
+cudaError_t read_clear_device_error_quant_weight(int* value);
 // Read and clear the device error word of each translation unit that waits (synchronous).
 cudaError_t read_clear_device_error_gemm(int* value);
 cudaError_t read_clear_device_error_gemm_ws(int* value);

@@ -69,6 +69,7 @@ BITNET_API const char* bitnet_strerror(int status) {
     case BITNET_ECUDA: return "CUDA runtime error or kernel launch failure";
     case BITNET_EUNSUPPORTED: return "unsupported device (an sm_103 / GB300 GPU is required)";
     case BITNET_ETIMEOUT: return "a device-side bounded wait timed out; results are invalid";
+    case BITNET_ERANGE: return "an input value outside the operation's supported range (found on the device)";
     default: return "unknown status";
   }
 }
@@ -91,6 +92,19 @@ BITNET_API int bitnet_quant_act(const void* x, int dtype, int64_t M, int64_t K, 
   int sms = 0;
   if (int st = check_device(&sms)) return st;
   return status_of(launch_quant_act(x, dtype, M, K, xq, act_scale, rowsum, static_cast<cudaStream_t>(stream)));
+}
+
+BITNET_API int bitnet_quant_weight(const void* w, int dtype, int mode, int64_t N, int64_t K, uint8_t* wp,
+                                   float* w_scale, void* stream) {
+  if (!w || !wp || !w_scale) return BITNET_EINVAL;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_EINVAL;
+  if (mode != BITNET_QW_ABSMEAN && mode != BITNET_QW_SIGN) return BITNET_EINVAL;
+  if (N < 1 || !valid_k(K) || N > (int64_t(1) << 40) / K) return BITNET_EINVAL;
+  if (!aligned(w, 16) || !aligned(wp, 16) || !aligned(w_scale, 4)) return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  return status_of(launch_quant_weight(w, dtype == BITNET_BF16, N, K, mode, wp, w_scale, sms,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, const int32_t* rowsum,
@@ -236,7 +250,8 @@ BITNET_API int bitnet_last_device_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return BITNET_ECUDA;
   int status = BITNET_OK;
   cudaError_t (*readers[])(int*) = {read_clear_device_error_gemm, read_clear_device_error_gemm_ws,
-                                    read_clear_device_error_gemv_group, read_clear_device_error_smallm};
+                                    read_clear_device_error_gemv_group, read_clear_device_error_smallm,
+                                    read_clear_device_error_quant_weight};
   for (auto rd : readers) {
     int v = 0;
     if (rd(&v) != cudaSuccess) return BITNET_ECUDA;

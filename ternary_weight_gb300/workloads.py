@@ -17,7 +17,10 @@ Recipe (all draws use numpy's PCG64 ``default_rng`` with the seed stated per ten
     of min(N*K, 2**20) elements stands for the full matrix; the expectation is
     0.02*sqrt(2/pi) ~= 0.01596);
   * activations: fp32 N(0, 1), or fp32 N(0, 1) rounded to bf16 (round-to-nearest-even),
-    optionally with Bernoulli(p) outliers multiplied by 20 before the rounding.
+    optionally with Bernoulli(p) outliers multiplied by 20 before the rounding;
+  * full-precision weights for the ternarisation: fp32 N(0, 0.02^2); for the sign rule,
+    ternary weights times 0.0156 with each zero replaced by a magnitude uniform in
+    [0.5e-6, 2e-6] of random sign (so about a third of them fall below the 1e-6 threshold).
 """
 from __future__ import annotations
 
@@ -68,6 +71,21 @@ def weight_scale(N: int, K: int, seed: int) -> float:
     n = int(min(N * K, 1 << 20))
     src = rng.normal(0.0, 0.02, size=n)
     return float(np.float32(np.mean(np.abs(src))))
+
+
+def source_weights_f32(N: int, K: int, seed: int, std: float = 0.02) -> np.ndarray:
+    """N x K fp32 full-precision weights ~ N(0, std^2): the input of the weight ternarisation."""
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal(size=(N, K), dtype=np.float32) * np.float32(std)).astype(np.float32)
+
+
+def near_ternary_weights_f32(N: int, K: int, seed: int, a: float = 0.0156) -> np.ndarray:
+    """N x K fp32 weights that are already ternary up to noise, for the sign rule: values
+    +-a, and zeros replaced by magnitudes spread across 1e-6 (half below, half above)."""
+    rng = np.random.default_rng(seed)
+    t = ternary_weights(N, K, seed).astype(np.float32) * np.float32(a)
+    tiny = (rng.uniform(0.5e-6, 2e-6, size=(N, K)) * rng.choice([-1.0, 1.0], size=(N, K))).astype(np.float32)
+    return np.where(t == 0, tiny, t).astype(np.float32)
 
 
 def activations_f32(M: int, K: int, seed: int, outlier_p: float = 0.0) -> np.ndarray:

@@ -97,6 +97,26 @@ def test_pack_rejects_bad_arguments_on_host(lib, args, status):
     assert lib.bitnet_pack_i2s(*args, None) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    # (w, dtype, mode, N, K, wp, w_scale)
+    ((None, 0, 0, 1, 128, FAKE, FAKE), -1),
+    ((FAKE, 0, 0, 1, 128, None, FAKE), -1),
+    ((FAKE, 0, 0, 1, 128, FAKE, None), -1),
+    ((FAKE, 2, 0, 1, 128, FAKE, FAKE), -1),
+    ((FAKE, 0, 2, 1, 128, FAKE, FAKE), -1),
+    ((FAKE, 0, -1, 1, 128, FAKE, FAKE), -1),
+    ((FAKE, 0, 0, 0, 128, FAKE, FAKE), -1),
+    ((FAKE, 0, 0, 1, 192, FAKE, FAKE), -1),
+    ((FAKE, 0, 0, 1, 65536 + 128, FAKE, FAKE), -1),
+    ((FAKE, 0, 0, 1 << 30, 65536, FAKE, FAKE), -1),
+    ((FAKE + 8, 0, 0, 1, 128, FAKE, FAKE), -2),
+    ((FAKE, 1, 1, 1, 128, FAKE + 4, FAKE), -2),
+    ((FAKE, 0, 0, 1, 128, FAKE, FAKE + 2), -2),
+])
+def test_quant_weight_rejects_bad_arguments_on_host(lib, args, status):
+    assert lib.bitnet_quant_weight(*args, None) == status
+
+
 def test_valid_call_without_gpu_is_unsupported(lib):
     import torch
 

@@ -480,3 +480,136 @@ def test_matmul_ws_two_calls_reuse_workspace():
         torch.cuda.synchronize()
         o_out, _ = oracle.ternary_matmul(xq, s, wp, 0.02, nthreads=NT)
         assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- weight ternarisation
+
+QW_CASES = [
+    # (N, K, dtype, mode): one block, ragged N, the 2B-4T shapes, a 100B-class row length
+    (1, 128, "f32", "absmean"), (7, 384, "bf16", "absmean"), (640, 2560, "f32", "absmean"),
+    (2560, 6912, "bf16", "absmean"), (33, 8192, "f32", "absmean"), (129, 10240, "bf16", "absmean"),
+    (300, 2560, "f32", "sign"), (65, 640, "bf16", "sign"), (2560, 2560, "f32", "sign"),
+]
+
+
+def _qw_inputs(N, K, dtype, mode, seed):
+    w = (workloads.source_weights_f32(N, K, seed) if mode == "absmean"
+         else workloads.near_ternary_weights_f32(N, K, seed))
+    return (w, w) if dtype == "f32" else (workloads.to_bf16_bits(w), workloads.to_bf16_bits(w))
+
+
+@pytest.mark.parametrize("N,K,dtype,mode", QW_CASES)
+def test_quant_weight_parity(N, K, dtype, mode):
+    """Packed bytes and the scale's bit pattern, against the oracle's ternarisation + pack."""
+    w_np, w_dev = _qw_inputs(N, K, dtype, mode, seed=400 + N)
+    g_wp, g_s = binding.quant_weight(x_device(w_dev, dtype), mode=mode)
+    torch.cuda.synchronize()
+    o_q, o_s = oracle.quant_weight(w_np, dtype=dtype, mode=mode)
+    assert np.array_equal(host(g_s).view(np.uint32), np.array([o_s], dtype=np.float32).view(np.uint32))
+    assert np.array_equal(host(g_wp), oracle.pack_i2s(o_q)[0])
+    assert binding.last_device_error() == 0
+
+
+def test_quant_weight_all_zero_and_ties():
+    # all zero: the 1e-5 floor, every code 1 (weight 0)
+    g_wp, g_s = binding.quant_weight(torch.zeros((5, 256), dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert host(g_s)[0] == np.float32(1e-5) and np.all(host(g_wp) == 0x55)
+    # mean |w| = 1 exactly: +-0.5 round to even (0), +-1.5 to +-2 and clip to +-1
+    w = np.tile(np.array([0.5, -0.5, 1.5, -1.5], dtype=np.float32), (3, 64))
+    g_wp, g_s = binding.quant_weight(dev(w))
+    torch.cuda.synchronize()
+    o_q, o_s = oracle.quant_weight(w)
+    assert o_s == 1.0 and host(g_s)[0] == 1.0
+    assert np.array_equal(host(g_wp), oracle.pack_i2s(o_q)[0])
+
+
+def test_quant_weight_full_exponent_range():
+    """Magnitudes from subnormal to just under 2^12: every part of the 128-bit fixed-point sum,
+    the floor of values below 2^-74, and codes far from the thresholds."""
+    rng = np.random.default_rng(420)
+    N, K = 37, 1280
+    e = rng.uniform(-149.0, 11.99, size=(N, K))
+    w = (np.exp2(e) * rng.choice([-1.0, 1.0], size=(N, K))).astype(np.float32)
+    w[0, :4] = [0.0, -0.0, np.float32(2.0 ** -149), np.float32(2.0 ** -74)]
+    for dtype in ("f32", "bf16"):
+        top = np.float32(4095.9997) if dtype == "f32" else np.float32(4080.0)  # largest in range
+        w[0, 4:6] = [top, -top]
+        w_dev = w if dtype == "f32" else workloads.to_bf16_bits(w)
+        g_wp, g_s = binding.quant_weight(x_device(w_dev, dtype))
+        torch.cuda.synchronize()
+        o_q, o_s = oracle.quant_weight(w_dev, dtype=dtype)
+        assert np.array_equal(host(g_s).view(np.uint32), np.array([o_s], dtype=np.float32).view(np.uint32))
+        assert np.array_equal(host(g_wp), oracle.pack_i2s(o_q)[0])
+    assert binding.last_device_error() == 0
+
+
+def _absmean_threshold(scale):
+    """Largest fp32 T with T <= scale * (1/2 + 2^-25): rne(fl(w / scale)) is +1 exactly for w > T."""
+    from fractions import Fraction
+    c = Fraction(float(scale)) * (Fraction(1, 2) + Fraction(1, 2 ** 25))
+    t = np.float32(float(c))
+    return np.nextafter(t, np.float32(0)) if Fraction(float(t)) > c else t
+
+
+def test_quant_weight_codes_at_the_rounding_boundary():
+    """Weights placed on and next to the +-1/2 rounding boundary of w / scale (the scale is
+    iterated to a fixed point so the placed values sit on the boundary of the final scale)."""
+    N, K = 16, 512
+    w = workloads.source_weights_f32(N, K, 430)
+    _, s = oracle.quant_weight(w)
+    for _ in range(20):
+        t = _absmean_threshold(s)
+        edge = np.array([t, np.nextafter(t, np.float32(1)), np.nextafter(t, np.float32(0)), s / 2,
+                         np.nextafter(s / 2, np.float32(1))], dtype=np.float32)
+        w[:, :5] = edge
+        w[:, 5:10] = -edge
+        _, s_new = oracle.quant_weight(w)
+        if s_new == s:
+            break
+        s = s_new
+    assert s_new == s, "scale did not settle"
+    o_q, o_s = oracle.quant_weight(w)
+    # the boundary really is exercised: T codes 0, the float above T codes +1
+    assert list(o_q[0, :3]) == [0, 1, 0] and list(o_q[0, 5:8]) == [0, -1, 0]
+    g_wp, g_s = binding.quant_weight(dev(w))
+    torch.cuda.synchronize()
+    assert host(g_s)[0] == o_s
+    assert np.array_equal(host(g_wp), oracle.pack_i2s(o_q)[0])
+
+
+@pytest.mark.parametrize("bad", [4096.0, float("inf"), float("nan")])
+def test_quant_weight_range_error_is_reported(bad):
+    """|w| >= 2^12, inf or NaN under AbsMean: BITNET_ERANGE in the device error word and a NaN
+    scale; the word is cleared by the read and the next call is clean."""
+    w = workloads.source_weights_f32(9, 256, 440)
+    w[4, 100] = np.float32(bad)
+    _, g_s = binding.quant_weight(dev(w))
+    torch.cuda.synchronize()
+    assert np.isnan(host(g_s)[0])
+    assert binding.last_device_error() == binding.BITNET_ERANGE
+    assert binding.last_device_error() == 0
+    w[4, 100] = np.float32(4095.9997)  # the largest magnitude still in range
+    g_wp, g_s = binding.quant_weight(dev(w))
+    torch.cuda.synchronize()
+    o_q, o_s = oracle.quant_weight(w)
+    assert host(g_s)[0] == o_s and np.array_equal(host(g_wp), oracle.pack_i2s(o_q)[0])
+    assert binding.last_device_error() == 0
+
+
+def test_quant_weight_then_matmul_chain():
+    """fp32 source weights -> ternarise + pack -> matmul with the returned scale, end to end."""
+    M, N, K = 3, 700, 2560
+    w = workloads.source_weights_f32(N, K, 410)
+    x = workloads.activations(M, K, seed=411, dtype="f32")
+    g_wp, g_s = binding.quant_weight(dev(w))
+    g_xq, g_sx, g_rs = binding.quant_act(dev(x))
+    torch.cuda.synchronize()
+    scale = float(host(g_s)[0])
+    g_out = binding.i2s_matmul(g_xq, g_sx, g_rs, g_wp, scale)
+    torch.cuda.synchronize()
+    o_q, o_s = oracle.quant_weight(w)
+    o_xq, o_sx, _ = oracle.quant_act(x)
+    o_out, _ = oracle.ternary_matmul(o_xq, o_sx, oracle.pack_i2s(o_q)[0], float(o_s), nthreads=NT)
+    assert scale == o_s
+    assert np.array_equal(host(g_out).view(np.uint32), o_out.view(np.uint32))
