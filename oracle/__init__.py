@@ -67,6 +67,8 @@ def _load():
     for fn in (lib.oracle_quant_weight_f32, lib.oracle_quant_weight_bf16):
         fn.argtypes = [P, I64, I64, ctypes.c_int, P, P]
         fn.restype = ctypes.c_int
+    lib.oracle_ffn_inner.argtypes = [P, P, P, ctypes.c_float, I64, I64, P]
+    lib.oracle_ffn_inner.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -183,6 +185,26 @@ def quant_weight(w: np.ndarray, dtype: str = "f32", mode: str = "absmean"):
     if rc != 0:
         raise RuntimeError("oracle quant_weight failed: %d" % rc)
     return q, scale[0]
+
+
+def ffn_inner(gate: np.ndarray, up: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """FFN inner activation of M x F fp32 gate and up rows: inner = RMSNorm(max(g, 0)^2 * u)
+    with per-channel weight gamma (F fp32) and epsilon eps, the sum of squares in the fixed
+    order of bitnet_oracle.c. Returns M x F float32."""
+    lib = _load()
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    up = np.ascontiguousarray(up, dtype=np.float32)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    if gate.ndim == 1:
+        gate, up = gate[None, :], up[None, :]
+    M, F = gate.shape
+    if up.shape != (M, F) or gamma.shape != (F,):
+        raise ValueError("shape mismatch")
+    inner = np.empty((M, F), dtype=np.float32)
+    rc = lib.oracle_ffn_inner(_ptr(gate), _ptr(up), _ptr(gamma), float(eps), M, F, _ptr(inner))
+    if rc != 0:
+        raise RuntimeError("oracle ffn_inner failed: %d" % rc)
+    return inner
 
 
 def default_threads() -> int:

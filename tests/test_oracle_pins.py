@@ -423,3 +423,89 @@ def test_sign_rule_threshold_and_scale():
     q, scale = oracle.quant_weight(w, mode="sign")
     assert q.tolist() == [[0, 0, 1, -1, 0, 0, 1, -1]]
     assert scale == np.float32(7.5)
+
+
+# ---------------------------------------------------------------- FFN inner activation
+
+def _ffn_rows(M, F, seed):
+    rng = np.random.default_rng(seed)
+    g = rng.standard_normal((M, F)).astype(np.float32)
+    u = rng.standard_normal((M, F)).astype(np.float32)
+    gamma = (1.0 + 0.1 * rng.standard_normal(F)).astype(np.float32)
+    return g, u, gamma
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-5, 0.5])
+def test_ffn_inner_matches_fp64_definition(eps):
+    """[bitnet.rs] "Forward Pass": inner = RMSNorm(sqrelu(gate) * up), against the same
+    formula in float64 (numpy). The fp32 oracle's error is a few ulps plus the sum's
+    rounding (< 40 * 2^-24 relative); a dropped or misplaced term (no square in sqrelu, no
+    gamma, eps outside the root, sum instead of mean) is off by far more."""
+    M, F = 3, 6912
+    g, u, gamma = _ffn_rows(M, F, 11)
+    got = oracle.ffn_inner(g, u, gamma, eps)
+    h = np.maximum(g.astype(np.float64), 0.0) ** 2 * u
+    ref = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + eps) * gamma
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-30)
+
+
+def test_ffn_inner_sqrelu_zeroes_non_positive_gates():
+    """max(g, 0)^2: negative, -0 and NaN gates give a zero at their position (signed like
+    u * gamma, since (0 * 0) * u keeps the sign of u); the rest of the row stays finite."""
+    g, u, gamma = _ffn_rows(1, 1024, 12)
+    g[0, :4] = [-3.0, -0.0, np.nan, -1e-30]
+    inner = oracle.ffn_inner(g, u, gamma, 1e-5)
+    assert np.all(inner[0, :4] == 0.0)
+    assert np.array_equal(np.signbit(inner[0, :4]), np.signbit(u[0, :4] * gamma[:4]))
+    assert np.all(np.isfinite(inner))
+
+
+def test_ffn_inner_constant_row_normalises_to_gamma():
+    """h constant = 12 (g = 2, u = 3): ss = 144 F exactly, mean 144, root 12, so inner is
+    gamma * fl(12 * fl(1/12)), within one ulp of gamma; with gamma = 1 every element is ~1."""
+    F = 2048
+    g = np.full((1, F), 2.0, np.float32)
+    u = np.full((1, F), 3.0, np.float32)
+    gamma = np.linspace(0.5, 2.0, F).astype(np.float32)
+    inner = oracle.ffn_inner(g, u, gamma, 0.0)[0]
+    assert np.all(np.abs(inner - gamma) <= np.spacing(gamma) * 1.0)
+    ones = oracle.ffn_inner(g, u, np.ones(F, np.float32), 0.0)[0]
+    assert np.all(np.abs(ones - 1.0) <= 2.0 ** -23)
+
+
+def test_ffn_inner_single_spike_is_sqrt_f():
+    """One positive gate: h = (a, 0, ...), mean = a^2 / F, so with eps = 0 inner_0 = sqrt(F)
+    (to a few ulps) and every other element is 0."""
+    F = 4096
+    g = np.full((1, F), -1.0, np.float32)
+    u = np.ones((1, F), np.float32)
+    g[0, 1234] = 1.75
+    inner = oracle.ffn_inner(g, u, np.ones(F, np.float32), 0.0)[0]
+    assert abs(inner[1234] - 64.0) <= 4 * np.spacing(np.float32(64.0))
+    assert np.count_nonzero(inner) == 1
+
+
+def test_ffn_inner_scale_invariance_exact():
+    """With eps = 0 RMSNorm is invariant under scaling h by 2^k, and every fp32 step scales
+    exactly, so inner is bit-identical: up * 2^k scales h by 2^k, gate * 2^k by 2^2k."""
+    g, u, gamma = _ffn_rows(2, 2560, 13)
+    base = oracle.ffn_inner(g, u, gamma, 0.0)
+    for k in (-5, 3):
+        assert np.array_equal(oracle.ffn_inner(g, u * np.float32(2.0 ** k), gamma, 0.0), base)
+        assert np.array_equal(oracle.ffn_inner(g * np.float32(2.0 ** k), u, gamma, 0.0), base)
+
+
+def test_ffn_inner_all_gates_negative_with_eps():
+    """h = 0 everywhere: ss = 0, c = 1/sqrt(eps) finite, inner exactly 0 (no NaN)."""
+    g = -np.abs(_ffn_rows(1, 640, 14)[0]) - 1.0
+    u = np.ones_like(g)
+    inner = oracle.ffn_inner(g, u, np.ones(640, np.float32), 1e-5)
+    assert np.all(inner == 0.0)
+
+
+def test_ffn_inner_rows_are_independent():
+    """Each row is normalised by its own sum: a row computed alone equals it in a batch."""
+    g, u, gamma = _ffn_rows(4, 1024, 15)
+    batch = oracle.ffn_inner(g, u, gamma, 1e-5)
+    for m in range(4):
+        assert np.array_equal(oracle.ffn_inner(g[m:m + 1], u[m:m + 1], gamma, 1e-5)[0], batch[m])
