@@ -259,6 +259,67 @@ BITNET_API int bitnet_w2a8_linear(const void *x, int dtype, int64_t M, int64_t K
                                   float *act_scale, int32_t *rowsum, void *stream);
 
 /*
+ * bitnet_ffn_act_quant -- the FFN's inner activation fused with its per-token quantisation
+ * ("bitnet.rs" "Forward Pass": inner = ffn_sub_norm(sqrelu(gate(x)) * up(x)), out =
+ * down(inner); the quantisation is that of [DeepDive] §4-5). Per row m, in fp32 with one
+ * rounding per operation:
+ *   h = max(g, 0)^2 * u  (as (r * r) * u, r = g > 0 ? g : 0)
+ *   inner = (h * c) * gamma,  c = 1 / sqrt(ss / F + eps)        (RMSNorm, weight gamma)
+ *   xq, act_scale, rowsum = what bitnet_quant_act gives for the fp32 row inner.
+ * ss, the sum of h^2, is taken in a fixed order so the result is reproducible bit for bit:
+ * 256 partial sums, partial p accumulating by fused multiply-add, in ascending k, the h_k
+ * with floor(k / 4) mod 256 == p; each run of 32 partials combined by the pairwise tree that
+ * adds partial p + d into p for d = 16, 8, 4, 2, 1; the eight run sums combined as
+ * ((R0 + R1) + (R2 + R3)) + ((R4 + R5) + (R6 + R7)).
+ *
+ *   gate, up  : M x F fp32 (device, read), 16-byte aligned
+ *   gamma     : F fp32 (device, read), 16-byte aligned, shared by all rows
+ *   eps       : finite, > 0
+ *   xq        : M x F int8 (device, written), 16-byte aligned
+ *   act_scale, rowsum : M fp32 / M int32 (device, written)
+ *   inner_out : M x F fp32 (device, written) or NULL, 16-byte aligned
+ *   M >= 1; F >= 128, F % 128 == 0, F <= 32768. One kernel launch on `stream`.
+ *   Values of h whose square overflows fp32 are outside the operation.
+ */
+BITNET_API int bitnet_ffn_act_quant(const float *gate, const float *up, const float *gamma, float eps,
+                                    int64_t M, int64_t F, int8_t *xq, float *act_scale, int32_t *rowsum,
+                                    float *inner_out, void *stream);
+
+/*
+ * bitnet_w2a8_ffn -- the FFN block of one decoder layer on packed ternary weights
+ * ("bitnet.rs" "Forward Pass", FFN with squared-ReLU gating and sub-norm):
+ *   gate = W2A8(x; wp_gate, a_gate), up = W2A8(x; wp_up, a_up)   (F outputs each, over K)
+ *   xq', s', rowsum' = bitnet_ffn_act_quant(gate, up, gamma, eps)
+ *   out = W2A8(xq', s', rowsum'; wp_down, a_down)                  (K outputs, over F)
+ * where W2A8 is bitnet_quant_act followed by bitnet_i2s_matmul. The results are exactly those
+ * of that sequence of calls.
+ *
+ *   x        : M x K fp32 or bf16 (dtype) (device, read), 16-byte aligned
+ *   wp_gate, wp_up : F x K/4 packed (device), wp_down : K x F/4 packed (device), 16-byte aligned
+ *   a_gate, a_up, a_down : the weight scales
+ *   gamma, eps : as bitnet_ffn_act_quant
+ *   gate_out, up_out : M x F fp32 (device, written), 16-byte aligned
+ *   out      : M x K fp32 (device, written)
+ *   xq       : M * max(K, F) bytes of int8 workspace (device), act_scale, rowsum : M each
+ *              (device). On return the first M * F bytes of xq (a contiguous M x F array),
+ *              act_scale and rowsum hold the down projection's input (the quantised inner rows). With
+ *              M == 1 and K, F <= 10240 the call is two kernel launches (the gate/up group, then
+ *              the down projection with the sub-norm and quantisation in its prologue) and these
+ *              three may be NULL.
+ *   workspace, workspace_bytes : optional (NULL, 0) device workspace, 256-byte aligned, of at
+ *              least bitnet_w2a8_ffn_workspace_size(M, K, F) bytes; when given and that size is
+ *              non-zero, the three projections run on the expand-once GEMM path of
+ *              bitnet_i2s_matmul_ws.
+ *   M >= 1; K and F multiples of 128 with K <= 65536 and F <= 32768; eps finite and > 0.
+ */
+BITNET_API int64_t bitnet_w2a8_ffn_workspace_size(int64_t M, int64_t K, int64_t F);
+BITNET_API int bitnet_w2a8_ffn(const void *x, int dtype, int64_t M, int64_t K, int64_t F,
+                               const uint8_t *wp_gate, float a_gate, const uint8_t *wp_up, float a_up,
+                               const uint8_t *wp_down, float a_down, const float *gamma, float eps,
+                               float *gate_out, float *up_out, float *out, int8_t *xq, float *act_scale,
+                               int32_t *rowsum, void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
  * bitnet_last_device_error -- read and clear the device-side error word of the current
  * device. Kernels that wait on an mbarrier give up after a bounded number of polls and
  * record BITNET_ETIMEOUT there instead of hanging; bitnet_quant_weight records BITNET_ERANGE

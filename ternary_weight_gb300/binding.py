@@ -50,6 +50,11 @@ SIGNATURES = {
     "bitnet_i2s_matmul_noalloc": ([_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "bitnet_last_device_error": ([], ctypes.c_int),
     "bitnet_quant_weight": ([_P, ctypes.c_int, ctypes.c_int, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "bitnet_ffn_act_quant": ([_P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
+    "bitnet_w2a8_ffn_workspace_size": ([_I64, _I64, _I64], _I64),
+    "bitnet_w2a8_ffn": (
+        [_P, ctypes.c_int, _I64, _I64, _I64, _P, ctypes.c_float, _P, ctypes.c_float, _P, ctypes.c_float, _P,
+         ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _I64, _P], ctypes.c_int),
 }
 
 _lib = None
@@ -277,3 +282,63 @@ def linear(x, wp, w_scale, out=None, algo="auto", stream=None):
     """Quantise activation rows and multiply them with packed ternary weights (two launches)."""
     xq, s, rs = quant_act(x, stream=stream)
     return i2s_matmul(xq, s, rs, wp, w_scale, out=out, algo=algo, stream=stream)
+
+
+def ffn_act_quant(gate, up, gamma, eps, xq=None, scale=None, rowsum=None, inner_out=None, stream=None):
+    """FFN inner activation (squared-ReLU gate times up, RMS sub-norm with weight gamma and
+    epsilon eps) fused with its per-token quantisation. gate, up: M x F fp32 CUDA tensors;
+    gamma: F fp32. Returns (xq int8 M x F, s fp32 M, rowsum int32 M); inner_out (M x F fp32)
+    is written when given."""
+    import torch
+
+    M, F = gate.shape
+    if up.shape != gate.shape or gamma.shape != (F,):
+        raise ValueError("gate and up must be M x F, gamma F")
+    dev = gate.device
+    xq = torch.empty((M, F), dtype=torch.int8, device=dev) if xq is None else xq
+    scale = torch.empty(M, dtype=torch.float32, device=dev) if scale is None else scale
+    rowsum = torch.empty(M, dtype=torch.int32, device=dev) if rowsum is None else rowsum
+    _require_cuda(gate, up, gamma, xq, scale, rowsum, inner_out)
+    _check(lib().bitnet_ffn_act_quant(_ptr(gate), _ptr(up), _ptr(gamma), float(eps), M, F, _ptr(xq), _ptr(scale),
+                                      _ptr(rowsum), _ptr(inner_out), _stream(stream)),
+           "bitnet_ffn_act_quant")
+    return xq, scale, rowsum
+
+
+def ffn_workspace_size(M, K, F) -> int:
+    n = lib().bitnet_w2a8_ffn_workspace_size(M, K, F)
+    if n < 0:
+        raise BitnetError(int(n), "bitnet_w2a8_ffn_workspace_size")
+    return int(n)
+
+
+def w2a8_ffn(x, wp_gate, a_gate, wp_up, a_up, wp_down, a_down, gamma, eps, out=None, gate_out=None, up_out=None,
+             xq=None, scale=None, rowsum=None, workspace=None, stream=None):
+    """The FFN block: gate/up W2A8 projections of x (M x K fp32/bf16), the squared-ReLU gate
+    and RMS sub-norm, then the down W2A8 projection. Returns out (M x K fp32); gate_out and
+    up_out (M x F) and, when given, xq/scale/rowsum (the quantised inner rows) are written.
+    For M > 1 the workspace buffers are allocated here if not given; ``workspace`` (a uint8
+    CUDA tensor of at least ffn_workspace_size bytes) selects the expand-once GEMM path."""
+    import torch
+
+    dt = _act_dtype(x)
+    M, K = x.shape
+    F = wp_gate.shape[0]
+    if wp_gate.shape != (F, K // 4) or wp_up.shape != (F, K // 4) or wp_down.shape != (K, F // 4):
+        raise ValueError("wp_gate/wp_up must be F x K/4 and wp_down K x F/4")
+    dev = x.device
+    out = torch.empty((M, K), dtype=torch.float32, device=dev) if out is None else out
+    gate_out = torch.empty((M, F), dtype=torch.float32, device=dev) if gate_out is None else gate_out
+    up_out = torch.empty((M, F), dtype=torch.float32, device=dev) if up_out is None else up_out
+    if M > 1:
+        xq = torch.empty((M, max(K, F)), dtype=torch.int8, device=dev) if xq is None else xq
+        scale = torch.empty(M, dtype=torch.float32, device=dev) if scale is None else scale
+        rowsum = torch.empty(M, dtype=torch.int32, device=dev) if rowsum is None else rowsum
+    _require_cuda(x, wp_gate, wp_up, wp_down, gamma, out, gate_out, up_out, xq, scale, rowsum, workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().bitnet_w2a8_ffn(_ptr(x), dt, M, K, F, _ptr(wp_gate), float(a_gate), _ptr(wp_up), float(a_up),
+                                 _ptr(wp_down), float(a_down), _ptr(gamma), float(eps), _ptr(gate_out),
+                                 _ptr(up_out), _ptr(out), _ptr(xq), _ptr(scale), _ptr(rowsum), _ptr(workspace),
+                                 ws_bytes, _stream(stream)),
+           "bitnet_w2a8_ffn")
+    return out

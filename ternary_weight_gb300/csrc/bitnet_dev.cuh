@@ -263,6 +263,40 @@ struct QuantOut {  // optional outputs of a fused quantisation (each may be null
   float* scale;
   int32_t* rowsum;
 };
+// FFN inner activation ("bitnet.rs" "Forward Pass": inner = ffn_sub_norm(sqrelu(gate) * up)),
+// the input row of the FFN's down projection. ffn_sub_norm is an RMSNorm with per-channel
+// weight gamma and epsilon eps:
+//   h = max(g, 0)^2 * u = (r * r) * u with r = (g > 0 ? g : 0)
+//   inner = (h * c) * gamma,  c = 1 / sqrt(ss / F + eps)
+// every operation one fp32 rounding. ss = sum of h^2 in a fixed order, so every
+// implementation gets the same value: 256 partials, partial p taking the h_k with
+// floor(k / 4) mod 256 == p in ascending k, each by one fma; then within each run of 32
+// partials the xor butterfly with offsets 16, 8, 4, 2, 1 (the tree adding partial p + d into
+// p); then the eight run sums as ((R0 + R1) + (R2 + R3)) + ((R4 + R5) + (R6 + R7)).
+struct FfnIn {
+  const float* gate;   // F fp32 per row
+  const float* up;     // F fp32 per row
+  const float* gamma;  // F fp32, shared by all rows
+  float eps;
+};
+__device__ __forceinline__ float ffn_h(float g, float u) {
+  const float r = g > 0.0f ? g : 0.0f;
+  return __fmul_rn(__fmul_rn(r, r), u);
+}
+__device__ __forceinline__ float ffn_rms_factor(float ss, int F, float eps) {
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)F), eps)));
+}
+// the within-run tree of the sum of squares, on one warp's 32 partials (all lanes get it)
+__device__ __forceinline__ float ffn_run_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+__device__ __forceinline__ float ffn_runs_total(const float* r) {
+  return __fadd_rn(__fadd_rn(__fadd_rn(r[0], r[1]), __fadd_rn(r[2], r[3])),
+                   __fadd_rn(__fadd_rn(r[4], r[5]), __fadd_rn(r[6], r[7])));
+}
+
 constexpr int kMaxPrefetch = 8;
 struct Prefetch {  // byte ranges to pull into L2 (a hint; 16-byte aligned starts)
   const void* ptr[kMaxPrefetch];
@@ -279,6 +313,14 @@ struct Prefetch {  // byte ranges to pull into L2 (a hint; 16-byte aligned start
 bool gemv_group_supported(int64_t K);
 cudaError_t launch_gemv_group(const void* x, bool bf16, const LinearSet& set, const QuantOut& qout,
                               const Prefetch& pf, int64_t K, int num_sms, cudaStream_t stream);
+// The same kernel with the FFN inner activation as its input row (F = K): the down
+// projection of the FFN, fused with the sub-norm and the quantisation.
+cudaError_t launch_gemv_group_ffn(const FfnIn& ffn, const LinearSet& set, const QuantOut& qout, const Prefetch& pf,
+                                  int64_t F, int num_sms, cudaStream_t stream);
+// FFN inner activation + per-token quantisation for M rows (ffn.cu); inner_out optional.
+constexpr int64_t kFfnMaxF = 32768;
+cudaError_t launch_ffn_act_quant(const FfnIn& ffn, int64_t M, int64_t F, int8_t* xq, float* act_scale,
+                                 int32_t* rowsum, float* inner_out, cudaStream_t stream);
 cudaError_t launch_pack_i2s(const int8_t* w, uint8_t* wp, int64_t N, int64_t K, int32_t* invalid_count,
                             cudaStream_t stream);
 cudaError_t launch_quant_act(const void* x, int dtype, int64_t M, int64_t K, int8_t* xq, float* act_scale,

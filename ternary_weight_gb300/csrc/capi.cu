@@ -6,6 +6,8 @@
 #include "bitnet.h"
 #include "bitnet_dev.cuh"
 
+#include <cmath>
+
 #include <atomic>
 #include <cstdint>
 
@@ -242,6 +244,94 @@ BITNET_API int bitnet_w2a8_linear(const void* x, int dtype, int64_t M, int64_t K
                                   int32_t* rowsum, void* stream) {
   int32_t* accs[1] = {acc_out};
   return bitnet_w2a8_linear_group(x, dtype, M, K, 1, &wp, &w_scale, &N, &out, accs, xq, act_scale, rowsum, stream);
+}
+
+BITNET_API int bitnet_ffn_act_quant(const float* gate, const float* up, const float* gamma, float eps, int64_t M,
+                                    int64_t F, int8_t* xq, float* act_scale, int32_t* rowsum, float* inner_out,
+                                    void* stream) {
+  if (!gate || !up || !gamma || !xq || !act_scale || !rowsum) return BITNET_EINVAL;
+  if (M < 1 || M > INT32_MAX || !valid_k(F) || F > kFfnMaxF) return BITNET_EINVAL;
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return BITNET_EINVAL;
+  if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(gamma, 16) || !aligned(xq, 16) || !aligned(act_scale, 4) ||
+      !aligned(rowsum, 4) || (inner_out && !aligned(inner_out, 16)))
+    return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  return status_of(launch_ffn_act_quant(FfnIn{gate, up, gamma, eps}, M, F, xq, act_scale, rowsum, inner_out,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+bool valid_ffn_shape(int64_t M, int64_t K, int64_t F) {
+  return M >= 1 && M <= INT32_MAX && valid_k(K) && valid_k(F) && F <= kFfnMaxF;
+}
+// workspace of the expand-once GEMM path for the three projections (gate and up: N = F over
+// K; down: N = K over F), or 0 when that path does not apply (few rows, or K or F too long)
+int64_t ffn_ws_bytes(int64_t M, int64_t K, int64_t F) {
+  if (M <= kGemvMaxM || K > kMaxKTensorCore || F > kMaxKTensorCore) return 0;
+  const int64_t a = gemm_ws_bytes(M, F, K), b = gemm_ws_bytes(M, K, F);
+  return a > b ? a : b;
+}
+}  // namespace
+
+BITNET_API int64_t bitnet_w2a8_ffn_workspace_size(int64_t M, int64_t K, int64_t F) {
+  if (!valid_ffn_shape(M, K, F)) return BITNET_EINVAL;
+  return ffn_ws_bytes(M, K, F);
+}
+
+BITNET_API int bitnet_w2a8_ffn(const void* x, int dtype, int64_t M, int64_t K, int64_t F, const uint8_t* wp_gate,
+                               float a_gate, const uint8_t* wp_up, float a_up, const uint8_t* wp_down, float a_down,
+                               const float* gamma, float eps, float* gate_out, float* up_out, float* out, int8_t* xq,
+                               float* act_scale, int32_t* rowsum, void* workspace, int64_t workspace_bytes,
+                               void* stream) {
+  if (!x || !wp_gate || !wp_up || !wp_down || !gamma || !gate_out || !up_out || !out) return BITNET_EINVAL;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_EINVAL;
+  if (!valid_ffn_shape(M, K, F)) return BITNET_EINVAL;
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return BITNET_EINVAL;
+  const bool single = M == 1 && gemv_group_supported(K) && gemv_group_supported(F);
+  if (!single && (!xq || !act_scale || !rowsum)) return BITNET_EINVAL;
+  const int64_t ws_need = ffn_ws_bytes(M, K, F);
+  if (workspace && workspace_bytes < ws_need) return BITNET_EINVAL;
+  if (!aligned(x, 16) || !aligned(wp_gate, 16) || !aligned(wp_up, 16) || !aligned(wp_down, 16) ||
+      !aligned(gamma, 16) || !aligned(gate_out, 16) || !aligned(up_out, 16) || !aligned(out, 4))
+    return BITNET_EALIGN;
+  if ((xq && !aligned(xq, 16)) || (act_scale && !aligned(act_scale, 4)) || (rowsum && !aligned(rowsum, 4)) ||
+      (workspace && !aligned(workspace, 256)))
+    return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const FfnIn ffn{gate_out, up_out, gamma, eps};
+  if (single) {
+    // two launches: the gate/up group (quantising x), then the down projection whose input
+    // row is the sub-normed, quantised inner activation computed in its own prologue
+    LinearSet gu{};
+    gu.wp[0] = wp_gate, gu.wp[1] = wp_up;
+    gu.out[0] = gate_out, gu.out[1] = up_out;
+    gu.w_scale[0] = a_gate, gu.w_scale[1] = a_up;
+    gu.N[0] = gu.N[1] = (int)F;
+    gu.count = 2;
+    if (cudaError_t e = launch_gemv_group(x, dtype == BITNET_BF16, gu, QuantOut{}, Prefetch{}, K, sms, s))
+      return status_of(e);
+    LinearSet dn{};
+    dn.wp[0] = wp_down;
+    dn.out[0] = out;
+    dn.w_scale[0] = a_down;
+    dn.N[0] = (int)K;
+    dn.count = 1;
+    return status_of(launch_gemv_group_ffn(ffn, dn, QuantOut{xq, act_scale, rowsum}, Prefetch{}, F, sms, s));
+  }
+  auto matmul = [&](const uint8_t* wp, float a, float* o, int64_t N, int64_t Kd) -> int {
+    if (workspace && ws_need > 0)
+      return bitnet_i2s_matmul_ws(xq, act_scale, rowsum, wp, a, o, nullptr, M, N, Kd, workspace, workspace_bytes,
+                                  stream);
+    return bitnet_i2s_matmul_algo(xq, act_scale, rowsum, wp, a, o, nullptr, M, N, Kd, BITNET_ALGO_AUTO, stream);
+  };
+  if (cudaError_t e = launch_quant_act(x, dtype, M, K, xq, act_scale, rowsum, s)) return status_of(e);
+  if (int st = matmul(wp_gate, a_gate, gate_out, F, K)) return st;
+  if (int st = matmul(wp_up, a_up, up_out, F, K)) return st;
+  if (cudaError_t e = launch_ffn_act_quant(ffn, M, F, xq, act_scale, rowsum, nullptr, s)) return status_of(e);
+  return matmul(wp_down, a_down, out, K, F);
 }
 
 BITNET_API int bitnet_last_device_error(void) {

@@ -117,12 +117,19 @@ __device__ __forceinline__ int count_tiles(const int* N, int count, int begin, i
   return n;
 }
 
-// BF16: x is bf16 (else fp32).
+// Input row modes: fp32 x, bf16 x, or the FFN inner activation computed from the gate and up
+// rows (FfnIn: squared-ReLU gate times up, RMS sub-norm with gamma; K is then F).
+constexpr int kInF32 = 0, kInBF16 = 1, kInFfn = 2;
+
+// IN: the input row mode.
 // S: row steps per tile (1..8), a compile-time constant so the step loops carry no
 // predicated dead steps.
-template <bool BF16, int S>
+template <int IN, int S>
 __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __restrict__ xin, LinearSet set,
-                                                                 QuantOut qout, Prefetch pf, int K, int log2G) {
+                                                                 QuantOut qout, Prefetch pf, FfnIn ffn, int K,
+                                                                 int log2G) {
+  constexpr bool BF16 = IN == kInBF16;
+  constexpr bool FFN = IN == kInFfn;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;                      // kSlots x kSlotBytes
   uint8_t* xq_s = smem + kRingBytes;         // K + 64 bytes, [j][c][16] (c = C is zero)
@@ -130,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
   __shared__ __align__(16) float red_f[kConsumerWarps];  // read back as float4
   __shared__ __align__(16) int red_i[kConsumerWarps];    // read back as int4
+  __shared__ __align__(16) float red_ss[kConsumerWarps]; // FFN: run sums of the squares
   // the tile held by each ring slot (written by the producer before its release-arrive on
   // the slot's full barrier, read by the consumer after its acquire-wait)
   __shared__ int slot_rows[kSlots];
@@ -148,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   __shared__ int p_count;
   __shared__ const void* p_x;
   __shared__ QuantOut p_q;
+  __shared__ FfnIn p_ffn;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = K >> 6;
@@ -171,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
       p_count = set.count;
       p_x = xin;
       p_q = qout;
+      p_ffn = ffn;
     }
   }
   __syncthreads();
@@ -237,7 +247,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   const uint4* xv = static_cast<const uint4*>(p_x);
   // an L2 prefetch of the row is safe before the wait: it returns no data, and a write by
   // the previous kernel lands in L2 all the same
-  if (threadIdx.x == 0) prefetch_l2(xv, (uint32_t)K * (BF16 ? 2u : 4u));
+  const FfnIn fi = p_ffn;
+  if (threadIdx.x == 0) {
+    if constexpr (FFN) {
+      prefetch_l2(fi.gate, (uint32_t)K * 4u);
+      prefetch_l2(fi.up, (uint32_t)K * 4u);
+      prefetch_l2(fi.gamma, (uint32_t)K * 4u);  // model state: could be read before the wait too
+    } else {
+      prefetch_l2(xv, (uint32_t)K * (BF16 ? 2u : 4u));
+    }
+  }
   if (warp < n_tiles) mbar_wait(&full_bar[warp], 0, &abort);  // tile `warp`: slot warp, use 0
   float s_act;
   int rs_total;
@@ -248,19 +267,73 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     const int nvec = K / E;
     uint4 xr[kRegVec];
     float amax = 0.0f;
+    float c_ffn = 0.0f;
+    const float4* g4 = reinterpret_cast<const float4*>(fi.gate);
+    const float4* u4 = reinterpret_cast<const float4*>(fi.up);
+    const float4* gm4 = reinterpret_cast<const float4*>(fi.gamma);
+    if constexpr (FFN) {
+      // pass 1: h = max(g, 0)^2 * u and this thread's partial of the sum of squares
+      // (partial = thread, vectors in ascending order: the order FfnIn defines)
+      float ssp = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kMaxVecPerThread; ++i) {
-      const int v = threadIdx.x + kConsumers * i;
-      const uint4 u = v < nvec ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
-      if (i < kRegVec) xr[i] = u;
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+      for (int i = 0; i < kMaxVecPerThread; ++i) {
+        const int v = threadIdx.x + kConsumers * i;
+        if (v < nvec) {
+          const float4 g = __ldg(g4 + v), u = __ldg(u4 + v);
+          const float h0 = ffn_h(g.x, u.x), h1 = ffn_h(g.y, u.y), h2 = ffn_h(g.z, u.z), h3 = ffn_h(g.w, u.w);
+          ssp = __fmaf_rn(h0, h0, ssp);
+          ssp = __fmaf_rn(h1, h1, ssp);
+          ssp = __fmaf_rn(h2, h2, ssp);
+          ssp = __fmaf_rn(h3, h3, ssp);
+          if (i < kRegVec)
+            xr[i] = make_uint4(__float_as_uint(h0), __float_as_uint(h1), __float_as_uint(h2), __float_as_uint(h3));
+        }
+      }
+      ssp = ffn_run_sum(ssp);
+      if (lane == 0) red_ss[warp] = ssp;
+      named_bar_sync(1, kConsumers);
+      {
+        const float4 r0 = *reinterpret_cast<const float4*>(&red_ss[0]);
+        const float4 r1 = *reinterpret_cast<const float4*>(&red_ss[4]);
+        const float runs[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        c_ffn = ffn_rms_factor(ffn_runs_total(runs), K, fi.eps);
+      }
+      // pass 2: inner = (h * c) * gamma and its absolute maximum
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if constexpr (BF16) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] & 0xFFFF0000u)));
-        } else {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[e])));
+      for (int i = 0; i < kMaxVecPerThread; ++i) {
+        const int v = threadIdx.x + kConsumers * i;
+        if (v < nvec) {
+          float4 h;
+          if (i < kRegVec) {
+            h = make_float4(__uint_as_float(xr[i].x), __uint_as_float(xr[i].y), __uint_as_float(xr[i].z),
+                            __uint_as_float(xr[i].w));
+          } else {
+            const float4 g = __ldg(g4 + v), u = __ldg(u4 + v);
+            h = make_float4(ffn_h(g.x, u.x), ffn_h(g.y, u.y), ffn_h(g.z, u.z), ffn_h(g.w, u.w));
+          }
+          const float4 gm = __ldg(gm4 + v);
+          const float y0 = __fmul_rn(__fmul_rn(h.x, c_ffn), gm.x), y1 = __fmul_rn(__fmul_rn(h.y, c_ffn), gm.y);
+          const float y2 = __fmul_rn(__fmul_rn(h.z, c_ffn), gm.z), y3 = __fmul_rn(__fmul_rn(h.w, c_ffn), gm.w);
+          amax = fmaxf(fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1))), fmaxf(fabsf(y2), fabsf(y3)));
+          if (i < kRegVec)
+            xr[i] = make_uint4(__float_as_uint(y0), __float_as_uint(y1), __float_as_uint(y2), __float_as_uint(y3));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kMaxVecPerThread; ++i) {
+        const int v = threadIdx.x + kConsumers * i;
+        const uint4 u = v < nvec ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+        if (i < kRegVec) xr[i] = u;
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (BF16) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] & 0xFFFF0000u)));
+          } else {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w4[e])));
+          }
         }
       }
     }
@@ -285,7 +358,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     for (int i = 0; i < kMaxVecPerThread; ++i) {
       const int v = threadIdx.x + kConsumers * i;
       if (v < nvec) {
-        const uint4 u = i < kRegVec ? xr[i] : __ldg(xv + v);
+        uint4 u;
+        if (i < kRegVec) {
+          u = xr[i];
+        } else if constexpr (FFN) {  // recompute inner for a vector that did not stay in registers
+          const float4 g = __ldg(g4 + v), uu = __ldg(u4 + v), gm = __ldg(gm4 + v);
+          u = make_uint4(__float_as_uint(__fmul_rn(__fmul_rn(ffn_h(g.x, uu.x), c_ffn), gm.x)),
+                         __float_as_uint(__fmul_rn(__fmul_rn(ffn_h(g.y, uu.y), c_ffn), gm.y)),
+                         __float_as_uint(__fmul_rn(__fmul_rn(ffn_h(g.z, uu.z), c_ffn), gm.z)),
+                         __float_as_uint(__fmul_rn(__fmul_rn(ffn_h(g.w, uu.w), c_ffn), gm.w)));
+        } else {
+          u = __ldg(xv + v);
+        }
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
         uint32_t qb[E];
 #pragma unroll
@@ -449,10 +533,10 @@ int choose_log2g(int K) {
   return log2G;
 }
 
-template <bool BF16, int S>
-cudaError_t launch_s(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
-                     int blocks, cudaStream_t stream) {
-  auto kern = gemv_group_kernel<BF16, S>;
+template <int IN, int S>
+cudaError_t launch_s(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, const FfnIn& ffn,
+                     int K, int log2G, int blocks, cudaStream_t stream) {
+  auto kern = gemv_group_kernel<IN, S>;
   const int smem = kRingBytes + K + 64;  // ring, activations + one zero column per plane
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -474,12 +558,12 @@ cudaError_t launch_s(const void* x, const LinearSet& set, const QuantOut& q, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, set, q, pf, K, log2G);
+  return cudaLaunchKernelEx(&cfg, kern, x, set, q, pf, ffn, K, log2G);
 }
 
-template <bool BF16>
-cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, int K, int log2G,
-                     int num_sms, cudaStream_t stream) {
+template <int IN>
+cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, const Prefetch& pf, const FfnIn& ffn,
+                     int K, int log2G, int num_sms, cudaStream_t stream) {
   int64_t total = 0;
   for (int j = 0; j < set.count; ++j) total += set.N[j];
   const int rpw = 32 >> log2G;
@@ -496,14 +580,14 @@ cudaError_t launch_t(const void* x, const LinearSet& set, const QuantOut& q, con
   const int64_t want = ((per_cta + kConsumerWarps - 1) / kConsumerWarps + rpw - 1) / rpw;
   if (S > want) S = want < 1 ? 1 : want;
   switch (S) {
-    case 1: return launch_s<BF16, 1>(x, set, q, pf, K, log2G, blocks, stream);
-    case 2: return launch_s<BF16, 2>(x, set, q, pf, K, log2G, blocks, stream);
-    case 3: return launch_s<BF16, 3>(x, set, q, pf, K, log2G, blocks, stream);
-    case 4: return launch_s<BF16, 4>(x, set, q, pf, K, log2G, blocks, stream);
-    case 5: return launch_s<BF16, 5>(x, set, q, pf, K, log2G, blocks, stream);
-    case 6: return launch_s<BF16, 6>(x, set, q, pf, K, log2G, blocks, stream);
-    case 7: return launch_s<BF16, 7>(x, set, q, pf, K, log2G, blocks, stream);
-    default: return launch_s<BF16, 8>(x, set, q, pf, K, log2G, blocks, stream);
+    case 1: return launch_s<IN, 1>(x, set, q, pf, ffn, K, log2G, blocks, stream);
+    case 2: return launch_s<IN, 2>(x, set, q, pf, ffn, K, log2G, blocks, stream);
+    case 3: return launch_s<IN, 3>(x, set, q, pf, ffn, K, log2G, blocks, stream);
+    case 4: return launch_s<IN, 4>(x, set, q, pf, ffn, K, log2G, blocks, stream);
+    case 5: return launch_s<IN, 5>(x, set, q, pf, ffn, K, log2G, blocks, stream);
+    case 6: return launch_s<IN, 6>(x, set, q, pf, ffn, K, log2G, blocks, stream);
+    case 7: return launch_s<IN, 7>(x, set, q, pf, ffn, K, log2G, blocks, stream);
+    default: return launch_s<IN, 8>(x, set, q, pf, ffn, K, log2G, blocks, stream);
   }
 }
 
@@ -521,8 +605,15 @@ bool gemv_group_supported(int64_t K) { return K <= kMaxK; }
 cudaError_t launch_gemv_group(const void* x, bool bf16, const LinearSet& set, const QuantOut& qout,
                               const Prefetch& pf, int64_t K, int num_sms, cudaStream_t stream) {
   const int log2G = choose_log2g((int)K);
-  return bf16 ? launch_t<true>(x, set, qout, pf, (int)K, log2G, num_sms, stream)
-              : launch_t<false>(x, set, qout, pf, (int)K, log2G, num_sms, stream);
+  const FfnIn none{};
+  return bf16 ? launch_t<kInBF16>(x, set, qout, pf, none, (int)K, log2G, num_sms, stream)
+              : launch_t<kInF32>(x, set, qout, pf, none, (int)K, log2G, num_sms, stream);
+}
+
+cudaError_t launch_gemv_group_ffn(const FfnIn& ffn, const LinearSet& set, const QuantOut& qout, const Prefetch& pf,
+                                  int64_t F, int num_sms, cudaStream_t stream) {
+  const int log2G = choose_log2g((int)F);
+  return launch_t<kInFfn>(nullptr, set, qout, pf, ffn, (int)F, log2G, num_sms, stream);
 }
 
 }  // namespace bitnet

@@ -117,6 +117,57 @@ def test_quant_weight_rejects_bad_arguments_on_host(lib, args, status):
     assert lib.bitnet_quant_weight(*args, None) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    # (gate, up, gamma, eps, M, F, xq, s, rowsum, inner_out)
+    ((None, FAKE, FAKE, 1e-5, 1, 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, None, 1e-5, 1, 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, 1e-5, 1, 128, FAKE, None, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, 0.0, 1, 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, -1e-5, 1, 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, float("inf"), 1, 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, float("nan"), 1, 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, 1e-5, 0, 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, 1e-5, 1, 192, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE, FAKE, FAKE, 1e-5, 1, 32768 + 128, FAKE, FAKE, FAKE, None), -1),
+    ((FAKE + 4, FAKE, FAKE, 1e-5, 1, 128, FAKE, FAKE, FAKE, None), -2),
+    ((FAKE, FAKE, FAKE + 8, 1e-5, 1, 128, FAKE, FAKE, FAKE, None), -2),
+    ((FAKE, FAKE, FAKE, 1e-5, 1, 128, FAKE + 4, FAKE, FAKE, None), -2),
+    ((FAKE, FAKE, FAKE, 1e-5, 1, 128, FAKE, FAKE, FAKE, FAKE + 4), -2),
+])
+def test_ffn_act_quant_rejects_bad_arguments_on_host(lib, args, status):
+    assert lib.bitnet_ffn_act_quant(*args, None) == status
+
+
+def _ffn(lib, x=FAKE, dtype=0, M=1, K=128, F=128, wg=FAKE, wu=FAKE, wd=FAKE, gamma=FAKE, eps=1e-5, go=FAKE,
+         uo=FAKE, out=FAKE, xq=None, s=None, rs=None, ws=None, ws_bytes=0):
+    return lib.bitnet_w2a8_ffn(x, dtype, M, K, F, wg, 1.0, wu, 1.0, wd, 1.0, gamma, eps, go, uo, out, xq, s, rs, ws,
+                               ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), -1), (dict(wd=None), -1), (dict(gamma=None), -1), (dict(uo=None), -1),
+    (dict(dtype=2), -1), (dict(M=0), -1), (dict(K=192), -1), (dict(F=64), -1), (dict(F=32768 + 128), -1),
+    (dict(eps=0.0), -1), (dict(eps=float("nan")), -1),
+    (dict(M=2), -1),                                   # several rows need the quantisation workspace
+    (dict(M=1, K=10240 + 128), -1),                    # beyond the two-launch path: workspace again
+    (dict(M=65, K=256, F=256, xq=FAKE, s=FAKE, rs=FAKE, ws=FAKE, ws_bytes=16), -1),  # workspace too small
+    (dict(x=FAKE + 8), -2), (dict(wu=FAKE + 4), -2), (dict(go=FAKE + 4), -2), (dict(gamma=FAKE + 4), -2),
+    (dict(M=2, xq=FAKE + 4, s=FAKE, rs=FAKE), -2),
+])
+def test_w2a8_ffn_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _ffn(lib, **kw) == status
+
+
+def test_ffn_workspace_size(lib):
+    assert lib.bitnet_w2a8_ffn_workspace_size(1, 2560, 6912) == 0   # few rows: no expand-once path
+    assert lib.bitnet_w2a8_ffn_workspace_size(64, 2560, 6912) == 0
+    n = lib.bitnet_w2a8_ffn_workspace_size(4096, 2560, 6912)
+    assert n == max(lib.bitnet_i2s_matmul_workspace_size(4096, 6912, 2560),
+                    lib.bitnet_i2s_matmul_workspace_size(4096, 2560, 6912))
+    assert lib.bitnet_w2a8_ffn_workspace_size(0, 2560, 6912) == -1
+    assert lib.bitnet_w2a8_ffn_workspace_size(4096, 2560, 32768 + 128) == -1
+
+
 def test_valid_call_without_gpu_is_unsupported(lib):
     import torch
 

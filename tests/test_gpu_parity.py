@@ -613,3 +613,107 @@ def test_quant_weight_then_matmul_chain():
     o_out, _ = oracle.ternary_matmul(o_xq, o_sx, oracle.pack_i2s(o_q)[0], float(o_s), nthreads=NT)
     assert scale == o_s
     assert np.array_equal(host(g_out).view(np.uint32), o_out.view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- FFN block
+
+def _ffn_gamma(F, seed):
+    rng = np.random.default_rng(seed)
+    return (1.0 + 0.1 * rng.standard_normal(F)).astype(np.float32)
+
+
+@pytest.mark.parametrize("M,F,eps", [
+    (1, 128, 1e-5), (3, 6912, 1e-5), (5, 1152, 0.25), (2, 28672, 1e-5), (7, 32768, 1e-6), (300, 2560, 1e-5),
+])
+def test_ffn_act_quant_parity(M, F, eps):
+    """inner (bit pattern), xq, s and rowsum of the fused sub-norm + quantisation kernel against
+    oracle.ffn_inner followed by oracle.quant_act."""
+    rng = np.random.default_rng(500 + F + M)
+    g = (rng.standard_normal((M, F)) * 1.5).astype(np.float32)
+    u = rng.standard_normal((M, F)).astype(np.float32)
+    gamma = _ffn_gamma(F, 501)
+    inner = torch.empty((M, F), dtype=torch.float32, device="cuda")
+    g_xq, g_s, g_rs = binding.ffn_act_quant(dev(g), dev(u), dev(gamma), eps, inner_out=inner)
+    torch.cuda.synchronize()
+    o_inner = oracle.ffn_inner(g, u, gamma, eps)
+    o_xq, o_s, o_rs = oracle.quant_act(o_inner)
+    assert np.array_equal(host(inner).view(np.uint32), o_inner.view(np.uint32))
+    assert np.array_equal(host(g_xq), o_xq)
+    assert np.array_equal(host(g_s).view(np.uint32), o_s.view(np.uint32))
+    assert np.array_equal(host(g_rs), o_rs)
+
+
+def test_ffn_act_quant_degenerate_rows():
+    """All gates non-positive (inner = 0: s at the 1e-5 floor, every code 0), a single positive
+    gate (one code at +-127), and a row with huge and tiny h side by side."""
+    F = 1024
+    g = np.full((3, F), -1.0, np.float32)
+    u = np.ones((3, F), np.float32)
+    g[1, 77] = 2.0
+    rng = np.random.default_rng(510)
+    g[2] = rng.standard_normal(F).astype(np.float32)
+    g[2, :8] = [1e6, 1e-6, 3e5, -2.0, 7e-8, 1.0, 1e4, 5e-3]
+    gamma = _ffn_gamma(F, 511)
+    g_xq, g_s, g_rs = binding.ffn_act_quant(dev(g), dev(u), dev(gamma), 1e-5)
+    torch.cuda.synchronize()
+    o_xq, o_s, o_rs = oracle.quant_act(oracle.ffn_inner(g, u, gamma, 1e-5))
+    assert np.all(o_xq[0] == 0) and o_s[0] == np.float32(127.0) / np.float32(1e-5)
+    assert abs(int(o_xq[1, 77])) == 127
+    assert np.array_equal(host(g_xq), o_xq)
+    assert np.array_equal(host(g_s).view(np.uint32), o_s.view(np.uint32))
+    assert np.array_equal(host(g_rs), o_rs)
+
+
+def _ffn_oracle(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps):
+    """The FFN block on the CPU: quant_act -> gate/up matmuls -> ffn_inner -> quant_act -> down."""
+    xq, s, _ = oracle.quant_act(x_np, dtype)
+    gate, _ = oracle.ternary_matmul(xq, s, oracle.pack_i2s(wg)[0], ag, nthreads=NT)
+    up, _ = oracle.ternary_matmul(xq, s, oracle.pack_i2s(wu)[0], au, nthreads=NT)
+    iq, i_s, i_rs = oracle.quant_act(oracle.ffn_inner(gate, up, gamma, eps))
+    out, _ = oracle.ternary_matmul(iq, i_s, oracle.pack_i2s(wd)[0], ad, nthreads=NT)
+    return dict(gate=gate, up=up, xq=iq, s=i_s, rs=i_rs, out=out)
+
+
+FFN_CASES = [
+    # (M, K, F, dtype, workspace): the two-launch path (M = 1, including a row too long for
+    # the registers, F = 10240), the few-token and GEMM paths, and the expand-once workspace
+    (1, 2560, 6912, "f32", False), (1, 2560, 6912, "bf16", False), (1, 512, 10240, "f32", False),
+    (1, 1024, 128, "bf16", False), (2, 2560, 6912, "bf16", False), (17, 640, 1280, "f32", False),
+    (65, 2560, 6912, "bf16", False), (130, 1024, 2048, "f32", True),
+]
+
+
+@pytest.mark.parametrize("M,K,F,dtype,use_ws", FFN_CASES)
+def test_w2a8_ffn_parity(M, K, F, dtype, use_ws):
+    """gate/up outputs, the quantised inner rows and the block output, bit for bit."""
+    seed = 520 + M + F
+    x_np = workloads.activations(M, K, seed, dtype)
+    wg = workloads.ternary_weights(F, K, seed + 1)
+    wu = workloads.ternary_weights(F, K, seed + 2)
+    wd = workloads.ternary_weights(K, F, seed + 3)
+    ag, au, ad = (workloads.weight_scale(F, K, seed + 4), workloads.weight_scale(F, K, seed + 5),
+                  workloads.weight_scale(K, F, seed + 6))
+    gamma = _ffn_gamma(F, seed + 7)
+    eps = 1e-5
+    g_wg, g_wu, g_wd = binding.pack_i2s(dev(wg)), binding.pack_i2s(dev(wu)), binding.pack_i2s(dev(wd))
+    gate = torch.empty((M, F), dtype=torch.float32, device="cuda")
+    up = torch.empty((M, F), dtype=torch.float32, device="cuda")
+    xq = torch.empty((M, max(K, F)), dtype=torch.int8, device="cuda")
+    s = torch.empty(M, dtype=torch.float32, device="cuda")
+    rs = torch.empty(M, dtype=torch.int32, device="cuda")
+    ws = None
+    if use_ws:
+        ws = torch.empty(binding.ffn_workspace_size(M, K, F), dtype=torch.uint8, device="cuda")
+    g_out = binding.w2a8_ffn(x_device(x_np, dtype), g_wg, ag, g_wu, au, g_wd, ad, dev(gamma), eps,
+                             gate_out=gate, up_out=up, xq=xq, scale=s, rowsum=rs, workspace=ws)
+    torch.cuda.synchronize()
+    o = _ffn_oracle(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps)
+    assert np.array_equal(host(gate).view(np.uint32), o["gate"].view(np.uint32))
+    assert np.array_equal(host(up).view(np.uint32), o["up"].view(np.uint32))
+    # the workspace holds the quantised inner rows as a contiguous M x F array at its start
+    assert np.array_equal(host(xq).reshape(-1)[:M * F].reshape(M, F), o["xq"])
+    assert np.array_equal(host(s).view(np.uint32), o["s"].view(np.uint32))
+    assert np.array_equal(host(rs), o["rs"])
+    assert_out_close(host(g_out), o["out"])
+    assert np.array_equal(host(g_out).view(np.uint32), o["out"].view(np.uint32))
+    assert binding.last_device_error() == 0
