@@ -54,6 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-gemv-leg", action="store_true", help="skip the 100B-class GEMV leg of the default line")
+    p.add_argument("--no-ffn-leg", action="store_true", help="skip the fused FFN-block leg of the default line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill"], default="decode_sweep",
                    help="decode_sweep (default, the headline) or one single-kernel leg")
@@ -385,6 +386,77 @@ def kernel_leg(kind, device, peaks, reps=20, warmup=3, sets=None):
                          "traffic": recorded_traffic("gemv_i2s.cu")}}
 
 
+def ffn_leg(stack, device, peaks, reps=20):
+    """The FFN block of every layer of the sweep at M=1, chained in one CUDA graph: per layer
+    bitnet_w2a8_ffn (the gate/up group launch, then the down projection with the squared-ReLU
+    gate, RMS sub-norm and quantisation in its prologue) on the sweep's resident gate/up/down
+    weights (30 x 13.27 MB, larger than L2). The same chain unfused (group, then
+    bitnet_ffn_act_quant, then the down GEMV: three launches) is timed beside it."""
+    import torch
+
+    from ternary_weight_gb300 import binding
+
+    by_name = {g.name: g for g in stack.groups}
+    layers = sorted({int(g.name.split(".")[0][1:]) for g in stack.groups})
+    blocks = []
+    for l in layers:
+        gin, gmid = by_name["L%d.ffn_in" % l], by_name["L%d.ffn_mid" % l]
+        gate_l, up_l = gin.linears
+        down_l = gmid.linears[0]
+        K, F = gin.K, gate_l.N
+        x = stack.x[stack.groups.index(gin)]
+        gamma = torch.from_numpy(workloads.rmsnorm_gamma(F, 7000 + l)).to(device)
+        blocks.append(dict(x=x, gate=gate_l, up=up_l, down=down_l, gamma=gamma, K=K, F=F,
+                           go=torch.empty((1, F), dtype=torch.float32, device=device),
+                           uo=torch.empty((1, F), dtype=torch.float32, device=device),
+                           out=torch.empty((1, K), dtype=torch.float32, device=device),
+                           xq=torch.empty((1, F), dtype=torch.int8, device=device),
+                           s=torch.empty(1, dtype=torch.float32, device=device),
+                           rs=torch.empty(1, dtype=torch.int32, device=device)))
+
+    def fused():
+        for b in blocks:
+            binding.w2a8_ffn(b["x"], b["gate"].wp, b["gate"].w_scale, b["up"].wp, b["up"].w_scale, b["down"].wp,
+                             b["down"].w_scale, b["gamma"], workloads.FFN_EPS, out=b["out"], gate_out=b["go"],
+                             up_out=b["uo"])
+
+    def unfused():
+        for b in blocks:
+            binding.linear_group(b["x"], [b["gate"].wp, b["up"].wp], [b["gate"].w_scale, b["up"].w_scale],
+                                 outs=[b["go"], b["uo"]])
+            binding.ffn_act_quant(b["go"], b["uo"], b["gamma"], workloads.FFN_EPS, xq=b["xq"], scale=b["s"],
+                                  rowsum=b["rs"])
+            binding.i2s_matmul(b["xq"], b["s"], b["rs"], b["down"].wp, b["down"].w_scale, out=b["out"])
+
+    stream = torch.cuda.current_stream(device)
+    times = {}
+    for name, fn in (("fused", fused), ("unfused", unfused)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(device)
+        times[name] = time_replays(g, reps, stream) / reps
+    n = len(blocks)
+    K, F = blocks[0]["K"], blocks[0]["F"]
+    # algorithmic bytes per block: the three packed weight matrices, x (fp32), gate/up written and
+    # read back, gamma, the output
+    per_block = 3 * F * K // 4 + 4 * K + 2 * (2 * 4 * F) + 4 * F + 4 * K
+    gbs = per_block * n / times["fused"] / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"workload": "FFN block (gate/up W2A8, squared-ReLU gate, RMS sub-norm, act-quant, down W2A8) of "
+                        "%d layers, M=1, K=%d, F=%d, fp32 input rows" % (n, K, F),
+            "value": gbs, "unit": "GB/s", "us_per_block": times["fused"] / n * 1e6,
+            "launches_per_block": 2, "unfused_us_per_block": times["unfused"] / n * 1e6,
+            "unfused_launches_per_block": 3, "bytes_per_block": per_block,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "note": "latency-bound chain: the block's two launches average"}}
+
+
 def run_kernel_workload(args):
     """--workload gemv_100b | prefill: one line for that single kernel (no e2e / CPU leg)."""
     import torch
@@ -491,6 +563,7 @@ def run_ours(args):
 
     prefill = None if args.no_prefill else kernel_leg("prefill", device, peaks)
     gemv_100b = None if args.no_gemv_leg else kernel_leg("gemv_100b", device, peaks)
+    ffn = None if args.no_ffn_leg else ffn_leg(stack, device, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -519,6 +592,7 @@ def run_ours(args):
                 "note": "pinned host activations -> device, graph step, all projection outputs -> host, each step"},
         "prefill": prefill,
         "gemv_100b": gemv_100b,
+        "ffn": ffn,
         "cpu_baseline": cpu,
     }
     if rank == 0:

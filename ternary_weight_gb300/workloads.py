@@ -18,6 +18,7 @@ Recipe (all draws use numpy's PCG64 ``default_rng`` with the seed stated per ten
     0.02*sqrt(2/pi) ~= 0.01596);
   * activations: fp32 N(0, 1), or fp32 N(0, 1) rounded to bf16 (round-to-nearest-even),
     optionally with Bernoulli(p) outliers multiplied by 20 before the rounding;
+  * FFN sub-norm weight gamma: fp32 1 + 0.1 N(0, 1), epsilon 1e-5;
   * full-precision weights for the ternarisation: fp32 N(0, 0.02^2); for the sign rule,
     ternary weights times 0.0156 with each zero replaced by a magnitude uniform in
     [0.5e-6, 2e-6] of random sign (so about a third of them fall below the 1e-6 threshold).
@@ -86,6 +87,15 @@ def near_ternary_weights_f32(N: int, K: int, seed: int, a: float = 0.0156) -> np
     t = ternary_weights(N, K, seed).astype(np.float32) * np.float32(a)
     tiny = (rng.uniform(0.5e-6, 2e-6, size=(N, K)) * rng.choice([-1.0, 1.0], size=(N, K))).astype(np.float32)
     return np.where(t == 0, tiny, t).astype(np.float32)
+
+
+def rmsnorm_gamma(F: int, seed: int) -> np.ndarray:
+    """F fp32 per-channel weights of an RMSNorm (the FFN sub-norm): 1 + 0.1 N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    return (1.0 + 0.1 * rng.standard_normal(F)).astype(np.float32)
+
+
+FFN_EPS = 1e-5  # the sub-norm's epsilon in the FFN workloads (the pages print none)
 
 
 def activations_f32(M: int, K: int, seed: int, outlier_p: float = 0.0) -> np.ndarray:

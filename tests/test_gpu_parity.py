@@ -618,8 +618,7 @@ def test_quant_weight_then_matmul_chain():
 # ----------------------------------------------------------------------------- FFN block
 
 def _ffn_gamma(F, seed):
-    rng = np.random.default_rng(seed)
-    return (1.0 + 0.1 * rng.standard_normal(F)).astype(np.float32)
+    return workloads.rmsnorm_gamma(F, seed)
 
 
 @pytest.mark.parametrize("M,F,eps", [
