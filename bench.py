@@ -56,7 +56,7 @@ def parse_args(argv=None):
     p.add_argument("--no-gemv-leg", action="store_true", help="skip the 100B-class GEMV leg of the default line")
     p.add_argument("--no-ffn-leg", action="store_true", help="skip the fused FFN-block leg of the default line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
-    p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill"], default="decode_sweep",
+    p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill", "ffn"], default="decode_sweep",
                    help="decode_sweep (default, the headline) or one single-kernel leg")
     return p.parse_args(argv)
 
@@ -469,15 +469,21 @@ def run_kernel_workload(args):
     _build.build()
     binding.lib()
     peaks, _ = measured_peaks()
+    stack = build_stack(args.layers, device)[0] if args.workload == "ffn" else None
     sampler = ClockSampler(local)
     sampler.start()
-    leg = kernel_leg(args.workload, device, peaks, reps=args.steps, warmup=args.warmup)
+    if args.workload == "ffn":
+        leg = ffn_leg(stack, device, peaks, reps=args.steps)
+        leg["ms_per_call"] = leg["us_per_block"] * args.layers * 1e-3  # one step = every layer's block
+    else:
+        leg = kernel_leg(args.workload, device, peaks, reps=args.steps, warmup=args.warmup)
     clocks = sampler.stop()
     line = {"metric": METRIC, "value": leg["value"], "unit": leg["unit"], "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": leg["ms_per_call"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "i8xi2->i32", "data": "synthetic",
             "config": {"workload": leg["workload"], "l2": "rotating input sets larger than L2"},
-            "gpu_launches": args.steps, "clocks": clocks, "roofline": leg["roofline"]}
+            "gpu_launches": args.steps * (2 * args.layers if args.workload == "ffn" else 1), "clocks": clocks,
+            "roofline": leg["roofline"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
