@@ -320,6 +320,37 @@ BITNET_API int bitnet_w2a8_ffn(const void *x, int dtype, int64_t M, int64_t K, i
                                int32_t *rowsum, void *workspace, int64_t workspace_bytes, void *stream);
 
 /*
+ * Persistent sweep over independent projection groups -- one kernel launch that computes, for
+ * every group g, exactly what bitnet_w2a8_linear_group(x, dtype, 1, K, count, wp, w_scale, N,
+ * out, NULL, ...) computes for that group at M = 1 (per-token quantisation of x, then the
+ * ternary matmuls; [DeepDive] §4-5 and §4-2, "bitnet.rs" "Quantised Forward Pass").
+ *   The groups must be independent: no group's x may be written by any group's out in the
+ *   same run. This is the set of projections of a decode step whose input rows are given,
+ *   streamed at HBM rate. A chain of dependent layers is the per-group call, launch by launch.
+ *   One CTA per SM streams a contiguous slice of all groups' packed weights through a
+ *   192 KB shared-memory ring.
+ * bitnet_sweep_plan_create validates the table and copies it to the current device (host,
+ * synchronous; allocates the plan's device table). Pointers inside are bound to the plan.
+ * bitnet_sweep_plan_run launches it on `stream` (no allocation; may be captured into a CUDA
+ * graph); the current device must be the plan's.
+ * bitnet_sweep_plan_destroy frees the plan (NULL is a no-op).
+ */
+typedef struct bitnet_linear_group {
+  const void *x;            /* K activations, dtype of the plan (device), 16-byte aligned     */
+  int64_t K;                /* multiple of 128, 128 <= K <= 10240                             */
+  int count;                /* 1..8 projections                                               */
+  const uint8_t *wp[8];     /* wp[l]: N[l] x K/4 packed codes (device), 16-byte aligned       */
+  float w_scale[8];         /* alpha_W of each projection                                     */
+  int64_t N[8];             /* rows of each projection, >= 1 (total over all groups < 2^31)   */
+  float *out[8];            /* out[l]: N[l] fp32 (device, written), 4-byte aligned            */
+} bitnet_linear_group;
+typedef struct bitnet_sweep_plan_s *bitnet_sweep_plan;
+BITNET_API int bitnet_sweep_plan_create(const bitnet_linear_group *groups, int n_groups, int dtype,
+                                        bitnet_sweep_plan *plan);
+BITNET_API int bitnet_sweep_plan_run(bitnet_sweep_plan plan, void *stream);
+BITNET_API int bitnet_sweep_plan_destroy(bitnet_sweep_plan plan);
+
+/*
  * bitnet_last_device_error -- read and clear the device-side error word of the current
  * device. Kernels that wait on an mbarrier give up after a bounded number of polls and
  * record BITNET_ETIMEOUT there instead of hanging; bitnet_quant_weight records BITNET_ERANGE

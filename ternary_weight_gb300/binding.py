@@ -52,6 +52,9 @@ SIGNATURES = {
     "bitnet_quant_weight": ([_P, ctypes.c_int, ctypes.c_int, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "bitnet_ffn_act_quant": ([_P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
     "bitnet_w2a8_ffn_workspace_size": ([_I64, _I64, _I64], _I64),
+    "bitnet_sweep_plan_create": ([_P, ctypes.c_int, ctypes.c_int, _P], ctypes.c_int),
+    "bitnet_sweep_plan_run": ([_P, _P], ctypes.c_int),
+    "bitnet_sweep_plan_destroy": ([_P], ctypes.c_int),
     "bitnet_w2a8_ffn": (
         [_P, ctypes.c_int, _I64, _I64, _I64, _P, ctypes.c_float, _P, ctypes.c_float, _P, ctypes.c_float, _P,
          ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _I64, _P], ctypes.c_int),
@@ -342,3 +345,64 @@ def w2a8_ffn(x, wp_gate, a_gate, wp_up, a_up, wp_down, a_down, gamma, eps, out=N
                                  ws_bytes, _stream(stream)),
            "bitnet_w2a8_ffn")
     return out
+
+
+class LinearGroupDesc(ctypes.Structure):
+    """ctypes mirror of bitnet_linear_group (include/bitnet.h)."""
+    _fields_ = [("x", ctypes.c_void_p), ("K", ctypes.c_int64), ("count", ctypes.c_int),
+                ("wp", ctypes.c_void_p * 8), ("w_scale", ctypes.c_float * 8), ("N", ctypes.c_int64 * 8),
+                ("out", ctypes.c_void_p * 8)]
+
+
+class SweepPlan:
+    """A persistent sweep over independent projection groups (one kernel launch per run).
+
+    ``groups`` is a list of (x, [(wp, w_scale, out), ...]) with x a 1-D fp32 or bf16 CUDA
+    tensor of K values, wp an N x K/4 uint8 tensor and out an N-element fp32 tensor. The
+    tensors are bound to the plan (it keeps references to them); run() recomputes every
+    group's outputs from the current contents of its x."""
+
+    def __init__(self, groups):
+        import torch
+
+        if not groups:
+            raise ValueError("at least one group")
+        dt = None
+        descs = (LinearGroupDesc * len(groups))()
+        self._keep = []
+        for g, (x, projs) in enumerate(groups):
+            d = _act_dtype(x.view(1, -1))
+            if dt is None:
+                dt = d
+            elif d != dt:
+                raise ValueError("every group's x must have the same dtype")
+            if not 1 <= len(projs) <= 8:
+                raise ValueError("1..8 projections per group")
+            K = x.numel()
+            desc = descs[g]
+            desc.x, desc.K, desc.count = x.data_ptr(), K, len(projs)
+            for l, (wp, w_scale, out) in enumerate(projs):
+                if wp.shape[1] * 4 != K or out.numel() != wp.shape[0] or out.dtype != torch.float32:
+                    raise ValueError("wp must be N x K/4 and out N fp32")
+                desc.wp[l], desc.w_scale[l], desc.N[l], desc.out[l] = wp.data_ptr(), float(w_scale), wp.shape[0], \
+                    out.data_ptr()
+            _require_cuda(x, *[t for p in projs for t in (p[0], p[2])])
+            self._keep.append((x, projs))
+        self._handle = ctypes.c_void_p()
+        _check(lib().bitnet_sweep_plan_create(ctypes.cast(descs, ctypes.c_void_p), len(groups), dt,
+                                              ctypes.byref(self._handle)),
+               "bitnet_sweep_plan_create")
+
+    def run(self, stream=None):
+        _check(lib().bitnet_sweep_plan_run(self._handle, _stream(stream)), "bitnet_sweep_plan_run")
+
+    def close(self):
+        if getattr(self, "_handle", None) and self._handle.value:
+            lib().bitnet_sweep_plan_destroy(self._handle)
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -115,6 +115,19 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// The same barrier, returning the OR of `pred` over all the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -297,6 +310,20 @@ __device__ __forceinline__ float ffn_runs_total(const float* r) {
                    __fadd_rn(__fadd_rn(r[4], r[5]), __fadd_rn(r[6], r[7])));
 }
 
+// One group of the persistent sweep (gemv_sweep.cu): an activation row and the projections
+// that consume it. row0 / byte0 are the group's first row and first packed byte in the
+// concatenated row space of all groups, rows its row count; log2G and S are the lane layout
+// and the steps per tile chosen for K.
+struct SweepGroup {
+  const void* x;
+  int64_t byte0;
+  int K, log2G, S, count, row0, rows;
+  const uint8_t* wp[kMaxGroupLinears];
+  float* out[kMaxGroupLinears];
+  float w_scale[kMaxGroupLinears];
+  int N[kMaxGroupLinears];
+};
+
 constexpr int kMaxPrefetch = 8;
 struct Prefetch {  // byte ranges to pull into L2 (a hint; 16-byte aligned starts)
   const void* ptr[kMaxPrefetch];
@@ -317,6 +344,21 @@ cudaError_t launch_gemv_group(const void* x, bool bf16, const LinearSet& set, co
 // projection of the FFN, fused with the sub-norm and the quantisation.
 cudaError_t launch_gemv_group_ffn(const FfnIn& ffn, const LinearSet& set, const QuantOut& qout, const Prefetch& pf,
                                   int64_t F, int num_sms, cudaStream_t stream);
+// One CTA's share of the sweep: rows [begin, end) of the concatenated row space, whose first
+// row lies in group g0.
+struct SweepSlice {
+  int begin, end, g0;
+};
+// Persistent sweep over independent groups (gemv_sweep.cu). groups_dev (n_groups entries) and
+// slices_dev (one per CTA, grid = n_slices) are device tables built by the host.
+bool gemv_sweep_supported(int64_t K);
+void sweep_fill_layout(SweepGroup& g);  // host: log2G and S from K
+// host: the slices of n CTAs, balanced by packed bytes; total_rows >= n
+void sweep_slices(const SweepGroup* groups, int n_groups, int total_rows, int64_t total_bytes, int n,
+                  SweepSlice* slices);
+cudaError_t launch_gemv_sweep(const SweepGroup* groups_dev, int n_groups, const SweepSlice* slices_dev, int n_slices,
+                              bool bf16, cudaStream_t stream);
+cudaError_t read_clear_device_error_sweep(int* value);
 // FFN inner activation + per-token quantisation for M rows (ffn.cu); inner_out optional.
 constexpr int64_t kFfnMaxF = 32768;
 cudaError_t launch_ffn_act_quant(const FfnIn& ffn, int64_t M, int64_t F, int8_t* xq, float* act_scale,

@@ -7,6 +7,8 @@
 #include "bitnet_dev.cuh"
 
 #include <cmath>
+#include <new>
+#include <vector>
 
 #include <atomic>
 #include <cstdint>
@@ -334,6 +336,97 @@ BITNET_API int bitnet_w2a8_ffn(const void* x, int dtype, int64_t M, int64_t K, i
   return matmul(wp_down, a_down, out, K, F);
 }
 
+// ---- the persistent sweep: a plan owns device copies of the group table and of the per-CTA
+// slices (built once on the host) ----
+struct bitnet_sweep_plan_s {
+  bitnet::SweepGroup* table;   // device, n_groups entries
+  bitnet::SweepSlice* slices;  // device, n_slices entries (one per CTA)
+  int n_groups;
+  int n_slices;
+  int dtype;
+  int device;
+};
+
+BITNET_API int bitnet_sweep_plan_create(const bitnet_linear_group* groups, int n_groups, int dtype,
+                                        bitnet_sweep_plan* plan) {
+  if (!plan) return BITNET_EINVAL;
+  *plan = nullptr;
+  if (!groups || n_groups < 1 || n_groups > (1 << 20)) return BITNET_EINVAL;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_EINVAL;
+  std::vector<SweepGroup> host((size_t)n_groups);
+  int64_t rows = 0, bytes = 0;
+  for (int g = 0; g < n_groups; ++g) {
+    const bitnet_linear_group& in = groups[g];
+    if (!in.x || in.count < 1 || in.count > kMaxGroupLinears) return BITNET_EINVAL;
+    if (!valid_k(in.K) || !gemv_sweep_supported(in.K)) return BITNET_EINVAL;
+    if (!aligned(in.x, 16)) return BITNET_EALIGN;
+    SweepGroup& out = host[(size_t)g];
+    out = SweepGroup{};
+    out.x = in.x;
+    out.K = (int)in.K;
+    out.count = in.count;
+    out.row0 = (int)rows;
+    out.byte0 = bytes;
+    for (int l = 0; l < in.count; ++l) {
+      if (!in.wp[l] || !in.out[l] || in.N[l] < 1 || in.N[l] > INT32_MAX) return BITNET_EINVAL;
+      if (!aligned(in.wp[l], 16) || !aligned(in.out[l], 4)) return BITNET_EALIGN;
+      out.wp[l] = in.wp[l];
+      out.out[l] = in.out[l];
+      out.w_scale[l] = in.w_scale[l];
+      out.N[l] = (int)in.N[l];
+      rows += in.N[l];
+      if (rows > INT32_MAX) return BITNET_EINVAL;
+    }
+    out.rows = (int)(rows - out.row0);
+    bytes += (int64_t)out.rows * (in.K / 4);
+    sweep_fill_layout(out);
+  }
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  // one CTA per SM (fewer if there are fewer rows), each with a byte-balanced slice
+  const int n_slices = (int)(rows < sms ? rows : sms);
+  std::vector<SweepSlice> slices((size_t)n_slices);
+  sweep_slices(host.data(), n_groups, (int)rows, bytes, n_slices, slices.data());
+  auto* p = new (std::nothrow) bitnet_sweep_plan_s{};
+  if (!p) return BITNET_ECUDA;
+  const size_t tb = sizeof(SweepGroup) * (size_t)n_groups, sb = sizeof(SweepSlice) * (size_t)n_slices;
+  const bool ok = cudaGetDevice(&p->device) == cudaSuccess &&
+                  cudaMalloc(reinterpret_cast<void**>(&p->table), tb) == cudaSuccess &&
+                  cudaMalloc(reinterpret_cast<void**>(&p->slices), sb) == cudaSuccess &&
+                  cudaMemcpy(p->table, host.data(), tb, cudaMemcpyHostToDevice) == cudaSuccess &&
+                  cudaMemcpy(p->slices, slices.data(), sb, cudaMemcpyHostToDevice) == cudaSuccess;
+  if (!ok) {
+    cudaFree(p->table);
+    cudaFree(p->slices);
+    delete p;
+    return BITNET_ECUDA;
+  }
+  p->n_groups = n_groups;
+  p->n_slices = n_slices;
+  p->dtype = dtype;
+  *plan = p;
+  return BITNET_OK;
+}
+
+BITNET_API int bitnet_sweep_plan_run(bitnet_sweep_plan plan, void* stream) {
+  if (!plan) return BITNET_EINVAL;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BITNET_ECUDA;
+  if (dev != plan->device) return BITNET_EINVAL;
+  return status_of(launch_gemv_sweep(plan->table, plan->n_groups, plan->slices, plan->n_slices,
+                                     plan->dtype == BITNET_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+BITNET_API int bitnet_sweep_plan_destroy(bitnet_sweep_plan plan) {
+  if (!plan) return BITNET_OK;
+  const cudaError_t e1 = cudaFree(plan->table);
+  const cudaError_t e2 = cudaFree(plan->slices);
+  delete plan;
+  return e1 == cudaSuccess && e2 == cudaSuccess ? BITNET_OK : BITNET_ECUDA;
+}
+
 BITNET_API int bitnet_last_device_error(void) {
   int sms = 0;
   if (int st = check_device(&sms)) return st;
@@ -341,7 +434,7 @@ BITNET_API int bitnet_last_device_error(void) {
   int status = BITNET_OK;
   cudaError_t (*readers[])(int*) = {read_clear_device_error_gemm, read_clear_device_error_gemm_ws,
                                     read_clear_device_error_gemv_group, read_clear_device_error_smallm,
-                                    read_clear_device_error_quant_weight};
+                                    read_clear_device_error_quant_weight, read_clear_device_error_sweep};
   for (auto rd : readers) {
     int v = 0;
     if (rd(&v) != cudaSuccess) return BITNET_ECUDA;

@@ -43,7 +43,7 @@
 //    sum when asked.
 //  * Every wait is bounded; a timeout is recorded in the device error word and the kernel
 //    leaves after waiting (bounded) for the copies it issued.
-#include "bitnet_dev.cuh"
+#include "gemv_tile.cuh"
 
 #include <atomic>
 
@@ -65,8 +65,6 @@ constexpr int kMaxK = 10240;            // largest K this kernel takes
 // and the quantise pass (all of them for K <= 6144 fp32 / 12288 bf16), the rest are re-read
 constexpr int kMaxVecPerThread = kMaxK / 4 / (kConsumerWarps * 32);
 constexpr int kRegVec = 6;
-// chunk columns per lane: the lane layout keeps C/G <= 5, or G = 32 with C <= kMaxK/64 = 160
-constexpr int kMaxColsPerLane = 5;
 static_assert(kMaxK / 64 <= 32 * kMaxColsPerLane, "column loop bound");
 // Tile i lives in slot i % kSlots and is consumed by warp i % kConsumerWarps. With the slot
 // count a multiple of the consumer-warp count, every slot is only ever waited on by one
@@ -91,18 +89,6 @@ __device__ __forceinline__ void issue_prefetch(const Prefetch& pf) {
       lo += len;
     }
   }
-}
-
-// x * s rounded to the nearest integer, ties to even, returned as the bits of the fp32 sum
-// x*s + 1.5*2^23: for |x*s| < 2^22 the sum lies in [2^23, 2^24), where fp32 steps by exactly 1,
-// so the round-to-nearest-even add performs the integer rounding (1.5*2^23 is even, so ties
-// go the same way), and bits - 0x4B400000 is the integer; its low byte is the int8 code.
-// The clamp to [-127, 127] is never active: s = fl(127/a) with a >= max|x| gives
-// |fl(x*s)| <= 127 (1 + 2^-24)^2 < 127.5, so the rounded value is at most 127 in magnitude.
-constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
-constexpr uint32_t kRoundMagicBits = 0x4B400000u;
-__device__ __forceinline__ uint32_t quant_bits(float x, float s) {
-  return __float_as_uint(__fadd_rn(__fmul_rn(x, s), kRoundMagic));
 }
 
 // Number of tiles (whole-row runs of at most TR rows, never across two projections) in the
@@ -425,7 +411,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   // A transpose-reduce over the G lanes (three halving levels, then plain xor levels) leaves
   // the total of step st in the lanes whose top three lane-in-group bits spell st, so the
   // epilogue (one IEEE divide per output) runs for up to 8 rows in parallel. ----
-  const int hb = (G >= 8) ? log2G - 3 : 0;  // low lane bits left after the halving levels
   const uint32_t xq_u = smem_u32(xq_s);
   const int step_stride = rpw * row_bytes;
   for (int i = warp; i < n_tiles; i += kConsumerWarps) {
@@ -441,82 +426,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
     const float ws = slot_ws[slot];
     // this lane's row of step 0; step st is st * step_stride bytes further
     const uint32_t tile_lane = smem_u32(ring + slot * kSlotBytes) + (uint32_t)(rg * row_bytes);
-    // per step: hi = 64 * (sum of bit pairs 0 and 1), lo = 4 * (sum of bit pairs 2 and 3);
-    // shifting the weight word left by 2 puts pair 1 under pair 0's mask and pair 3 under
-    // pair 2's, so one accumulator serves two pairs at the same scale
-    int acc[S][2];
-#pragma unroll
-    for (int st = 0; st < S; ++st) acc[st][0] = acc[st][1] = 0;
-    // (fully unrolled up to 6 steps; beyond that the registers of a second column would spill)
-    constexpr int kUnrollCols = S <= 6 ? kMaxColsPerLane : 1;
-#pragma unroll kUnrollCols
-    for (int t = 0; t < T; ++t) {
-      // A ragged column past the row's end multiplies the row's last column by the zero
-      // activation column: it adds nothing. Rows past the tile's end (a short last tile)
-      // hold stale bytes; their sums are never written.
-      const int c = kl + (t << log2G);
-      const uint32_t w_off = (uint32_t)(min(c, C - 1) * 16);
-      const uint32_t a_off = (uint32_t)((c < C ? c : C) * 16);
-      // all of the column's shared-memory loads first: the S weight vectors, then the
-      // activations
-      uint4 wv[S];
-#pragma unroll
-      for (int st = 0; st < S; ++st) wv[st] = lds128(tile_lane + (uint32_t)(st * step_stride) + w_off);
-      uint4 a[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) a[j] = lds128(xq_u + (uint32_t)(j * plane) + a_off);
-#pragma unroll
-      for (int st = 0; st < S; ++st) {
-        const uint4 w = wv[st];
-        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-        const uint32_t a0[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
-        const uint32_t a1[4] = {a[1].x, a[1].y, a[1].z, a[1].w};
-        const uint32_t a2[4] = {a[2].x, a[2].y, a[2].z, a[2].w};
-        const uint32_t a3[4] = {a[3].x, a[3].y, a[3].z, a[3].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t sh = w4[q] << 2;
-          acc[st][0] = dp4a_us(w4[q] & 0xC0C0C0C0u, a0[q], acc[st][0]);
-          acc[st][0] = dp4a_us(sh & 0xC0C0C0C0u, a1[q], acc[st][0]);
-          acc[st][1] = dp4a_us(w4[q] & 0x0C0C0C0Cu, a2[q], acc[st][1]);
-          acc[st][1] = dp4a_us(sh & 0x0C0C0C0Cu, a3[q], acc[st][1]);
-        }
-      }
-    }
-    int v[8];
-#pragma unroll
-    for (int st = 0; st < 8; ++st) v[st] = st < S ? (acc[st < S ? st : 0][0] >> 6) + (acc[st < S ? st : 0][1] >> 2) : 0;
-    int mine_step = 0;
-    bool writer = kl == 0;
-    if (G >= 8) {
-      const bool up = (kl >> (log2G - 1)) & 1;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int send = up ? v[k] : v[k + 4], keep = up ? v[k + 4] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, G >> 1);
-      }
-      const bool up2 = (kl >> (log2G - 2)) & 1;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int send = up2 ? v[k] : v[k + 2], keep = up2 ? v[k + 2] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, G >> 2);
-      }
-      const bool up3 = (kl >> (log2G - 3)) & 1;
-      {
-        const int send = up3 ? v[0] : v[1], keep = up3 ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, G >> 3);
-      }
-      for (int o = (G >> 4); o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-      mine_step = (up ? 4 : 0) + (up2 ? 2 : 0) + (up3 ? 1 : 0);
-      writer = (kl & ((1 << hb) - 1)) == 0;
-    } else {
-      for (int o = G >> 1; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-    }
-    const int rr = mine_step * rpw + rg;
-    if (writer && mine_step < S && rr < rows) {
-      const int a = v[0] - rs_total;
-      out_row[rr] = __fmul_rn(__fdiv_rn(__int2float_rn(a), s_act), ws);
-      if (acc_row) acc_row[rr] = a;
+    const TileDot r = tile_raw_dots<S>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride);
+    if (r.writer && r.row < rows) {
+      const int a = r.sum - rs_total;
+      out_row[r.row] = __fmul_rn(__fdiv_rn(__int2float_rn(a), s_act), ws);
+      if (acc_row) acc_row[r.row] = a;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);

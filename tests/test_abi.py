@@ -168,6 +168,44 @@ def test_ffn_workspace_size(lib):
     assert lib.bitnet_w2a8_ffn_workspace_size(4096, 2560, 32768 + 128) == -1
 
 
+def _sweep_desc(**kw):
+    d = binding.LinearGroupDesc()
+    d.x, d.K, d.count = kw.get("x", FAKE), kw.get("K", 256), kw.get("count", 1)
+    d.wp[0], d.w_scale[0], d.N[0], d.out[0] = kw.get("wp", FAKE), 1.0, kw.get("N", 4), kw.get("out", FAKE)
+    return d
+
+
+@pytest.mark.parametrize("kw,dtype,status", [
+    (dict(x=None), 0, -1), (dict(count=0), 0, -1), (dict(count=9), 0, -1), (dict(K=192), 0, -1),
+    (dict(K=10240 + 128), 0, -1), (dict(N=0), 0, -1), (dict(wp=None), 0, -1), (dict(out=None), 0, -1),
+    (dict(), 2, -1),
+    (dict(x=FAKE + 8), 0, -2), (dict(wp=FAKE + 4), 0, -2), (dict(out=FAKE + 2), 0, -2),
+])
+def test_sweep_plan_rejects_bad_tables_on_host(lib, kw, dtype, status):
+    descs = (binding.LinearGroupDesc * 2)(_sweep_desc(), _sweep_desc(**kw))
+    handle = ctypes.c_void_p(123)
+    assert lib.bitnet_sweep_plan_create(ctypes.cast(descs, ctypes.c_void_p), 2, dtype, ctypes.byref(handle)) == status
+    assert handle.value is None  # no plan on failure
+
+
+def test_sweep_plan_null_arguments(lib):
+    handle = ctypes.c_void_p()
+    descs = (binding.LinearGroupDesc * 1)(_sweep_desc())
+    assert lib.bitnet_sweep_plan_create(None, 1, 0, ctypes.byref(handle)) == -1
+    assert lib.bitnet_sweep_plan_create(ctypes.cast(descs, ctypes.c_void_p), 0, 0, ctypes.byref(handle)) == -1
+    assert lib.bitnet_sweep_plan_create(ctypes.cast(descs, ctypes.c_void_p), 1, 0, None) == -1
+    assert lib.bitnet_sweep_plan_run(None, None) == -1
+    assert lib.bitnet_sweep_plan_destroy(None) == 0
+
+
+def test_sweep_plan_struct_layout_matches_header():
+    """The ctypes mirror has the C layout: 8-byte x, K, a 4-byte count padded to 8, then the arrays."""
+    D = binding.LinearGroupDesc
+    assert D.x.offset == 0 and D.K.offset == 8 and D.count.offset == 16 and D.wp.offset == 24
+    assert D.w_scale.offset == 24 + 64 and D.N.offset == 24 + 64 + 32 and D.out.offset == 24 + 64 + 32 + 64
+    assert ctypes.sizeof(D) == 24 + 64 + 32 + 64 + 64
+
+
 def test_valid_call_without_gpu_is_unsupported(lib):
     import torch
 

@@ -716,3 +716,78 @@ def test_w2a8_ffn_parity(M, K, F, dtype, use_ws):
     assert_out_close(host(g_out), o["out"])
     assert np.array_equal(host(g_out).view(np.uint32), o["out"].view(np.uint32))
     assert binding.last_device_error() == 0
+
+
+# ----------------------------------------------------------------------------- persistent sweep
+
+SWEEP_CASES = [
+    # (name, dtype, [(K, [N, ...]), ...]) -- mixed K, ragged N, groups split across CTAs and CTAs
+    # spanning many groups, the smallest and largest K
+    ("mixed", "f32", [(2560, [2560, 640, 640]), (2560, [2560]), (2560, [6912, 6912]), (6912, [2560])]),
+    ("ragged", "bf16", [(384, [7]), (128, [1, 3]), (10240, [33]), (1152, [300, 5, 77]), (640, [1000])]),
+    ("many_small", "f32", [(256 * (1 + i % 5), [1 + (37 * i) % 53] * (1 + i % 3)) for i in range(150)]),
+    ("big_rows", "bf16", [(8192, [28672 // 8]), (10240, [1500])]),
+]
+
+
+@pytest.mark.parametrize("name,dtype,spec", SWEEP_CASES, ids=[c[0] for c in SWEEP_CASES])
+def test_sweep_plan_parity(name, dtype, spec):
+    """Every group's outputs, bit for bit, against oracle.quant_act + oracle.ternary_matmul."""
+    groups, expect = [], []
+    for gi, (K, Ns) in enumerate(spec):
+        seed = 600 + 10 * gi
+        x_np = workloads.activations(1, K, seed, dtype)
+        projs, refs = [], []
+        xq, s, _ = oracle.quant_act(x_np, dtype)
+        for li, N in enumerate(Ns):
+            w = workloads.ternary_weights(N, K, seed + 1 + li)
+            ws = workloads.weight_scale(N, K, seed + 5 + li)
+            out = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+            projs.append((binding.pack_i2s(dev(w)), ws, out))
+            o_out, _ = oracle.ternary_matmul(xq, s, oracle.pack_i2s(w)[0], ws, nthreads=NT)
+            refs.append(o_out[0])
+        groups.append((x_device(x_np, dtype).view(-1), projs))
+        expect.append(refs)
+    plan = binding.SweepPlan(groups)
+    plan.run()
+    torch.cuda.synchronize()
+    for (x, projs), refs in zip(groups, expect):
+        for (_, _, out), ref in zip(projs, refs):
+            assert np.array_equal(host(out).view(np.uint32), ref.view(np.uint32))
+    # a second run over changed inputs recomputes everything (the plan binds buffers, not values)
+    for gi, (x, projs) in enumerate(groups):
+        x.copy_(x_device(workloads.activations(1, x.numel(), 900 + gi, dtype), dtype).view(-1))
+    plan.run()
+    torch.cuda.synchronize()
+    for gi, ((x, projs), (K, Ns)) in enumerate(zip(groups, spec)):
+        xq, s, _ = oracle.quant_act(workloads.activations(1, K, 900 + gi, dtype), dtype)
+        for li, (_, ws, out) in enumerate(projs):
+            w = workloads.ternary_weights(Ns[li], K, 600 + 10 * gi + 1 + li)
+            ref, _ = oracle.ternary_matmul(xq, s, oracle.pack_i2s(w)[0], ws, nthreads=NT)
+            assert np.array_equal(host(out).view(np.uint32), ref[0].view(np.uint32))
+    plan.close()
+    assert binding.last_device_error() == 0
+
+
+def test_sweep_plan_matches_group_calls_on_the_decode_layer():
+    """Two 2B-4T layers through the plan equal the per-group calls on the same buffers."""
+    groups, outs_ref = [], []
+    for layer in range(2):
+        for gname, names, K in workloads.LAYER_GROUPS:
+            mats = {n: (N, Kk) for n, N, Kk in workloads.LAYER_MATRICES}
+            x = dev(workloads.activations_f32(1, K, 700 + layer * 10 + len(groups))).view(-1)
+            projs = []
+            for n in names:
+                N = mats[n][0]
+                w = workloads.ternary_weights(N, K, 800 + len(groups) * 7 + len(projs))
+                projs.append((binding.pack_i2s(dev(w)), 0.016, torch.empty(N, dtype=torch.float32, device="cuda")))
+            groups.append((x, projs))
+            ref = binding.linear_group(x.view(1, -1), [p[0] for p in projs], [p[1] for p in projs])
+            outs_ref.append(ref)
+    plan = binding.SweepPlan(groups)
+    plan.run()
+    torch.cuda.synchronize()
+    for (x, projs), ref in zip(groups, outs_ref):
+        for (_, _, out), r in zip(projs, ref):
+            assert torch.equal(out.view(torch.int32), r.view(-1).view(torch.int32))
+    plan.close()
