@@ -1,16 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the W2A8 ternary matmul hot path on GB300.
 
-Default workload (one "step"): the decode pass of a 2B-4T-shaped BitNet b1.58 model at
+Default workload (one "step"): the decode projections of a 2B-4T-shaped BitNet b1.58 model at
 M = 1 -- 30 layers x {q, k, v, o: 2560x2560 / 640x2560, gate, up: 6912x2560, down:
-2560x6912} ternary projections, grouped by shared input; each group's fp32 activation row is
-quantised per token (bitnet_quant_act) and every projection runs the i2_s GEMV
-(bitnet_i2s_matmul) -- fused into one bitnet_w2a8_linear_group launch per group. 521 MB of
-packed weights per step stay resident in HBM; the step is one CUDA graph. The metric is algorithmic bytes moved per second (GB/s, 2 bits per weight).
+2560x6912} ternary projections, grouped by shared input. Each group's given fp32 activation
+row is quantised per token and every projection of the group runs the i2_s GEMV, for all 120
+groups in one persistent launch (bitnet_sweep_plan_run). 521 MB of packed weights per step stay
+resident in HBM; the step is one CUDA graph. The metric is algorithmic bytes moved per second
+(GB/s, 2 bits per weight).
 
-Also measured in the same run and reported alongside: the prefill GEMM (M=4096, K=6912,
-N=2560, bf16 activations) in TOPS, the end-to-end figure through host buffers (e2e), the
-roofline fraction of the dominant kernel, and the CPU oracle on a bounded sample.
+Also measured in the same run and reported alongside:
+  * decode_chain: the same sweep as a dependent chain, one fused launch per group, each
+    waiting for the previous one;
+  * prefill: the prefill GEMM (M=4096, K=6912, N=2560, bf16 activations) in TOPS;
+  * gemv_100b: the 100B-class GEMV;
+  * ffn: the fused FFN block;
+  * e2e: the end-to-end figure through host buffers;
+  * roofline: the roofline fraction of the dominant kernel;
+  * cpu_baseline: the CPU oracle on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -218,14 +225,39 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_sha(kernel_file):
+    """sha256 prefix over a kernel source and every local header it includes (transitively),
+    so that a traffic record goes stale when any code the kernel is built from changes."""
+    dirs = [os.path.join(ROOT, "ternary_weight_gb300", "csrc"), os.path.join(ROOT, "include")]
+    seen, h = set(), hashlib.sha256()
+
+    def visit(name):
+        if name in seen:
+            return
+        seen.add(name)
+        path = next((os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name))), None)
+        if path is None:
+            return
+        data = open(path, "rb").read()
+        h.update(data)
+        for line in data.decode("utf-8", "replace").splitlines():
+            line = line.strip()
+            if line.startswith("#include") and '"' in line:
+                visit(line.split('"')[1])
+
+    visit(kernel_file)
+    return h.hexdigest()[:16] if seen and any(
+        os.path.exists(os.path.join(d, kernel_file)) for d in dirs) else None
+
+
 def recorded_traffic(kernel_file):
     """DRAM bytes per launch of a kernel from a committed ncu summary, valid only while the
-    kernel source is unchanged (profiles/traffic.txt: file sha16 bytes_per_launch workload)."""
+    kernel source and the headers it includes are unchanged (profiles/traffic.txt: file,
+    source sha16, bytes_per_launch, workload)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    src = os.path.join(ROOT, "ternary_weight_gb300", "csrc", kernel_file)
-    if not (os.path.exists(path) and os.path.exists(src)):
+    sha = kernel_source_sha(kernel_file)
+    if sha is None or not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -491,6 +523,64 @@ def run_kernel_workload(args):
 
 # ------------------------------------------------------------------------------ main arm
 
+def sweep_plan_of(stack):
+    """One persistent-sweep plan over every group of the stack, bound to its buffers."""
+    from ternary_weight_gb300 import binding
+
+    groups = []
+    for gi, g in enumerate(stack.groups):
+        groups.append((stack.x[gi].view(-1),
+                       [(l.wp, l.w_scale, stack.out[gi][li].view(-1)) for li, l in enumerate(g.linears)]))
+    return binding.SweepPlan(groups)
+
+
+def sweep_bytes(stack):
+    """Algorithmic bytes of one sweep step: packed weights, the fp32 input rows, fp32 outputs."""
+    return (sum(l.weight_bytes() for g in stack.groups for l in g.linears) + stack.act_bytes_in
+            + stack.out_elems * 4)
+
+
+def capture(fn, device):
+    import torch
+
+    s = torch.cuda.Stream(device=device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def chain_leg(stack, device, peaks, steps):
+    """The same sweep run as a decode chain: one fused quantisation + GEMV launch per group,
+    each waiting for the previous one (programmatic dependent launch), as the layers of a real
+    decode step must. Latency-bound: see the chain note in the design notes."""
+    import torch
+
+    graph = stack.capture()
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    t = time_replays(graph, steps, stream) / steps
+    n_launch = stack.launches_per_step()
+    byts = stack.bytes_per_step()
+    gbs = byts / t / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"workload": "the same 30-layer sweep as a dependent chain: %d fused group launches per step, each "
+                        "waiting for the previous (programmatic dependent launch)" % n_launch,
+            "value": gbs, "unit": "GB/s", "ms_per_step": t * 1e3, "launches_per_step": n_launch,
+            "us_per_group": t / n_launch * 1e6,
+            "roofline": {"bound": "latency (dependent hops)", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": recorded_traffic("gemv_group.cu"),
+                         "kernel": "gemv_group_kernel, avg over the step's %d launches; algorithmic bytes per "
+                                   "launch %.0f" % (n_launch, byts / n_launch)}}
+
+
 def run_ours(args):
     import torch
 
@@ -509,14 +599,15 @@ def run_ours(args):
 
     peaks, peak_kind = measured_peaks()
     stack, x_host = build_stack(args.layers, device)
-    graph = stack.capture()
+    plan = sweep_plan_of(stack)
     stream = torch.cuda.current_stream(device)
+    graph = capture(lambda: plan.run(), device)
 
     for _ in range(max(3, args.warmup)):
         graph.replay()
     torch.cuda.synchronize(device)
 
-    # ---- timed region: K graph replays of the whole step ----
+    # ---- timed region: K graph replays of the whole step (one persistent launch each) ----
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
@@ -528,22 +619,20 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.stop()
 
-    bytes_step = stack.bytes_per_step()
+    bytes_step = sweep_bytes(stack)
     per_rank = allgather_floats(dist, world, [t_step, float(bytes_step * args.steps)], device)
     value_bps, t_max = aggregate([r[0] for r in per_rank], [r[1] for r in per_rank])
     ms_per_step = t_max / args.steps * 1e3
 
-    # ---- dominant kernel: every launch of the fused step is the single-token fused
-    # quantisation + GEMV kernel, so its average launch duration is the timed step over its
-    # launches (CUDA events on the launching stream, back-to-back launches in one graph) ----
-    n_launch = stack.launches_per_step()
-    achieved = (bytes_step / n_launch) / (t_step / args.steps / n_launch) / 1e9
+    # ---- dominant kernel: the step is one launch of the persistent sweep kernel, so its
+    # average launch duration is the timed step (CUDA events on the launching stream) ----
+    achieved = bytes_step / (t_step / args.steps) / 1e9
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": recorded_traffic("gemv_group.cu"),
+                "traffic": recorded_traffic("gemv_sweep.cu"),
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                "kernel": "gemv_group_kernel (fused quantisation + grouped GEMV), avg over the step's "
-                          "%d launches; algorithmic bytes per launch %.0f" % (n_launch, bytes_step / n_launch)}
+                "kernel": "gemv_sweep_kernel (per-group quantisation + every projection of every group, one "
+                          "persistent launch); algorithmic bytes per launch %.0f" % bytes_step}
 
     # ---- e2e: pinned host activations in, every projection's output back, each step ----
     x_pin = x_host.pin_memory()
@@ -567,35 +656,39 @@ def run_ours(args):
     per_rank_e2e = allgather_floats(dist, world, [t_e2e, float(bytes_step * e2e_steps)], device)
     e2e_bps, _ = aggregate([r[0] for r in per_rank_e2e], [r[1] for r in per_rank_e2e])
 
+    chain = chain_leg(stack, device, peaks, max(10, args.steps // 4))
     prefill = None if args.no_prefill else kernel_leg("prefill", device, peaks)
     gemv_100b = None if args.no_gemv_leg else kernel_leg("gemv_100b", device, peaks)
     ffn = None if args.no_ffn_leg else ffn_leg(stack, device, peaks)
+    plan.close()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, desc, nt, _, _ = oracle_sample(args.cpu_seconds, args.layers)
         cpu = {"value": gbs, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": desc}
 
+    packed = sum(l.weight_bytes() for g in stack.groups for l in g.linears)
     line = {
         "metric": METRIC, "value": value_bps / 1e9, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "i8xi2->i32", "data": "synthetic (seeded numpy PCG64; see workloads.py)",
         "config": {
-            "workload": "decode sweep of a 2B-4T-shaped model: %d layers x {q,k,v,o,gate,up,down}, M=1, fp32 "
-                        "activations quantised per token to int8" % args.layers,
-            "layers": args.layers, "M": 1, "bytes_per_step": bytes_step,
-            "packed_weight_bytes_per_step": sum(l.weight_bytes() for g in stack.groups for l in g.linears),
-            "l2": "inputs larger than L2: %.0f MB of packed weights streamed per step (L2 is 129 MB)"
-                  % (sum(l.weight_bytes() for g in stack.groups for l in g.linears) / 1e6),
-            "graph": "one CUDA graph per step: %d launches" % stack.launches_per_step(),
+            "workload": "decode sweep of a 2B-4T-shaped model: %d layers x {q,k,v,o,gate,up,down}, M=1, a given "
+                        "fp32 activation row per projection group, quantised per token to int8; the groups are "
+                        "independent (one persistent launch per step; the dependent-chain form is the "
+                        "decode_chain leg)" % args.layers,
+            "layers": args.layers, "M": 1, "bytes_per_step": bytes_step, "packed_weight_bytes_per_step": packed,
+            "l2": "inputs larger than L2: %.0f MB of packed weights streamed per step (L2 is 129 MB)" % (packed / 1e6),
+            "graph": "one CUDA graph per step: 1 launch (bitnet_sweep_plan_run)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
-        "gpu_launches": stack.launches_per_step() * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clocks,
         "roofline": roofline,
         "e2e": {"value": e2e_bps / 1e9, "unit": UNIT, "h2d_bytes_per_step": stack.act_bytes_in,
                 "d2h_bytes_per_step": stack.out_elems * 4,
                 "note": "pinned host activations -> device, graph step, all projection outputs -> host, each step"},
+        "decode_chain": chain,
         "prefill": prefill,
         "gemv_100b": gemv_100b,
         "ffn": ffn,

@@ -87,3 +87,22 @@ def test_reference_arm_other_ranks_exit_quietly():
 
 def test_traffic_record_requires_unchanged_kernel(tmp_path, monkeypatch):
     assert bench.recorded_traffic("no_such_kernel.cu") is None
+
+
+def test_kernel_source_sha_covers_included_headers(tmp_path, monkeypatch):
+    """A change to a header the kernel includes makes its traffic record stale."""
+    csrc = tmp_path / "ternary_weight_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "include").mkdir()
+    (csrc / "k.cu").write_text('#include "h.cuh"\nint k;\n')
+    (csrc / "h.cuh").write_text("int h;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    a = bench.kernel_source_sha("k.cu")
+    (csrc / "h.cuh").write_text("int h2;\n")
+    b = bench.kernel_source_sha("k.cu")
+    assert a and b and a != b
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.txt").write_text("k.cu %s 123 test\n" % b)
+    assert bench.recorded_traffic("k.cu") == 123.0
+    (csrc / "k.cu").write_text('#include "h.cuh"\nint k2;\n')
+    assert bench.recorded_traffic("k.cu") is None
