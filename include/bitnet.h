@@ -328,7 +328,7 @@ BITNET_API int bitnet_w2a8_ffn(const void *x, int dtype, int64_t M, int64_t K, i
  *   same run. This is the set of projections of a decode step whose input rows are given,
  *   streamed at HBM rate. A chain of dependent layers is the per-group call, launch by launch.
  *   One CTA per SM streams a contiguous slice of all groups' packed weights through a
- *   192 KB shared-memory ring.
+ *   216 KB shared-memory ring.
  * bitnet_sweep_plan_create validates the table and copies it to the current device (host,
  * synchronous; allocates the plan's device table). Pointers inside are bound to the plan.
  * bitnet_sweep_plan_run launches it on `stream` (no allocation; may be captured into a CUDA

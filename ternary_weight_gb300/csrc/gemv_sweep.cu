@@ -14,9 +14,9 @@
 //  * CTA b owns a contiguous slice of the concatenated rows of every projection of every group
 //    (in table order), balanced by packed bytes rather than rows (rows of different K differ
 //    in size: 640 bytes at K = 2560, 1728 at 6912). The slice is cut into tiles of whole rows
-//    (<= 12 KB, never across two projections).
+//    (<= 13.5 KB, never across two projections).
 //  * Warp 16 is the producer: one lane issues cp.async.bulk copies of consecutive tiles into a
-//    16-slot x 12 KB shared-memory ring (192 KB, about 29 MB in flight over the GPU), each
+//    16-slot x 13.5 KB shared-memory ring (216 KB, about 33 MB in flight over the GPU), each
 //    slot completing on its own mbarrier by transaction bytes. It runs ahead across group
 //    boundaries, bounded only by the ring.
 //  * Warps 0-15 are consumers; tile i goes to warp i % 16 (one waiter per slot, in order).
@@ -38,13 +38,21 @@ constexpr int kSwConsumerWarps = 16;
 constexpr int kSwConsumers = kSwConsumerWarps * 32;
 constexpr int kSwThreads = kSwConsumers + 32;
 constexpr int kSwSlots = 16;
-constexpr int kSwSlotBytes = 12288;
+// 13.5 KB slots: a tile of K = 6912 rows holds 8 steps (13.8 KB), one of K = 2560 rows 5 steps
+// of 4 rows (12.8 KB); the ring and the largest activation planes just fit the 227 KB a CTA
+// may use. Fewer, larger tiles cut the per-tile overhead (wait, reduce, epilogue, release):
+// on the 2B-4T sweep 91 us against 102 us with 12 KB slots and at most 6 steps.
+constexpr int kSwSlotBytes = 13824;
 constexpr int kSwRingBytes = kSwSlots * kSwSlotBytes;
 constexpr int kSwMaxK = 10240;
-constexpr int kSwMaxS = 6;  // steps per tile (the tile routine's column loop unrolls up to 6)
+constexpr int kSwMaxS = 8;        // steps per tile, at most (the tile routine takes up to 8)
+constexpr int kSwUnrollMaxS = 6;  // the column loop is unrolled for tiles of up to this many steps
+static_assert(kSwMaxS >= 1 && kSwMaxS <= 8, "steps per tile");
 constexpr int kSwMaxVec = kSwMaxK / 4 / kSwConsumers;  // fp32 16-byte vectors per thread
 static_assert(kSwSlots % kSwConsumerWarps == 0, "each ring slot must belong to one consumer warp");
 static_assert(kSwMaxK / 64 <= 32 * kMaxColsPerLane, "column loop bound");
+// (the static shared memory, barriers and slot tables, is 640 bytes)
+static_assert(kSwRingBytes + kSwMaxK + 64 + 768 <= 227 * 1024, "ring + planes + static shared memory");
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -66,7 +74,8 @@ __device__ __forceinline__ int group_tiles(const SweepGroup& G, int begin, int e
 template <int S>
 __device__ __forceinline__ TileDot sweep_tile(uint32_t tile_lane, uint32_t xq_u, int plane, int C, int T, int kl,
                                               int log2G, int rg, int rpw, int step_stride) {
-  return tile_raw_dots<S>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride);
+  constexpr int kUnroll = S <= kSwUnrollMaxS ? kMaxColsPerLane : 1;
+  return tile_raw_dots<S, kUnroll>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride);
 }
 
 template <bool BF16>
@@ -254,7 +263,9 @@ __global__ void __launch_bounds__(kSwThreads, 1) gemv_sweep_kernel(const SweepGr
         case 3: r = sweep_tile<3>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride); break;
         case 4: r = sweep_tile<4>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride); break;
         case 5: r = sweep_tile<5>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride); break;
-        default: r = sweep_tile<6>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride); break;
+        case 6: r = sweep_tile<6>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride); break;
+        case 7: r = sweep_tile<(kSwMaxS >= 7 ? 7 : 1)>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride); break;
+        default: r = sweep_tile<(kSwMaxS >= 8 ? 8 : 1)>(tile_lane, xq_u, plane, C, T, kl, log2G, rg, rpw, step_stride); break;
       }
       if (r.writer && r.row < rows) {
         const int a = r.sum - rs_total;

@@ -49,9 +49,12 @@ struct TileDot {
 // lane-in-group bits spell st, so the epilogue runs for up to 8 rows in parallel.
 //   tile_lane : shared address of this lane's row of step 0 (step st is st * step_stride on)
 //   xq_u      : shared address of activation plane 0; plane j is j * plane bytes on
-template <int S>
+// UNROLL: how many chunk columns the column loop unrolls (by default all 5 up to 6 steps;
+// beyond that the registers of a second column would spill in the group kernel).
+template <int S, int UNROLL = (S <= 6 ? kMaxColsPerLane : 1)>
 __device__ __forceinline__ TileDot tile_raw_dots(uint32_t tile_lane, uint32_t xq_u, int plane, int C, int T, int kl,
                                                  int log2G, int rg, int rpw, int step_stride) {
+  static_assert(S >= 1 && S <= 8, "one partial register per step, at most 8");
   const int G = 1 << log2G;
   // per step: hi = 64 * (sum of bit pairs 0 and 1), lo = 4 * (sum of bit pairs 2 and 3);
   // shifting the weight word left by 2 puts pair 1 under pair 0's mask and pair 3 under
@@ -59,9 +62,7 @@ __device__ __forceinline__ TileDot tile_raw_dots(uint32_t tile_lane, uint32_t xq
   int acc[S][2];
 #pragma unroll
   for (int st = 0; st < S; ++st) acc[st][0] = acc[st][1] = 0;
-  // (fully unrolled up to 6 steps; beyond that the registers of a second column would spill)
-  constexpr int kUnrollCols = S <= 6 ? kMaxColsPerLane : 1;
-#pragma unroll kUnrollCols
+#pragma unroll UNROLL
   for (int t = 0; t < T; ++t) {
     const int c = kl + (t << log2G);
     const uint32_t w_off = (uint32_t)(min(c, C - 1) * 16);
