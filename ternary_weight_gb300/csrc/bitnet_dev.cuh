@@ -74,6 +74,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool* 
   return false;
 }
 
+// mbar_wait by every lane of a warp, with the outcome made warp-uniform: a warp never splits at
+// a timeout before warp-collective code (shuffles, tcgen05.ld). All 32 lanes must call it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, bool* abort) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+  if (!ok) *abort = true;
+  return ok;
+}
+
 // One arrival that also announces tx_bytes of asynchronous (bulk copy) data for the phase.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx_bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_i2s_tc_kernel(const int8_t* _
     }
 
     // ===================== epilogue: TMEM -> registers -> correction, scale -> global ===========
-    const bool have = mbar_wait(&accum_bar, 0, &abort);
+    const bool have = mbar_wait_warp(&accum_bar, 0, &abort);
     tc_fence_after();
     if (have) {
       const int q = warp & 3;             // TMEM lane quarter this warp may access

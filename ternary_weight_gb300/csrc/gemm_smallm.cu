@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       const int si = kbl / KB_ST, q = kbl % KB_ST;  // staging stage and k-block within it
       const int s = si % ST_STAGES, us = si / ST_STAGES;
       const int a = kbl % AB_STAGES, ua = kbl / AB_STAGES;
-      if (q == 0 && !mbar_wait(&st_full[s], us & 1, &abort)) break;
-      if (ua > 0 && !mbar_wait(&ab_empty[a], (ua - 1) & 1, &abort)) break;
+      if (q == 0 && !mbar_wait_warp(&st_full[s], us & 1, &abort)) break;
+      if (ua > 0 && !mbar_wait_warp(&ab_empty[a], (ua - 1) & 1, &abort)) break;
       const uint8_t* st = st_ring + s * Cfg::ST_BYTES;
       uint8_t* at = ab_ring + a * Cfg::AB_BYTES;
       uint8_t* bt = at + A_TILE;
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
     }
 
     // ---- push this CTA's partial sums to the rows' owners in the cluster (8 warps) ----
-    if (warp < XP_WARP0 + 8 && mbar_wait(&done_bar, 0, &abort)) {
+    if (warp < XP_WARP0 + 8 && mbar_wait_warp(&done_bar, 0, &abort)) {
       tc_fence_after();
       const int e = warp - XP_WARP0;         // 0..7 (the first 8 expander warps)
       const int quarter = warp & 3;          // tensor-memory lanes this warp may read

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_f16_ws_kernel(const __grid_co
     int lt = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
       const int acc = lt & 1, ua = lt >> 1;
-      if (!mbar_wait(&tfull_bar[acc], ua & 1, &abort)) break;
+      if (!mbar_wait_warp(&tfull_bar[acc], ua & 1, &abort)) break;
       tc_fence_after();
       const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
       const int mrow = m0 + q * 32 + lane;  // this lane's accumulator row

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
       prefetch_l2(xv, (uint32_t)K * (BF16 ? 2u : 4u));
     }
   }
-  if (warp < n_tiles) mbar_wait(&full_bar[warp], 0, &abort);  // tile `warp`: slot warp, use 0
+  if (warp < n_tiles) mbar_wait_warp(&full_bar[warp], 0, &abort);  // tile `warp`: slot warp, use 0
   float s_act;
   int rs_total;
   pdl_wait();  // the activations may be the previous kernel's output
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
   for (int i = warp; i < n_tiles; i += kConsumerWarps) {
     const int slot = i % kSlots, use = i / kSlots;
     if (i != warp) {
-      if (!mbar_wait(&full_bar[slot], use & 1, &abort)) break;
+      if (!mbar_wait_warp(&full_bar[slot], use & 1, &abort)) break;
     } else if (abort) {
       break;
     }

@@ -247,11 +247,7 @@ __global__ void __launch_bounds__(kSwThreads, 1) gemv_sweep_kernel(const SweepGr
     const int first = tile_base + ((warp - tile_base) % kSwConsumerWarps + kSwConsumerWarps) % kSwConsumerWarps;
     for (int i = first; i < tile_base + n_tiles; i += kSwConsumerWarps) {
       const int slot = i % kSwSlots, use = i / kSwSlots;
-      // the wait's outcome is made warp-uniform so that the whole warp leaves together
-      if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[slot], use & 1, &abort))) {
-        abort = true;
-        break;
-      }
+      if (!mbar_wait_warp(&full_bar[slot], use & 1, &abort)) break;
       const int rows = slot_rows[slot];
       float* const out_row = slot_out[slot];
       const float ws = slot_ws[slot];
