@@ -367,8 +367,10 @@ cudaError_t launch_mp(const int8_t* xq, const float* act_scale, const int32_t* r
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   // K split across a cluster so that all CTAs run at once, one per SM (the shared memory allows
-  // one): at most 8 CTAs per cluster, at least four 64-k blocks each. A CTA more than the SMs
-  // would run as a second wave and double the time.
+  // one): at most 8 CTAs per cluster, at least four 64-k blocks each. A cluster that cannot be
+  // resident with the others runs as a second wave and doubles the time. A cluster must fit in
+  // one GPC, so SMs / tiles overestimates the size that fits: with 20 tiles, 7-CTA clusters pack
+  // only two per GPC. The occupancy query decides, shrinking the cluster until every one fits.
   const int64_t n_tiles = (N + TW - 1) / TW;
   const int64_t nkb = K / KB;
   int64_t cs = num_sms / n_tiles;
@@ -376,17 +378,27 @@ cudaError_t launch_mp(const int8_t* xq, const float* act_scale, const int32_t* r
   if (cs > nkb / 4) cs = nkb / 4;
   if (cs < 1) cs = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = (unsigned)cs;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  for (; cs > 1; --cs) {
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_smallm_kernel<MP>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();  // the query is only a hint: keep the size from the SM count
+      break;
+    }
+    if (clusters >= n_tiles) break;
+  }
+  attr[0].val.clusterDim.y = (unsigned)cs;
+  cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs);
   return cudaLaunchKernelEx(&cfg, gemm_smallm_kernel<MP>, xq, act_scale, rowsum, wp, w_scale, out, acc_out, (int)M,
                             (int)N, (int)K);
 }
