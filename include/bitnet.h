@@ -68,7 +68,8 @@ extern "C" {
 #define BITNET_QW_SIGN 1    /* q = 0 where |w| < 1e-6, else sign(w); scale = max|w|       */
 
 /* ---- matmul kernel selection (bitnet_i2s_matmul_algo) ---- */
-#define BITNET_ALGO_AUTO 0   /* GEMV M <= 16, few-token kernel M <= 64, GEMM beyond */
+#define BITNET_ALGO_AUTO 0   /* GEMV for a few rows (M < 9 when K >= 4096, else M < 12),
+                                the few-token kernel up to M = 64, GEMM beyond         */
 #define BITNET_ALGO_GEMV 1   /* force the dp4a decode GEMV (any M)                   */
 #define BITNET_ALGO_GEMM 2   /* force the tcgen05 tensor-core GEMM (any M)           */
 #define BITNET_ALGO_SMALLM 3 /* force the few-token tensor-core kernel (M <= 64)     */
@@ -130,8 +131,9 @@ BITNET_API int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, 
  *   xq and wp must be 16-byte aligned; out and acc_out 4-byte aligned.
  *   The 2-bit field value 3 never comes out of bitnet_pack_i2s; if present it is used
  *   arithmetically (3 - 1 = +2), the same rule as the unpacking of [DeepDive] §8.
- *   Kernel choice: for M <= 16 a dp4a GEMV streams the packed weights. For 17 <= M <= 64
- *   a few-token tcgen05 kernel decodes each weight once into fp16 for all token rows
+ *   Kernel choice: for a few rows (M < 9 when K >= 4096, M < 12 otherwise) a dp4a GEMV
+ *   streams the packed weights. From there up to M = 64 a few-token tcgen05 kernel decodes
+ *   each weight once into fp16 for all token rows
  *   (weights as the MMA's M, K split over a thread-block cluster). For larger M a tcgen05
  *   tile GEMM expands the codes in shared memory. The tensor-core paths are exact: every
  *   partial sum is an integer below 2^24 accumulated in fp32. All give bit-identical

@@ -20,7 +20,13 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxK = 1 << 16;          // staged activation rows must fit shared memory
 constexpr int64_t kMaxKTensorCore = 1 << 15; // exact fp32 accumulation bound of the GEMM
 constexpr int64_t kGemvMaxM = 64;           // auto dispatch: GEMV or few-token kernel up to here, GEMM above
-constexpr int64_t kSmallmMinM = 17;         // auto dispatch: the few-token tensor-core kernel from here
+// auto dispatch: the few-token tensor-core kernel from this many rows on. The dp4a GEMV's cost
+// grows with the rows (every weight word is decoded once per row); the tensor-core kernel's
+// barely does. Measured crossovers on the 2B-4T shapes: K = 6912 (N 2560) ties at 8 rows and
+// the tensor-core kernel wins from 9 (16 rows: 16.2 against 24.2 us); K = 2560 (N 6912) the
+// GEMV wins up to 8 (9.9 against 15.4 us) and loses from 12 (17.4 against 15.6 us).
+constexpr int64_t kSmallmMinMLongK = 9;      // K >= 4096
+constexpr int64_t kSmallmMinM = 12;          // shorter rows
 
 // per-device: 0 = unchecked, 1 = sm_103 ok, -1 = unsupported; and SM count
 std::atomic<int> g_dev_state[kMaxDevices];
@@ -121,10 +127,11 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
       (acc_out && !aligned(acc_out, 4)))
     return BITNET_EALIGN;
   if (algo == BITNET_ALGO_AUTO) {
-    // dp4a GEMV up to 16 tokens (it decodes each weight word once per token row, cheap while
-    // the rows are few); the few-token tensor-core kernel from 17 to 64 (each weight decoded
-    // once for all rows); the tile GEMM beyond
-    if (K > kMaxKTensorCore || M <= kSmallmMinM - 1)
+    // dp4a GEMV for a few tokens (it decodes each weight word once per token row, cheap while
+    // the rows are few); the few-token tensor-core kernel from 9 or 12 rows to 64 (each weight
+    // decoded once for all rows); the tile GEMM beyond
+    const int64_t smallm_from = K >= 4096 ? kSmallmMinMLongK : kSmallmMinM;
+    if (K > kMaxKTensorCore || M < smallm_from)
       algo = BITNET_ALGO_GEMV;
     else if (M <= kGemvMaxM)
       algo = BITNET_ALGO_SMALLM;

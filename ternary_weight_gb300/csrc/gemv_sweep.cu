@@ -96,11 +96,9 @@ __global__ void __launch_bounds__(kSwThreads, 1) gemv_sweep_kernel(const SweepGr
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const SweepSlice slice = slices[blockIdx.x];
   const int begin = slice.begin, end = slice.end, g0 = slice.g0;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kSwSlots; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
-    }
+  if (threadIdx.x < kSwSlots) {  // one barrier pair per thread
+    mbar_init(&full_bar[threadIdx.x], 1);
+    mbar_init(&empty_bar[threadIdx.x], 1);
     fence_mbar_init();
   }
   // (an empty slice, begin == end, touches no group: every loop below stops at row0 >= end or

@@ -791,3 +791,33 @@ def test_sweep_plan_matches_group_calls_on_the_decode_layer():
         for (_, _, out), r in zip(projs, ref):
             assert torch.equal(out.view(torch.int32), r.view(-1).view(torch.int32))
     plan.close()
+
+
+# ----------------------------------------------------------------------------- few token rows
+
+ROWS_CASES = [
+    # (M, N, K) through auto dispatch: both sides of the GEMV / few-token crossover (8-9 rows at
+    # long K, 11-12 at short), the 2B-4T shapes, a ragged 32-lane layout (K 6912), the 2-lane
+    # layout (K 384), the largest K of the GEMV's staged path, and fewer rows than SMs
+    (2, 6912, 2560), (3, 2560, 6912), (4, 640, 2560), (5, 7, 384), (8, 2560, 6912), (9, 2560, 6912),
+    (11, 6912, 2560), (12, 6912, 2560), (16, 2560, 6912), (16, 300, 10240), (13, 1000, 1152),
+    (2, 152, 128), (16, 1, 256),
+]
+
+
+@pytest.mark.parametrize("M,N,K", ROWS_CASES)
+def test_few_rows_parity(M, N, K):
+    """A few token rows through auto dispatch (dp4a GEMV or the few-token tensor-core kernel):
+    int32 accumulators and fp32 outputs bit for bit, on random packed bytes (code 3 included)
+    and full-range int8 rows."""
+    wp_np = workloads.random_packed_bytes(N, K, 900 + M + N)
+    xq_np = workloads.random_int8(M, K, 901 + K)
+    s_np = (np.random.default_rng(902).uniform(0.5, 60.0, M)).astype(np.float32)
+    rs_np = xq_np.astype(np.int64).sum(axis=1).astype(np.int32)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    out = binding.i2s_matmul(dev(xq_np), dev(s_np), dev(rs_np), dev(wp_np), 0.0173, acc_out=acc)
+    torch.cuda.synchronize()
+    o_out, o_acc = oracle.ternary_matmul(xq_np, s_np, wp_np, 0.0173, nthreads=NT)
+    assert np.array_equal(host(acc), o_acc)
+    assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32))
+    assert binding.last_device_error() == 0
