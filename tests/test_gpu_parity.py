@@ -821,3 +821,99 @@ def test_few_rows_parity(M, N, K):
     assert np.array_equal(host(acc), o_acc)
     assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32))
     assert binding.last_device_error() == 0
+
+
+# ----------------------------------------------------------------------------- seeded random cases
+
+def _rand_k(rng, hi=10240):
+    return int(rng.integers(1, hi // 128 + 1)) * 128
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_random_matmul_shapes(case):
+    """Seeded random (M, N, K) through auto dispatch, every kernel the dispatcher can pick, with
+    random packed bytes (code 3 included) and full-range int8 rows: bit for bit."""
+    rng = np.random.default_rng(7000 + case)
+    M = int(rng.choice([1, 2, 3, 5, 8, 9, 12, 15, 17, 31, 48, 64, 65, 100, 129, 200]))
+    N = int(rng.integers(1, 3000))
+    K = _rand_k(rng, 6912 if M > 64 else 10240)
+    wp_np = workloads.random_packed_bytes(N, K, 7100 + case)
+    xq_np = workloads.random_int8(M, K, 7200 + case)
+    s_np = rng.uniform(0.1, 100.0, M).astype(np.float32)
+    rs_np = xq_np.astype(np.int64).sum(axis=1).astype(np.int32)
+    ws = float(rng.uniform(0.001, 0.1))
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    out = binding.i2s_matmul(dev(xq_np), dev(s_np), dev(rs_np), dev(wp_np), ws, acc_out=acc)
+    torch.cuda.synchronize()
+    o_out, o_acc = oracle.ternary_matmul(xq_np, s_np, wp_np, ws, nthreads=NT)
+    assert np.array_equal(host(acc), o_acc), (M, N, K)
+    assert np.array_equal(host(out).view(np.uint32), o_out.view(np.uint32)), (M, N, K)
+    assert binding.last_device_error() == 0
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_random_sweep_plans(case):
+    """Seeded random sweep plans (group count, K, projections and rows per group, dtype)."""
+    rng = np.random.default_rng(7300 + case)
+    dtype = "bf16" if case % 2 else "f32"
+    groups, refs = [], []
+    for gi in range(int(rng.integers(1, 12))):
+        K = _rand_k(rng)
+        x_np = workloads.activations(1, K, 7400 + 10 * case + gi, dtype, outlier_p=0.01)
+        xq, s, _ = oracle.quant_act(x_np, dtype)
+        projs = []
+        for li in range(int(rng.integers(1, 9))):
+            N = int(rng.integers(1, 1500))
+            wp_np = workloads.random_packed_bytes(N, K, 7500 + 100 * case + 10 * gi + li)
+            ws = float(rng.uniform(0.001, 0.1))
+            projs.append((dev(wp_np), ws, torch.empty(N, dtype=torch.float32, device="cuda")))
+            refs.append(oracle.ternary_matmul(xq, s, wp_np, ws, nthreads=NT)[0][0])
+        groups.append((x_device(x_np, dtype).view(-1), projs))
+    plan = binding.SweepPlan(groups)
+    plan.run()
+    torch.cuda.synchronize()
+    outs = [p[2] for _, projs in groups for p in projs]
+    plan.close()
+    for got, ref in zip(outs, refs):
+        assert np.array_equal(host(got).view(np.uint32), ref.view(np.uint32))
+    assert binding.last_device_error() == 0
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_random_ffn_blocks(case):
+    """Seeded random FFN blocks (M, K, F, dtype, workspace) against the oracle chain."""
+    rng = np.random.default_rng(7600 + case)
+    M = int(rng.choice([1, 1, 2, 7, 20, 70]))
+    K = _rand_k(rng, 4096)
+    F = _rand_k(rng, 8192)
+    dtype = "bf16" if case % 2 else "f32"
+    x_np = workloads.activations(M, K, 7700 + case, dtype)
+    wg, wu = workloads.ternary_weights(F, K, 7710 + case), workloads.ternary_weights(F, K, 7720 + case)
+    wd = workloads.ternary_weights(K, F, 7730 + case)
+    ag, au, ad = (float(v) for v in rng.uniform(0.005, 0.05, 3))
+    gamma = workloads.rmsnorm_gamma(F, 7740 + case)
+    use_ws = M > 64 and bool(case % 3)
+    ws = (torch.empty(binding.ffn_workspace_size(M, K, F), dtype=torch.uint8, device="cuda") if use_ws else None)
+    g_out = binding.w2a8_ffn(x_device(x_np, dtype), binding.pack_i2s(dev(wg)), ag, binding.pack_i2s(dev(wu)), au,
+                             binding.pack_i2s(dev(wd)), ad, dev(gamma), 1e-5, workspace=ws)
+    torch.cuda.synchronize()
+    o = _ffn_oracle(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, 1e-5)
+    assert np.array_equal(host(g_out).view(np.uint32), o["out"].view(np.uint32)), (M, K, F)
+    assert binding.last_device_error() == 0
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_random_weight_ternarisation(case):
+    """Seeded random (N, K, dtype, mode, spread) for bitnet_quant_weight."""
+    rng = np.random.default_rng(7800 + case)
+    N, K = int(rng.integers(1, 700)), _rand_k(rng)
+    dtype, mode = ("bf16" if case % 2 else "f32"), ("sign" if case % 3 == 2 else "absmean")
+    w = (workloads.near_ternary_weights_f32(N, K, 7900 + case) if mode == "sign"
+         else workloads.source_weights_f32(N, K, 7900 + case, std=float(rng.uniform(0.001, 3.0))))
+    w_dev = w if dtype == "f32" else workloads.to_bf16_bits(w)
+    g_wp, g_s = binding.quant_weight(x_device(w_dev, dtype), mode=mode)
+    torch.cuda.synchronize()
+    o_q, o_s = oracle.quant_weight(w_dev, dtype=dtype, mode=mode)
+    assert np.array_equal(host(g_s).view(np.uint32), np.array([o_s], dtype=np.float32).view(np.uint32))
+    assert np.array_equal(host(g_wp), oracle.pack_i2s(o_q)[0])
+    assert binding.last_device_error() == 0
