@@ -296,24 +296,30 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       const uint32_t dst_c = cs > 1 ? map_to_rank(dst, (uint32_t)owner) : dst;
       const int c_lo = (e >> 2) * (MP / 2);  // two warps share a lane quarter: half the columns each
       const int used = nkb * (KB / 16) < Cfg::NACC ? nkb * (KB / 16) : Cfg::NACC;  // accumulators written
+      // per accumulator, every 8-column piece of this warp's half is loaded before one wait
+      // (a wait after each piece serialised 32 round trips per warp at 64 tokens)
+      constexpr int H = MP / 2, HC = H / 8;
+      float sum[H];
 #pragma unroll
-      for (int cb = 0; cb < MP / 2; cb += 8) {
-        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < used; ++j) {
-          uint32_t v[8];
-          tmem_ld_32x32b_x8(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * MP + c_lo + cb), v);
-          tmem_ld_wait();
+      for (int i = 0; i < H; ++i) sum[i] = 0.f;
+      for (int j = 0; j < used; ++j) {
+        uint32_t v[HC][8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) sum[i] += __uint_as_float(v[i]);  // integers < 2^24: exact
-        }
+        for (int cb = 0; cb < HC; ++cb)
+          tmem_ld_32x32b_x8(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * MP + c_lo + cb * 8), v[cb]);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t addr = dst_c + (uint32_t)((c_lo + cb + i) * 4);
-          if (cs > 1)
-            st_cluster_u32(addr, __float_as_uint(sum[i]));
-          else
-            st_shared_u32(addr, __float_as_uint(sum[i]));
-        }
+        for (int cb = 0; cb < HC; ++cb)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sum[cb * 8 + i] += __uint_as_float(v[cb][i]);  // integers < 2^24: exact
+      }
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const uint32_t addr = dst_c + (uint32_t)((c_lo + i) * 4);
+        if (cs > 1)
+          st_cluster_u32(addr, __float_as_uint(sum[i]));
+        else
+          st_shared_u32(addr, __float_as_uint(sum[i]));
       }
     }
   }
