@@ -63,7 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--no-gemv-leg", action="store_true", help="skip the 100B-class GEMV leg of the default line")
     p.add_argument("--no-ffn-leg", action="store_true", help="skip the fused FFN-block leg of the default line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
-    p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill", "ffn"], default="decode_sweep",
+    p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill", "ffn", "quant_weight"],
+                   default="decode_sweep",
                    help="decode_sweep (default, the headline) or one single-kernel leg")
     return p.parse_args(argv)
 
@@ -489,6 +490,58 @@ def ffn_leg(stack, device, peaks, reps=20):
                          "traffic": None, "note": "latency-bound chain: the block's two launches average"}}
 
 
+def quant_weight_leg(device, peaks, reps=10):
+    """Weight ternarisation and packing (bitnet_quant_weight, AbsMean) of a 100B-class matrix,
+    N = 28672, K = 8192, fp32 and bf16 sources N(0, 0.02^2), 2 rotating sets each.
+
+    The scale must be known before any code, so the weights are read twice: once for the exact
+    sum, once for the codes. The achieved figure counts both reads plus the packed write
+    (2 N K b + N K / 4 bytes for b-byte weights)."""
+    import torch
+
+    from ternary_weight_gb300 import binding
+
+    N, K = 28672, 8192
+    res = {}
+    stream = torch.cuda.current_stream(device)
+    for dt, tdt, b in (("f32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        sets = []
+        for i in range(2):
+            w = torch.from_numpy(workloads.source_weights_f32(N, K, 9100 + i)).to(device)
+            w = w.to(tdt)
+            sets.append((w, torch.empty((N, K // 4), dtype=torch.uint8, device=device),
+                         torch.empty(1, dtype=torch.float32, device=device)))
+
+        def call(i):
+            w, wp, sc = sets[i % 2]
+            binding.quant_weight(w, out=wp, scale=sc)
+
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                call(i)
+        g.replay()
+        torch.cuda.synchronize(device)
+        t = time_replays(g, 3, stream) / (3 * reps)
+        byts = 2 * N * K * b + N * K // 4
+        res[dt] = (t, byts / t / 1e9)
+        del sets
+        torch.cuda.empty_cache()
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    t32, g32 = res["f32"]
+    tbf, gbf = res["bf16"]
+    return {"workload": "weight ternarisation + packing (AbsMean), N=28672 K=8192, fp32 and bf16 sources",
+            "value": g32, "unit": "GB/s", "ms_per_call": t32 * 1e3, "us_per_call_f32": t32 * 1e6,
+            "us_per_call_bf16": tbf * 1e6, "gbs_bf16": gbf, "launches": reps * 3,
+            "roofline": {"bound": "hbm", "achieved": g32, "peak": peak, "unit": "GB/s", "frac": g32 / peak,
+                         "traffic": None,
+                         "note": "fp32 case; bytes = both reads of the weights + the packed write; the bf16 "
+                                 "case is bound by the integer work of the exact sum (gbs_bf16)"}}
+
+
 def run_kernel_workload(args):
     """--workload gemv_100b | prefill: one line for that single kernel (no e2e / CPU leg)."""
     import torch
@@ -507,6 +560,8 @@ def run_kernel_workload(args):
     if args.workload == "ffn":
         leg = ffn_leg(stack, device, peaks, reps=args.steps)
         leg["ms_per_call"] = leg["us_per_block"] * args.layers * 1e-3  # one step = every layer's block
+    elif args.workload == "quant_weight":
+        leg = quant_weight_leg(device, peaks, reps=args.steps)
     else:
         leg = kernel_leg(args.workload, device, peaks, reps=args.steps, warmup=args.warmup)
     clocks = sampler.stop()
@@ -514,8 +569,10 @@ def run_kernel_workload(args):
             "warmup": args.warmup, "ms_per_step": leg["ms_per_call"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "i8xi2->i32", "data": "synthetic",
             "config": {"workload": leg["workload"], "l2": "rotating input sets larger than L2"},
-            "gpu_launches": args.steps * (2 * args.layers if args.workload == "ffn" else 1), "clocks": clocks,
-            "roofline": leg["roofline"]}
+            "gpu_launches": args.steps * {"ffn": 2 * args.layers, "quant_weight": 3 * 2 * 3}.get(args.workload, 1),
+            "clocks": clocks,
+            "roofline": leg["roofline"],
+            "leg": {k: v for k, v in leg.items() if k not in ("workload", "value", "unit", "roofline")}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

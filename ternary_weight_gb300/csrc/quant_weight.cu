@@ -15,11 +15,11 @@
 // division rounding to nearest. A weight outside the range (or NaN) is reported as an error.
 //
 // Three launches on the caller's stream, no workspace:
-//   1. reduce: a grid-stride pass over the whole matrix (flat, four 16-byte loads per thread in
+//   1. qw_reduce: a grid-stride pass over the whole matrix (flat, four 16-byte loads per thread in
 //      flight); each CTA parks its partial (128-bit sum, or max |w|) in the first bytes of the
 //      packed output, 16 bytes per CTA;
-//   2. finish: one CTA adds the partials and writes the scale (device float);
-//   3. pack: one thread per packed 32-bit word (16 weights: four 16-byte loads), overwriting the
+//   2. qw_finish: one CTA adds the partials and writes the scale (device float);
+//   3. qw_pack: one thread per packed 32-bit word (16 weights: four 16-byte loads), overwriting the
 //      parked partials. The codes are decided by comparisons against thresholds derived from the
 //      scale that reproduce rne(fl(w / scale)) exactly (see code_threshold).
 #include "bitnet_dev.cuh"
@@ -82,7 +82,7 @@ __device__ __forceinline__ u128 shfl_xor_u128(u128 v, int off) {
 // mode 0: per-CTA 128-bit partial of S (bit 127 set when a weight is out of range);
 // mode 1: per-CTA max |w| bits (NaN ignored, as fmaxf does).
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads) reduce(const void* __restrict__ w, uint8_t* __restrict__ park,
+__global__ void __launch_bounds__(kThreads) qw_reduce(const void* __restrict__ w, uint8_t* __restrict__ park,
                                                    int64_t total, int mode) {
   const int64_t nvec = total >> 2;  // 4-weight vectors
   const int64_t stride = (int64_t)gridDim.x * kThreads * kVecPerThread;
@@ -159,7 +159,7 @@ __device__ double u128_to_double_rn(u128 s) {
   return ldexp(__ull2double_rn(top), 64 - lz);
 }
 
-__global__ void __launch_bounds__(kThreads) finish(const uint8_t* __restrict__ park, int nparts, float* __restrict__ w_scale,
+__global__ void __launch_bounds__(kThreads) qw_finish(const uint8_t* __restrict__ park, int nparts, float* __restrict__ w_scale,
                                                    int64_t total, int mode) {
   __shared__ u128 red_s[kThreads / 32];
   __shared__ uint32_t red_m[kThreads / 32];
@@ -228,7 +228,7 @@ __device__ __forceinline__ uint32_t code_of(float v, float thr, int mode) {
 // Thread t writes packed word t: row n, word c of the row (block i = c / 8, bytes g0..g0+3 with
 // g0 = 4 (c % 8)); byte g0 + b holds the codes of k = 128 i + g0 + b + 32 j at bit 6 - 2j.
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads) pack(const void* __restrict__ w, const float* __restrict__ w_scale,
+__global__ void __launch_bounds__(kThreads) qw_pack(const void* __restrict__ w, const float* __restrict__ w_scale,
                                                  uint32_t* __restrict__ wp, int64_t N, int64_t K, int mode) {
   const float thr = code_threshold(*w_scale, mode);
   const int64_t words_per_row = K / 16;
@@ -260,12 +260,12 @@ cudaError_t launch_t(const void* w, int64_t N, int64_t K, int mode, uint8_t* wp,
   // bytes) with room to spare; four CTAs per SM keep enough loads in flight for HBM
   int64_t parts = (total + kThreads * kVecPerThread * 4 - 1) / (kThreads * kVecPerThread * 4);
   if (parts > (int64_t)num_sms * 4) parts = (int64_t)num_sms * 4;
-  reduce<BF16><<<(unsigned)parts, kThreads, 0, stream>>>(w, wp, total, mode);
-  finish<<<1, kThreads, 0, stream>>>(wp, (int)parts, w_scale, total, mode);
+  qw_reduce<BF16><<<(unsigned)parts, kThreads, 0, stream>>>(w, wp, total, mode);
+  qw_finish<<<1, kThreads, 0, stream>>>(wp, (int)parts, w_scale, total, mode);
   const int64_t words = total / 16;
   int64_t blocks = (words + kThreads - 1) / kThreads;
   if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
-  pack<BF16><<<(unsigned)blocks, kThreads, 0, stream>>>(w, w_scale, reinterpret_cast<uint32_t*>(wp), N, K, mode);
+  qw_pack<BF16><<<(unsigned)blocks, kThreads, 0, stream>>>(w, w_scale, reinterpret_cast<uint32_t*>(wp), N, K, mode);
   return cudaGetLastError();
 }
 
