@@ -62,6 +62,7 @@ def parse_args(argv=None):
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-gemv-leg", action="store_true", help="skip the 100B-class GEMV leg of the default line")
     p.add_argument("--no-ffn-leg", action="store_true", help="skip the fused FFN-block leg of the default line")
+    p.add_argument("--no-batched-leg", action="store_true", help="skip the batched-decode leg of the default line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill", "ffn", "quant_weight"],
                    default="decode_sweep",
@@ -542,6 +543,49 @@ def quant_weight_leg(device, peaks, reps=10):
                                  "case is bound by the integer work of the exact sum (gbs_bf16)"}}
 
 
+def batched_decode_leg(device, peaks, reps=20, nsets=32):
+    """The batched decode matmuls at M in {1, 4, 16, 64} on the FFN shapes (K 2560, N 6912 and
+    K 6912, N 2560), bf16 activations with 1% x20 outliers quantised per token, then
+    bitnet_i2s_matmul with automatic kernel choice. 32 rotating weight sets per shape (141 MB,
+    larger than L2), each case one graph of back-to-back calls."""
+    import torch
+
+    from ternary_weight_gb300 import binding
+
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    stream = torch.cuda.current_stream(device)
+    cases = []
+    for (K, N) in ((workloads.HIDDEN, workloads.FFN), (workloads.FFN, workloads.HIDDEN)):
+        wps = [binding.pack_i2s(torch.from_numpy(workloads.ternary_weights(N, K, 9300 + i)).to(device))
+               for i in range(nsets)]
+        for M in (1, 4, 16, 64):
+            x = torch.from_numpy(workloads.activations(M, K, 9400 + M, "bf16", 0.01).view(np.int16)).to(device)
+            xq, s_, rs = binding.quant_act(x.view(torch.bfloat16))
+            out = torch.empty((M, N), dtype=torch.float32, device=device)
+
+            def call(i):
+                binding.i2s_matmul(xq, s_, rs, wps[i % nsets], 0.016, out=out)
+
+            for i in range(3):
+                call(i)
+            torch.cuda.synchronize(device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(reps):
+                    call(i)
+            g.replay()
+            torch.cuda.synchronize(device)
+            t = time_replays(g, 3, stream) / (3 * reps)
+            byts = N * K // 4 + M * K + 8 * M + 4 * M * N
+            gbs = byts / t / 1e9
+            cases.append({"M": M, "K": K, "N": N, "us": t * 1e6, "GB/s": gbs, "frac": gbs / peak,
+                          "TOPS": 2.0 * M * N * K / t / 1e12})
+        del wps
+    return {"workload": "batched decode matmuls, M in {1,4,16,64}, (K,N) in {(2560,6912),(6912,2560)}, bf16 "
+                        "activations with 1% x20 outliers, auto kernel choice",
+            "unit": "GB/s", "peak": peak, "cases": cases}
+
+
 def run_kernel_workload(args):
     """--workload gemv_100b | prefill: one line for that single kernel (no e2e / CPU leg)."""
     import torch
@@ -773,6 +817,7 @@ def run_ours(args):
     prefill = None if args.no_prefill else kernel_leg("prefill", device, peaks)
     gemv_100b = None if args.no_gemv_leg else kernel_leg("gemv_100b", device, peaks)
     ffn = None if args.no_ffn_leg else ffn_leg(stack, device, peaks)
+    batched = None if args.no_batched_leg else batched_decode_leg(device, peaks)
     plan.close()
     plan_b.close()
 
@@ -809,6 +854,7 @@ def run_ours(args):
         "prefill": prefill,
         "gemv_100b": gemv_100b,
         "ffn": ffn,
+        "batched_decode": batched,
         "cpu_baseline": cpu,
     }
     if rank == 0:
