@@ -13,33 +13,45 @@
 // tensor core applies it to all tokens: D[n][m] += W[n][k] * X[m][k] with tcgen05.mma
 // kind::f16, M = 128 weight rows, N = MP (the token count rounded up to 16), K = 16.
 //
-// K order. A 128-weight i2_s block is 32 bytes; byte g holds the codes of k = g + 32j at bit
-// pair j (j = 0 at bits 7:6). The dot product does not care about the order of k as long as
-// both operands agree, so the kernel uses the byte order: within a block, word w (bytes
-// 4w..4w+3), pair j and byte b of the word sit at position p = 16w + 4j + b. The 64 positions
-// of a k-block are then 16 contiguous packed bytes of a row, and the 4 codes that share (w, j)
-// are one shift and one mask of a 32-bit word. The activations follow the same order: position
-// 16w + 4j + b holds activation k = 4w + b + 32j, so 4-byte groups move as a whole.
+// Stages. The K range is walked in stages of 256 k: two i2_s blocks, sixteen K = 16 MMAs.
+// Synchronisation is per stage: one wait, one fence and one barrier arrival per warp cover 256 k.
 //
-// Structure (one CTA per 128 weight rows and a K range; a thread-block cluster of up to 8
-// CTAs splits K at 64-k granularity):
-//  * warps 1-2 (loaders) copy the inputs of 8 k-blocks at a time with 16-byte cp.async into a
-//    staging ring: k-block kb is packed bytes 16kb..16kb+15 of every weight row, so a stage is
-//    128 contiguous bytes per row (8 consecutive lanes per row), plus the 5 activation blocks
-//    of 128 bytes per token row those k-blocks draw on. Contiguous lanes keep each warp's
-//    copies to a few cache lines; copies of single 16-byte pieces per row left the loads
-//    bound by the request rate. Completion is signalled on the stage's mbarrier by
-//    cp.async.mbarrier.arrive.noinc, so the loads stay in flight while the loaders move on;
-//  * warps 3-18 (expanders) turn a staged k-block into the fp16 weight tile (codes 0..3,
-//    exact) and the fp16 activation tile (int8 values, exact) in the 128-byte-swizzled K-major
-//    layout the MMA reads, in a ring of tile slots. They touch only shared memory: the proxy
-//    fence they need before the tensor core reads a tile then has no global loads to wait for;
-//  * warp 0: allocates tensor memory; one lane issues the MMAs, rotating over 8 independent
-//    128 x MP fp32 accumulators (tiny MMAs into one accumulator would wait on each other);
-//  * then eight expander warps read the accumulator and store each row's partial sums into the
-//    shared memory of the cluster CTA that owns that row (distributed shared memory, remote
-//    stores); after one cluster barrier each CTA sums its rows' partials locally and writes
-//    those outputs.
+// Operands. The decoded weights (A, 128 rows x 256 k of fp16 per stage) are written straight
+// into tensor memory with tcgen05.st, and the MMA reads A from there; only the activations (B,
+// MP rows) go through shared memory. A weight stage is 64 KB of fp16 against 8 KB of packed
+// input: staged through shared memory it would be written and read back by the tensor core,
+// 128 KB of shared-memory traffic per stage, more than the stage's arithmetic takes.
+//
+// K order. Inside an i2_s block byte g holds the codes of k = g + 32j at bit pair j (j = 0 at
+// bits 7:6), so the 16 bytes 16h..16h+15 of block b hold, for each j, the 16 consecutive
+// k = 128b + 32j + 16h + e of the stage. Stage position p = 64q + 16j + pe (q = 2b + h) holds that
+// k, where pe runs over e in the order 0, 2, 1, 3 inside each group of four: two codes per fp16
+// pair come from bytes 0 and 2 (or 1 and 3) of one word under one mask, and the activations'
+// byte permute applies the same order at no cost. The dot product only needs both operands to
+// agree.
+//
+// Decoding (exact): (word & (3 << sh, in bytes 0 and 2)) | 0x6400 in each half is the fp16
+// 1024 + c * 2^sh; one fma by 2^-sh and -1024 * 2^-sh gives c in {0, 1, 2, 3}. An int8 x becomes
+// 1024 + (x + 128) by a byte permute under 0x64, minus 1152.
+//
+// Structure (one CTA per 128 weight rows and a range of stages; a thread-block cluster of up to
+// 8 CTAs splits the stages):
+//  * warps 1-16 (workers): warp w owns tensor-memory lanes 32(w%4)..+31, i.e. weight rows, and
+//    the 16-byte quarter q = (w-1)/4 of each row's 64 stage bytes. Each thread copies its own
+//    16 weight bytes and up to two 16-byte pieces of the stage's int8 activations with
+//    cp.async into a private ring of PD stages in shared memory (one commit group per stage, so
+//    PD stages are in flight without tying up registers; the weights of the first stages are
+//    requested before waiting for the previous kernel). Per stage it decodes its bytes into 32
+//    tensor-memory columns of the stage's A slot, writes its activation pieces into the
+//    128-byte-swizzled K-major B tile, fences, and its warp arrives once;
+//  * warp 0: allocates tensor memory; one lane issues the MMAs, rotating over NACC independent
+//    128 x MP fp32 accumulators (tiny MMAs into one accumulator would wait on each other), and
+//    commits one release of the slot per stage;
+//  * epilogue: each worker warp reads 32 accumulator rows (its tensor-memory lane quarter) and
+//    a quarter of the columns, adds the NACC accumulators, and either keeps the sums (rows its
+//    CTA owns) or stores them as 16-byte pieces into the shared memory of the cluster CTA that
+//    owns those rows; after one cluster barrier the owners add what they received and write
+//    the outputs.
 // Exactness: every operand is a small integer fp16 holds exactly, and every partial and total
 // sum is an integer of magnitude <= 3 * 127 * K < 2^24 for K <= 32768, so the fp32
 // accumulations and the cross-CTA sums are exact.
@@ -53,61 +65,73 @@
 namespace bitnet {
 namespace {
 
-constexpr int TW = 128;                  // weight rows per CTA (the MMA's M)
-constexpr int KB = 64;                   // k positions per MMA k-block (one 128-byte fp16 row)
-constexpr int A_TILE = TW * KB * 2;      // fp16 weight tile
-constexpr int XP_WARPS = 16;             // expander warps (the first 8 also drain the accumulator)
-constexpr int XP_THREADS = XP_WARPS * 32;
-constexpr int LD_WARPS = 2;              // loader warps
-constexpr int LD_THREADS = LD_WARPS * 32;
-constexpr int THREADS = (1 + LD_WARPS + XP_WARPS) * 32;
-constexpr int XP_WARP0 = 1 + LD_WARPS;   // first expander warp
+constexpr int TW = 128;                    // weight rows per CTA (the MMA's M)
+constexpr int SK = 256;                    // k per stage (two i2_s blocks)
+constexpr int KSTEPS = SK / 16;            // K = 16 MMAs per stage
+constexpr int WK_WARPS = 16;               // workers
+constexpr int WK_THREADS = WK_WARPS * 32;  // four per weight row
+constexpr int THREADS = 32 + WK_THREADS;
 constexpr int kMaxCluster = 8;
-constexpr int KB_ST = 8;                 // k-blocks per staging stage
-constexpr int W_PITCH = 16 * KB_ST + 16;  // staged packed bytes per weight row (padded: conflict-free reads)
-constexpr int W_ST = TW * W_PITCH;
-constexpr int X_BLKS = KB_ST / 2 + 1;    // 128-activation blocks a stage may draw on
+constexpr uint32_t TMEM_COLS = 512;        // accumulators, then the A stages (one CTA per SM)
+constexpr int A_COLS = SK / 2;             // tensor-memory columns of one fp16 A stage
+
+// rows [row_lo(r), row_lo(r + 1)) of the tile are finished by cluster rank r
+__host__ __device__ constexpr int row_lo(int r, int cs) { return TW * r / cs; }
+
+// most partial rows one CTA receives: (cs - 1) sources times its largest row share
+constexpr int max_recv_rows() {
+  int best = 0;
+  for (int cs = 2; cs <= kMaxCluster; ++cs)
+    for (int r = 0; r < cs; ++r) {
+      const int v = (cs - 1) * (row_lo(r + 1, cs) - row_lo(r, cs));
+      best = v > best ? v : best;
+    }
+  return best;
+}
 
 template <int MP>
 struct SmallCfg {
   static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "tokens per MMA: a multiple of 16, at most 64");
-  static constexpr int B_TILE = MP * KB * 2;          // fp16 activation tile
-  static constexpr int AB_BYTES = A_TILE + B_TILE;
-  static constexpr int AB_STAGES = 3;
-  static constexpr int X_ROW = X_BLKS * 128;          // staged activation bytes per token row
-  static constexpr int ST_BYTES = W_ST + MP * X_ROW;
-  static constexpr int ST_STAGES = MP <= 32 ? 3 : 2;
-  static constexpr int XCH = (MP * 8 + XP_THREADS - 1) / XP_THREADS;  // activation chunks per thread
-  static constexpr int PITCH = MP + 1;                // fp32 partials per row (odd: conflict-free)
-  static constexpr int RECV_BYTES = (TW + kMaxCluster) * PITCH * 4;
-  static constexpr int SMEM = 1024 + AB_STAGES * AB_BYTES + ST_STAGES * ST_BYTES + RECV_BYTES + MP * 8;
-  // NACC accumulators of MP columns each: MMA i of the CTA goes to accumulator i % NACC, so
-  // consecutive MMAs are independent (with MP as small as 16 an MMA is far shorter than its
-  // latency, and one shared accumulator would serialise them); the epilogue adds them up
-  static constexpr int NACC = 8;
-  static constexpr uint32_t TMEM_COLS = NACC * MP <= 128 ? 128 : (NACC * MP <= 256 ? 256 : 512);
+  static constexpr int NACC = MP <= 32 ? 8 : 4;                   // independent accumulators
+  static constexpr int ACOL = (NACC * MP + 127) / 128 * 128;       // first A column in tensor memory
+  static constexpr int NS = (int)(TMEM_COLS - ACOL) / A_COLS;      // A/B stages (tensor memory bound)
+  static constexpr int B_SUB = MP * 128;                           // fp16 activations, 64 k x MP rows
+  static constexpr int B_STAGE = 4 * B_SUB;
+  static constexpr int XV = (MP * 16 + WK_THREADS - 1) / WK_THREADS;  // 16-byte activation pieces per thread
+  static constexpr int PD = MP <= 32 ? 6 : 5;                      // staged input stages in flight
+  static constexpr int RAW_SLOT = WK_THREADS * 16 * (1 + XV);      // one stage's copies, 16 bytes per thread each
+  static constexpr int NC = MP / 4;                                // accumulator columns per epilogue warp
+  static constexpr int PITCH = MP + 4;                             // floats per received row (16-byte rows)
+  static constexpr int RECV_ROWS = max_recv_rows();
+  static constexpr int SMEM = 1024 + NS * B_STAGE + PD * RAW_SLOT + RECV_ROWS * PITCH * 4;
   static constexpr uint32_t IDESC = make_idesc_f16_f32(TW, MP);
-  static_assert(AB_BYTES % 1024 == 0, "1024-byte aligned tiles");
-  static_assert(ST_BYTES % 16 == 0, "16-byte copies");
-  static_assert(SMEM <= 227 * 1024, "shared memory");
+  // accumulators read per tensor-memory wait in the epilogue (registers: LB * NC)
+  static constexpr int LB = NACC * NC <= 64 ? NACC : NACC / 2;
+  static_assert(NS >= 2 && ACOL + NS * A_COLS <= (int)TMEM_COLS, "tensor memory columns");
+  static_assert(B_SUB % 1024 == 0, "1024-byte aligned tiles");
+  static_assert(SMEM <= 227 * 1024 - 256, "shared memory (static barriers included)");
 };
 
-// rows [row_lo(r), row_lo(r + 1)) of the tile are finished by cluster rank r
-__device__ __forceinline__ int row_lo(int r, int cs) { return TW * r / cs; }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
-__device__ __forceinline__ uint2 codes4_to_f16(uint32_t codes) {  // 4 codes (one per byte) -> 4 fp16
-  const uint32_t l = __byte_perm(codes, 0x64646464u, 0x4140);
-  const uint32_t h = __byte_perm(codes, 0x64646464u, 0x4342);
-  const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
-  const __half2 rl = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
-  const __half2 rh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
-  return make_uint2(*reinterpret_cast<const uint32_t*>(&rl), *reinterpret_cast<const uint32_t*>(&rh));
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint2 s8x4_to_f16(uint32_t w) {  // 4 int8 -> 4 exact fp16
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&c));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// 4 int8 (bytes 0..3) -> fp16 pairs (byte 0, byte 2) and (byte 1, byte 3), exact
+__device__ __forceinline__ uint2 s8x4_to_f16_perm(uint32_t w) {
   const uint32_t u = w ^ 0x80808080u;
-  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);
-  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342);
+  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4240);
+  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4341);
   const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480), __ushort_as_half((unsigned short)0x6480));
   const __half2 rl = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
   const __half2 rh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
@@ -119,6 +143,69 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is 128 lanes (rows) x 8 columns (16 fp16
+// along K, two per column, the lower k in the low half).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp writes lane (base + t).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x NC consecutive 32-bit columns (NC = 4, 8, 12 or 16) into r[0..NC)
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (NC == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+  } else if constexpr (NC == 8) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+  } else if constexpr (NC == 12) {
+    tmem_ld_cols<8>(taddr, r);
+    tmem_ld_cols<4>(taddr + 8, r + 8);
+  } else {
+    static_assert(NC == 16, "4, 8, 12 or 16 columns");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+  }
+}
+
 template <int MP>
 __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* __restrict__ xq,
                                                                  const float* __restrict__ act_scale,
@@ -127,53 +214,68 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
                                                                  float* __restrict__ out, int32_t* __restrict__ acc_out,
                                                                  int M, int N, int K) {
   using Cfg = SmallCfg<MP>;
-  constexpr int AB_STAGES = Cfg::AB_STAGES, ST_STAGES = Cfg::ST_STAGES;
+  constexpr int NS = Cfg::NS, XV = Cfg::XV, NC = Cfg::NC, PD = Cfg::PD, NACC = Cfg::NACC;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t st_full[ST_STAGES];   // a k-block's inputs staged
-  __shared__ __align__(8) uint64_t st_empty[ST_STAGES];  // expanders done with a staged k-block
-  __shared__ __align__(8) uint64_t ab_full[AB_STAGES];   // fp16 tiles of a k-block written
-  __shared__ __align__(8) uint64_t ab_empty[AB_STAGES];  // MMAs done reading a slot
-  __shared__ __align__(8) uint64_t done_bar;             // every MMA complete
+  __shared__ __align__(8) uint64_t full_bar[NS];   // a stage's operands written (one arrival per worker warp)
+  __shared__ __align__(8) uint64_t empty_bar[NS];  // the MMAs reading a stage slot are done (one commit)
+  __shared__ __align__(8) uint64_t done_bar;       // every MMA complete
   __shared__ uint32_t tmem_slot;
 
+  pdl_launch_dependents();
   const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* ab_ring = base;                                          // AB_STAGES x (A, B)
-  uint8_t* st_ring = base + AB_STAGES * Cfg::AB_BYTES;              // ST_STAGES x (W, X)
-  float* recv = reinterpret_cast<float*>(st_ring + ST_STAGES * Cfg::ST_BYTES);  // pushed partials
-  int* tok_rs = reinterpret_cast<int*>(recv + (TW + kMaxCluster) * Cfg::PITCH);  // rowsum per token
-  float* tok_s = reinterpret_cast<float*>(tok_rs + MP);                           // scale per token
+  const uint32_t bring = raw_addr + ((1024u - (raw_addr & 1023u)) & 1023u);  // NS B tiles
+  const uint32_t staged = bring + NS * Cfg::B_STAGE;                         // PD stages of copied inputs
+  const uint32_t recv = staged + PD * Cfg::RAW_SLOT;                         // received partial rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * TW;
   const int cs = (int)gridDim.y;
   const int rank = (int)cluster_ctarank();
-  const int nkb_all = K / KB;
-  const int kb_lo = nkb_all * rank / cs, kb_hi = nkb_all * (rank + 1) / cs;
-  const int nkb = kb_hi - kb_lo;
+  const int nblk = K / 128;               // i2_s blocks
+  const int nst_all = (nblk + 1) >> 1;    // 256-k stages (the last one half when nblk is odd)
+  const int st_lo = nst_all * rank / cs, st_hi = nst_all * (rank + 1) / cs;
+  const int nst = st_hi - st_lo;
+
+  // worker roles (meaningful for warps 1..16): tensor-memory lane quarter, weight row, and the
+  // 16-byte quarter q of the row's 64 stage bytes (i2_s block q/2 of the stage, half q%2)
+  const int t = (int)threadIdx.x - 32;
+  const int lq = warp & 3, q = (warp - 1) >> 2, qb = q >> 1;
+  const int row = 32 * lq + lane;
+  const bool row_ok = warp >= 1 && n0 + row < N;
+  const uint8_t* wrow = wp + (int64_t)(row_ok ? n0 + row : 0) * (K / 4) + 16 * q;
+  const uint32_t my_w = staged + (uint32_t)(16 * t);  // this thread's weight copy in stage slot 0
+  auto issue_w = [&](int i) {
+    const int gs = st_lo + i;
+    const bool ok = row_ok && 2 * gs + qb < nblk;
+    cp_async_16(my_w + (uint32_t)((i % PD) * Cfg::RAW_SLOT), ok ? wrow + 64 * (int64_t)gs : wp, ok ? 16u : 0u);
+  };
+  auto issue_x = [&](int i) {
+    const int gs = st_lo + i;
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int idx = t + WK_THREADS * v, m = idx >> 4, u = idx & 15;
+      if (idx < MP * 16) {
+        const bool ok = m < M && 2 * gs + (u >> 3) < nblk;
+        cp_async_16(my_w + (uint32_t)((i % PD) * Cfg::RAW_SLOT + WK_THREADS * 16 * (1 + v)),
+                    ok ? xq + (int64_t)m * K + 256 * (int64_t)gs + 16 * u : xq, ok ? 16u : 0u);
+      }
+    }
+  };
+  if (warp >= 1) {
+    for (int p = 0; p < PD && p < nst; ++p) issue_w(p);  // weights do not depend on the previous kernel
+  }
 
   if (threadIdx.x == 0) {
-    // expander barriers count warps: each warp's lanes order their own writes, __syncwarp,
-    // and one lane arrives (hundreds of per-thread arrivals on one barrier word serialise)
-    for (int s = 0; s < ST_STAGES; ++s) {
-      mbar_init(&st_full[s], LD_THREADS);
-      mbar_init(&st_empty[s], XP_WARPS);
-    }
-    for (int a = 0; a < AB_STAGES; ++a) {
-      mbar_init(&ab_full[a], XP_WARPS);
-      mbar_init(&ab_empty[a], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], WK_WARPS);
+      mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&done_bar, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_slot, Cfg::TMEM_COLS);
+    tmem_alloc(&tmem_slot, TMEM_COLS);
     tmem_relinquish();
-  }
-  if (threadIdx.x >= 64 && threadIdx.x < 64 + MP) {  // warps 2-3: the epilogue's per-token inputs
-    const int m = threadIdx.x - 64;
-    tok_rs[m] = m < M ? __ldg(rowsum + m) : 0;
-    tok_s[m] = m < M ? __ldg(act_scale + m) : 1.0f;
   }
   tc_fence_before();
   __syncthreads();
@@ -184,166 +286,160 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
   if (warp == 0) {
     // ================================ MMA issuer ================================
     if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int a = kb % AB_STAGES, ua = kb / AB_STAGES;
-        if (!mbar_wait(&ab_full[a], ua & 1, &abort)) break;
+      // The issuing thread's own arithmetic is on the critical path: a tiny MMA occupies the
+      // tensor pipe for only ~50 cycles, so each issue here is a few integer adds to
+      // descriptors built once (the address field is the low 14 bits; offsets never carry).
+      const uint64_t bdesc0 = make_sw128_kmajor_desc(bring);
+      const uint32_t acol0 = tmem + (uint32_t)Cfg::ACOL;
+      int s = 0;
+      uint32_t phase = 0;
+      for (int i = 0; i < nst; ++i) {
+        if (!mbar_wait(&full_bar[s], phase, &abort)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(ab_ring + a * Cfg::AB_BYTES), b_addr = a_addr + A_TILE;
+        const uint32_t a_col = acol0 + (uint32_t)(s * A_COLS);
+        const uint64_t bd = bdesc0 + (uint64_t)((s * Cfg::B_STAGE) >> 4);
+        const uint32_t first = i > 0 ? 1u : 0u;  // accumulate unless this is an accumulator's first MMA
 #pragma unroll
-        for (int kk = 0; kk < KB / 16; ++kk) {
-          const int i = kb * (KB / 16) + kk;  // MMA index within the CTA
-          mma_f16_ss(tmem + (uint32_t)((i % Cfg::NACC) * MP), make_sw128_kmajor_desc(a_addr + kk * 32),
-                     make_sw128_kmajor_desc(b_addr + kk * 32), Cfg::IDESC, i >= Cfg::NACC ? 1u : 0u);
+        for (int ks = 0; ks < KSTEPS; ++ks)
+          mma_f16_ts(tmem + (uint32_t)((ks % NACC) * MP), a_col + (uint32_t)(8 * ks),
+                     bd + (uint64_t)(((ks >> 2) * Cfg::B_SUB + (ks & 3) * 32) >> 4), Cfg::IDESC,
+                     ks >= NACC ? 1u : first);
+        mma_commit(&empty_bar[s]);
+        if (++s == NS) {
+          s = 0;
+          phase ^= 1u;
         }
-        mma_commit(&ab_empty[a]);
       }
       mma_commit(&done_bar);  // tracks every MMA this thread issued
     }
-  } else if (warp < XP_WARP0) {
-    // ================================ loaders ================================
-    // stage s holds k-blocks kb_lo + 8s .. +7: weight row r's bytes 16 * those (8 chunks,
-    // lanes 8i..8i+7 on one row), and token row m's activation blocks blk0 .. blk0 + 4,
-    // blk0 = (kb_lo + 8s) / 2
-    const int lt = threadIdx.x - 32;  // 0..63
-    const int nst = (nkb + KB_ST - 1) / KB_ST;
-    int st_i = 0;
-    for (; st_i < nst; ++st_i) {
-      const int s = st_i % ST_STAGES, u = st_i / ST_STAGES;
-      if (u > 0 && !mbar_wait(&st_empty[s], (u - 1) & 1, &abort)) break;
-      const int kb0 = kb_lo + st_i * KB_ST, blk0 = kb0 >> 1;
-      const uint32_t st = smem_u32(st_ring + s * Cfg::ST_BYTES);
-#pragma unroll 4
-      for (int id = lt; id < TW * KB_ST; id += LD_THREADS) {
-        const int r = id >> 3, c = id & 7;
-        const bool ok = n0 + r < N && kb0 + c < kb_hi;
-        cp_async_16(st + (uint32_t)(r * W_PITCH + c * 16),
-                    wp + (int64_t)(ok ? n0 + r : 0) * (K / 4) + (ok ? (kb0 + c) * 16 : 0), ok ? 16u : 0u);
-      }
-      for (int id = lt; id < MP * X_BLKS * 8; id += LD_THREADS) {
-        const int m = id / (X_BLKS * 8), c = id % (X_BLKS * 8);
-        const bool ok = m < M && blk0 * 8 + c < nkb_all * 4;  // 16-byte pieces within K
-        cp_async_16(st + (uint32_t)(W_ST + m * Cfg::X_ROW + c * 16),
-                    xq + (ok ? (int64_t)m * K + blk0 * 128 + c * 16 : 0), ok ? 16u : 0u);
-      }
-      cp_async_arrive_noinc(&st_full[s]);
-    }
-    // every copy issued must land before the CTA can exit
-    asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
-    // ================================ expanders ================================
-    const int t = threadIdx.x - XP_WARP0 * 32;  // 0..511
-    const int r = t >> 2, wq = t & 3;            // weight row and its word of each k-block
-    for (int kbl = 0; kbl < nkb && !abort; ++kbl) {
-      const int si = kbl / KB_ST, q = kbl % KB_ST;  // staging stage and k-block within it
-      const int s = si % ST_STAGES, us = si / ST_STAGES;
-      const int a = kbl % AB_STAGES, ua = kbl / AB_STAGES;
-      if (q == 0 && !mbar_wait_warp(&st_full[s], us & 1, &abort)) break;
-      if (ua > 0 && !mbar_wait_warp(&ab_empty[a], (ua - 1) & 1, &abort)) break;
-      const uint8_t* st = st_ring + s * Cfg::ST_BYTES;
-      uint8_t* at = ab_ring + a * Cfg::AB_BYTES;
-      uint8_t* bt = at + A_TILE;
-      const int kb = kb_lo + kbl;
-      const int rb = (kb >> 1) - ((kb_lo + si * KB_ST) >> 1), half = kb & 1;
-      const uint32_t word = *reinterpret_cast<const uint32_t*>(st + r * W_PITCH + q * 16 + wq * 4);
-      uint32_t xw[Cfg::XCH][2];
+    // ================================ workers ================================
+    pdl_wait();  // the activations may be the previous kernel's output
+#pragma unroll 1
+    for (int p = 0; p < PD; ++p) {  // one commit group per stage (the first also holds the weights)
+      if (p < nst) issue_x(p);
+      cp_async_commit();
+    }
+    // per bit pair j (shift sh = 6 - 2j): mask, and the fma's scale 2^-sh and bias -1024 * 2^-sh
+    const uint32_t kMask[4] = {0x00C000C0u, 0x00300030u, 0x000C000Cu, 0x00030003u};
+    const uint32_t kScale[4] = {0x24002400u, 0x2C002C00u, 0x34003400u, 0x3C003C00u};  // 2^-6, 2^-4, 2^-2, 1
+    const uint32_t kBias[4] = {0xCC00CC00u, 0xD400D400u, 0xDC00DC00u, 0xE400E400u};   // -16, -64, -256, -1024
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)(Cfg::ACOL + 32 * q);
+    for (int i = 0; i < nst; ++i) {
+      const int s = i % NS, u = i / NS;
+      const uint32_t slot = (uint32_t)((i % PD) * Cfg::RAW_SLOT);
+      cp_async_wait_group<PD - 1>();  // this thread's copies of stage i have landed
+      const uint4 wv = lds128(my_w + slot);
+      uint4 xv[XV];
 #pragma unroll
-      for (int i = 0; i < Cfg::XCH; ++i) {
-        // chunk idx: token row idx>>3, chunk c = idx&7 = word c/2 of runs j0 = 2(c%2), j0+1;
-        // run j of the k-block is the block's bytes 16*half + 32j .. +15
-        const int idx = t + XP_THREADS * i;
-        const int c = idx & 7;
-        const uint32_t* xr =
-            reinterpret_cast<const uint32_t*>(st + W_ST + (idx >> 3) * Cfg::X_ROW + rb * 128 + half * 16);
-        const int j0 = (c & 1) * 2, xq_w = c >> 1;
-        xw[i][0] = idx < MP * 8 ? xr[j0 * 8 + xq_w] : 0u;
-        xw[i][1] = idx < MP * 8 ? xr[(j0 + 1) * 8 + xq_w] : 0u;
-      }
-      if (q == KB_ST - 1 || kbl == nkb - 1) {  // stage read to the end (values are in registers)
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&st_empty[s]);
-      }
-      {  // positions 16*wq .. 16*wq+15 of the k-block: chunks 2wq (pairs 0, 1) and 2wq+1 (2, 3)
-        const uint2 p0 = codes4_to_f16((word >> 6) & 0x03030303u);
-        const uint2 p1 = codes4_to_f16((word >> 4) & 0x03030303u);
-        const uint2 p2 = codes4_to_f16((word >> 2) & 0x03030303u);
-        const uint2 p3 = codes4_to_f16(word & 0x03030303u);
-        *reinterpret_cast<uint4*>(at + sw128(r, 2 * wq)) = make_uint4(p0.x, p0.y, p1.x, p1.y);
-        *reinterpret_cast<uint4*>(at + sw128(r, 2 * wq + 1)) = make_uint4(p2.x, p2.y, p3.x, p3.y);
+      for (int v = 0; v < XV; ++v) xv[v] = lds128(my_w + slot + (uint32_t)(WK_THREADS * 16 * (1 + v)));
+      if (u > 0 && !mbar_wait_warp(&empty_bar[s], (uint32_t)(u - 1) & 1u, &abort)) break;
+      tc_fence_after();
+      {  // weights: 4 words x 4 bit pairs -> 64 fp16 in 32 tensor-memory columns (pair j: 8j..8j+7)
+        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t a[32];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          const uint32_t wh = w[wi] >> 8;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            a[8 * j + 2 * wi] = hfma2_u32((w[wi] & kMask[j]) | 0x64006400u, kScale[j], kBias[j]);
+            a[8 * j + 2 * wi + 1] = hfma2_u32((wh & kMask[j]) | 0x64006400u, kScale[j], kBias[j]);
+          }
+        }
+        tmem_st_32x32b_x32(a_lane + (uint32_t)(s * A_COLS), a);
       }
 #pragma unroll
-      for (int i = 0; i < Cfg::XCH; ++i) {
-        const int idx = t + XP_THREADS * i;
-        if (idx < MP * 8) {
-          const uint2 lo = s8x4_to_f16(xw[i][0]), hi = s8x4_to_f16(xw[i][1]);
-          *reinterpret_cast<uint4*>(bt + sw128(idx >> 3, idx & 7)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      for (int v = 0; v < XV; ++v) {  // activations: 16 int8 (k = 16uu..) -> two chunks of row m
+        const int idx = t + WK_THREADS * v, m = idx >> 4, uu = idx & 15;
+        if (idx < MP * 16) {
+          const uint2 f0 = s8x4_to_f16_perm(xv[v].x), f1 = s8x4_to_f16_perm(xv[v].y);
+          const uint2 f2 = s8x4_to_f16_perm(xv[v].z), f3 = s8x4_to_f16_perm(xv[v].w);
+          // k = 16uu + e lies in block uu/8, half uu%2, bit pair (uu/2)%4: stage positions
+          // 64q' + 16j' + pe with q' = 2(uu/8) + uu%2, j' = (uu/2)%4
+          const int qq = ((uu >> 3) << 1) | (uu & 1), jj = (uu >> 1) & 3;
+          const uint32_t bt = bring + (uint32_t)(s * Cfg::B_STAGE + qq * Cfg::B_SUB);
+          sts128(bt + sw128(m, 2 * jj), f0.x, f0.y, f1.x, f1.y);
+          sts128(bt + sw128(m, 2 * jj + 1), f2.x, f2.y, f3.x, f3.y);
         }
       }
+      if (i + PD < nst) {  // refill this copy slot with stage i + PD (its bytes are in registers)
+        issue_w(i + PD);
+        issue_x(i + PD);
+      }
+      cp_async_commit();
+      tmem_st_wait();            // this thread's tensor-memory writes complete
       fence_proxy_async_smem();  // this thread's generic-proxy writes -> the tensor core's reads
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ab_full[a]);
+      if (lane == 0) mbar_arrive(&full_bar[s]);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may land after the CTA is gone
+  }
 
-    // ---- push this CTA's partial sums to the rows' owners in the cluster (8 warps) ----
-    if (warp < XP_WARP0 + 8 && mbar_wait_warp(&done_bar, 0, &abort)) {
-      tc_fence_after();
-      const int e = warp - XP_WARP0;         // 0..7 (the first 8 expander warps)
-      const int quarter = warp & 3;          // tensor-memory lanes this warp may read
-      const int row = quarter * 32 + lane;   // accumulator row = weight row within the tile
-      int owner = 0;
-      while (owner + 1 < cs && row_lo(owner + 1, cs) <= row) ++owner;
-      const int o_lo = row_lo(owner, cs), o_rows = row_lo(owner + 1, cs) - o_lo;
-      const uint32_t dst = smem_u32(recv) + (uint32_t)(((rank * o_rows + (row - o_lo)) * Cfg::PITCH) * 4);
-      const uint32_t dst_c = cs > 1 ? map_to_rank(dst, (uint32_t)owner) : dst;
-      const int c_lo = (e >> 2) * (MP / 2);  // two warps share a lane quarter: half the columns each
-      const int used = nkb * (KB / 16) < Cfg::NACC ? nkb * (KB / 16) : Cfg::NACC;  // accumulators written
-      // per accumulator, every 8-column piece of this warp's half is loaded before one wait
-      // (a wait after each piece serialised 32 round trips per warp at 64 tokens)
-      constexpr int H = MP / 2, HC = H / 8;
-      float sum[H];
+  // ---- epilogue: sum the accumulators; push rows owned by other cluster CTAs ----
+  const int quarter = warp & 3;             // tensor-memory lanes this warp may read
+  const int c0 = ((warp - 1) >> 2) * NC;    // this warp's columns (token rows)
+  int owner = 0;
+  while (owner + 1 < cs && row_lo(owner + 1, cs) <= row) ++owner;
+  const int o_lo = row_lo(owner, cs), o_rows = row_lo(owner + 1, cs) - o_lo;
+  float sum[NC];
 #pragma unroll
-      for (int i = 0; i < H; ++i) sum[i] = 0.f;
-      for (int j = 0; j < used; ++j) {
-        uint32_t v[HC][8];
+  for (int c = 0; c < NC; ++c) sum[c] = 0.f;
+  bool have = false;
+  if (warp >= 1 && mbar_wait_warp(&done_bar, 0, &abort)) {
+    tc_fence_after();
+    const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0;
 #pragma unroll
-        for (int cb = 0; cb < HC; ++cb)
-          tmem_ld_32x32b_x8(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * MP + c_lo + cb * 8), v[cb]);
-        tmem_ld_wait();
+    for (int j0 = 0; j0 < NACC; j0 += Cfg::LB) {
+      uint32_t v[Cfg::LB][NC];
 #pragma unroll
-        for (int cb = 0; cb < HC; ++cb)
+      for (int j = 0; j < Cfg::LB; ++j) tmem_ld_cols<NC>(tbase + (uint32_t)((j0 + j) * MP), v[j]);
+      tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) sum[cb * 8 + i] += __uint_as_float(v[cb][i]);  // integers < 2^24: exact
-      }
+      for (int j = 0; j < Cfg::LB; ++j)
 #pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const uint32_t addr = dst_c + (uint32_t)((c_lo + i) * 4);
-        if (cs > 1)
-          st_cluster_u32(addr, __float_as_uint(sum[i]));
-        else
-          st_shared_u32(addr, __float_as_uint(sum[i]));
-      }
+        for (int c = 0; c < NC; ++c) sum[c] += __uint_as_float(v[j][c]);  // integers < 2^24: exact
+    }
+    have = true;
+    if (owner != rank) {
+      const int slot = rank - (rank > owner ? 1 : 0);
+      const uint32_t dst = map_to_rank(recv + (uint32_t)(((slot * o_rows + (row - o_lo)) * Cfg::PITCH + c0) * 4),
+                                       (uint32_t)owner);
+#pragma unroll
+      for (int c = 0; c < NC; c += 4) st_cluster_v4(dst + (uint32_t)(c * 4), sum[c], sum[c + 1], sum[c + 2], sum[c + 3]);
     }
   }
 
-  // ---- every partial pushed; each CTA finishes its own rows ----
+  // ---- every partial pushed (and every tensor-memory access done); owners finish their rows ----
   tc_fence_before();
   if (cs > 1)
     cluster_sync_all();
   else
     __syncthreads();
-  if (warp >= XP_WARP0 && !abort) {
-    const int t = threadIdx.x - XP_WARP0 * 32;
-    const int lo = row_lo(rank, cs), rows = row_lo(rank + 1, cs) - lo;
-    // rows <= 128: thread t takes row t % 128 of the slice (if any) for tokens t/128, +4, ...
-    const int rl = t & (TW - 1);
-    const int n = n0 + lo + rl;
-    if (rl < rows && n < N) {
-      for (int m = t >> 7; m < M; m += XP_THREADS / TW) {
-        float sum = 0.0f;
-        for (int src = 0; src < cs; ++src) sum += recv[(src * rows + rl) * Cfg::PITCH + m];
-        const int a = __float2int_rn(sum) - tok_rs[m];
-        const int64_t o = (int64_t)m * N + n;
-        out[o] = __fmul_rn(__fdiv_rn(__int2float_rn(a), tok_s[m]), w_scale);
-        if (acc_out) acc_out[o] = a;
+  if (have && owner == rank && !abort) {
+    for (int slot = 0; slot < cs - 1; ++slot) {
+      const uint32_t src = recv + (uint32_t)(((slot * o_rows + (row - o_lo)) * Cfg::PITCH + c0) * 4);
+#pragma unroll
+      for (int c = 0; c < NC; c += 4) {
+        const float4 f = lds_f4(src + (uint32_t)(c * 4));
+        sum[c] += f.x;
+        sum[c + 1] += f.y;
+        sum[c + 2] += f.z;
+        sum[c + 3] += f.w;
+      }
+    }
+    const int n = n0 + row;
+    if (n < N) {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int m = c0 + c;
+        if (m < M) {
+          const int a = __float2int_rn(sum[c]) - __ldg(rowsum + m);
+          const int64_t o = (int64_t)m * N + n;
+          out[o] = __fmul_rn(__fdiv_rn(__int2float_rn(a), __ldg(act_scale + m)), w_scale);
+          if (acc_out) acc_out[o] = a;
+        }
       }
     }
   }
@@ -353,7 +449,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
     tc_fence_after();
     bool dummy = false;
     mbar_wait(&done_bar, 0, &dummy);
-    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -372,22 +468,23 @@ cudaError_t launch_mp(const int8_t* xq, const float* act_scale, const int32_t* r
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  // K split across a cluster so that all CTAs run at once, one per SM (the shared memory allows
-  // one): at most 8 CTAs per cluster, at least four 64-k blocks each. A cluster that cannot be
-  // resident with the others runs as a second wave and doubles the time. A cluster must fit in
-  // one GPC, so SMs / tiles overestimates the size that fits: with 20 tiles, 7-CTA clusters pack
-  // only two per GPC. The occupancy query decides, shrinking the cluster until every one fits.
+  // The stages are split across a cluster so that all CTAs run at once, one per SM (the shared
+  // memory allows one): at most 8 CTAs per cluster, at least one 256-k stage each. A cluster
+  // that cannot be resident with the others runs as a second wave and doubles the time. A
+  // cluster must fit in one GPC, so SMs / tiles overestimates the size that fits: with 20
+  // tiles, 7-CTA clusters pack only two per GPC. The occupancy query decides, shrinking the
+  // cluster until every one fits.
   const int64_t n_tiles = (N + TW - 1) / TW;
-  const int64_t nkb = K / KB;
+  const int64_t n_stages = (K / 128 + 1) / 2;
   int64_t cs = num_sms / n_tiles;
   if (cs > kMaxCluster) cs = kMaxCluster;
-  if (cs > nkb / 4) cs = nkb / 4;
+  if (cs > n_stages) cs = n_stages;
   if (cs < 1) cs = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.z = 1;
@@ -405,6 +502,11 @@ cudaError_t launch_mp(const int8_t* xq, const float* act_scale, const int32_t* r
   }
   attr[0].val.clusterDim.y = (unsigned)cs;
   cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs);
+  // weights stream in while the previous kernel finishes (the kernel waits for it before reading
+  // the activations or writing anything)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, gemm_smallm_kernel<MP>, xq, act_scale, rowsum, wp, w_scale, out, acc_out, (int)M,
                             (int)N, (int)K);
 }
