@@ -9,30 +9,35 @@
 //
 // Why this shape: with a handful of tokens the work is 2-bit weight streaming, but the dp4a
 // GEMV re-decodes every weight word once per token row it serves and runs out of issue slots
-// from M ~ 8 on. Here each weight is decoded exactly once, into fp16 in shared memory, and the
-// tensor core applies it to all tokens: D[n][m] += W[n][k] * X[m][k] with tcgen05.mma
-// kind::f16, M = 128 weight rows, N = MP (the token count rounded up to 16), K = 16.
+// from M ~ 8 on. Here each weight is decoded exactly once and the tensor core applies it to
+// all tokens: D[n][j] += W'[n][k] * B[j][k] with tcgen05.mma kind::f8f6f4 (e4m3 x e4m3, fp32
+// accumulate), M = 128 weight rows, K = 32.
 //
-// Stages. The K range is walked in stages of 256 k: two i2_s blocks, sixteen K = 16 MMAs.
+// Operands (all exact in e4m3). A tiny MMA costs the tensor pipe a fixed ~45 cycles whatever
+// its N, so the MMA count per weight byte is what bounds this kernel; the 8-bit kind takes
+// K = 32 per MMA, half the count of fp16.
+//  * weights: w' = 8 + code in {8..11}, the e4m3 byte 0x50 | code (one mask-and-or per four
+//    codes); k positions past the end of K hold 0x00 (w' = 0);
+//  * activations: u = x + 128 in [1, 255] is split into base-8 digits d0, d1 in [0, 7] and
+//    d2 in [0, 3], each stored as the e4m3 byte 0x50 | d (= 8 + d). B has NB = 3 MP + 16 rows:
+//    digit 0, 1 and 2 planes of the MP tokens, then 16 rows of 1.0 whose D column is the
+//    weight-row sum W' = sum_k w'.
+//  Then with D_i = sum_k w'_k (8 + d_ik): sum_k code_k x_k = D0 + 8 D1 + 64 D2 - 712 W' - 8 rowsum
+//  (sum w' u = sum_i 8^i (D_i - 8 W'), and sum (w' - 8)(u - 128) over the K positions), so
+//  acc = raw - rowsum = (D0 + 8 D1 + 64 D2 - 712 W') - 9 rowsum. Every D_i <= 11 * 15 * K < 2^24
+//  for K <= 32768, so the fp32 accumulators hold exact integers; the combination is integer.
+//
+// Stages. The K range is walked in stages of 256 k: two i2_s blocks, eight K = 32 MMAs.
 // Synchronisation is per stage: one wait, one fence and one barrier arrival per warp cover 256 k.
-//
-// Operands. The decoded weights (A, 128 rows x 256 k of fp16 per stage) are written straight
-// into tensor memory with tcgen05.st, and the MMA reads A from there; only the activations (B,
-// MP rows) go through shared memory. A weight stage is 64 KB of fp16 against 8 KB of packed
-// input: staged through shared memory it would be written and read back by the tensor core,
-// 128 KB of shared-memory traffic per stage, more than the stage's arithmetic takes.
+// The decoded weights (A, 128 rows x 256 k) are written straight into tensor memory with
+// tcgen05.st and the MMA reads A from there; only the activation digits (B) go through shared
+// memory.
 //
 // K order. Inside an i2_s block byte g holds the codes of k = g + 32j at bit pair j (j = 0 at
 // bits 7:6), so the 16 bytes 16h..16h+15 of block b hold, for each j, the 16 consecutive
-// k = 128b + 32j + 16h + e of the stage. Stage position p = 64q + 16j + pe (q = 2b + h) holds that
-// k, where pe runs over e in the order 0, 2, 1, 3 inside each group of four: two codes per fp16
-// pair come from bytes 0 and 2 (or 1 and 3) of one word under one mask, and the activations'
-// byte permute applies the same order at no cost. The dot product only needs both operands to
-// agree.
-//
-// Decoding (exact): (word & (3 << sh, in bytes 0 and 2)) | 0x6400 in each half is the fp16
-// 1024 + c * 2^sh; one fma by 2^-sh and -1024 * 2^-sh gives c in {0, 1, 2, 3}. An int8 x becomes
-// 1024 + (x + 128) by a byte permute under 0x64, minus 1152.
+// k = 128b + 32j + 16h + e of the stage. Stage position p = 64q + 16j + e (q = 2b + h) holds
+// that k: a thread's 16 bytes give 16 tensor-memory columns of 4 positions each, and a
+// 16-byte piece of activations (16 consecutive k) is one 16-byte chunk of each digit row.
 //
 // Structure (one CTA per 128 weight rows and a range of stages; a thread-block cluster of up to
 // 8 CTAs splits the stages):
@@ -41,20 +46,16 @@
 //    16 weight bytes and up to two 16-byte pieces of the stage's int8 activations with
 //    cp.async into a private ring of PD stages in shared memory (one commit group per stage, so
 //    PD stages are in flight without tying up registers; the weights of the first stages are
-//    requested before waiting for the previous kernel). Per stage it decodes its bytes into 32
-//    tensor-memory columns of the stage's A slot, writes its activation pieces into the
+//    requested before waiting for the previous kernel). Per stage it decodes its bytes into 16
+//    tensor-memory columns of the stage's A slot, writes its activation digits into the
 //    128-byte-swizzled K-major B tile, fences, and its warp arrives once;
-//  * warp 0: allocates tensor memory; one lane issues the MMAs, rotating over NACC independent
-//    128 x MP fp32 accumulators (tiny MMAs into one accumulator would wait on each other), and
-//    commits one release of the slot per stage;
+//  * warp 0: allocates tensor memory; one lane issues the MMAs into NACC accumulators of NB
+//    columns and commits one release of the slot per stage;
 //  * epilogue: each worker warp reads 32 accumulator rows (its tensor-memory lane quarter) and
-//    a quarter of the columns, adds the NACC accumulators, and either keeps the sums (rows its
-//    CTA owns) or stores them as 16-byte pieces into the shared memory of the cluster CTA that
-//    owns those rows; after one cluster barrier the owners add what they received and write
-//    the outputs.
-// Exactness: every operand is a small integer fp16 holds exactly, and every partial and total
-// sum is an integer of magnitude <= 3 * 127 * K < 2^24 for K <= 32768, so the fp32
-// accumulations and the cross-CTA sums are exact.
+//    a quarter of the tokens, forms the integer partial D0 + 8 D1 + 64 D2 - 712 W', and either
+//    keeps it (rows its CTA owns) or stores it as 16-byte pieces into the shared memory of the
+//    cluster CTA that owns those rows; after one cluster barrier the owners add what they
+//    received and write the outputs.
 // Every mbarrier wait is bounded; a timeout is recorded in the device error word.
 #include "bitnet_dev.cuh"
 
@@ -67,13 +68,13 @@ namespace {
 
 constexpr int TW = 128;                    // weight rows per CTA (the MMA's M)
 constexpr int SK = 256;                    // k per stage (two i2_s blocks)
-constexpr int KSTEPS = SK / 16;            // K = 16 MMAs per stage
+constexpr int KSTEPS = SK / 32;            // K = 32 MMAs per stage
 constexpr int WK_WARPS = 16;               // workers
 constexpr int WK_THREADS = WK_WARPS * 32;  // four per weight row
 constexpr int THREADS = 32 + WK_THREADS;
 constexpr int kMaxCluster = 8;
 constexpr uint32_t TMEM_COLS = 512;        // accumulators, then the A stages (one CTA per SM)
-constexpr int A_COLS = SK / 2;             // tensor-memory columns of one fp16 A stage
+constexpr int A_COLS = SK / 4;             // tensor-memory columns of one e4m3 A stage
 
 // rows [row_lo(r), row_lo(r + 1)) of the tile are finished by cluster rank r
 __host__ __device__ constexpr int row_lo(int r, int cs) { return TW * r / cs; }
@@ -92,22 +93,23 @@ constexpr int max_recv_rows() {
 template <int MP>
 struct SmallCfg {
   static_assert(MP % 16 == 0 && MP >= 16 && MP <= 64, "tokens per MMA: a multiple of 16, at most 64");
-  static constexpr int NACC = MP <= 32 ? 8 : 4;                   // independent accumulators
-  static constexpr int ACOL = (NACC * MP + 127) / 128 * 128;       // first A column in tensor memory
-  static constexpr int NS = (int)(TMEM_COLS - ACOL) / A_COLS;      // A/B stages (tensor memory bound)
-  static constexpr int B_SUB = MP * 128;                           // fp16 activations, 64 k x MP rows
-  static constexpr int B_STAGE = 4 * B_SUB;
+  static constexpr int NB = 3 * MP + 16;                          // B rows: 3 digit planes, 16 rows of ones
+  static constexpr int ONES = 3 * MP;                             // the ones row
+  static constexpr int NACC = 2 * NB <= 256 ? 2 : 1;              // accumulators
+  static constexpr int ACOL = (NACC * NB + 63) / 64 * 64;         // first A column in tensor memory
+  static constexpr int NS = MP <= 32 ? 4 : (MP <= 48 ? 3 : 2);    // A/B stages
+  static constexpr int B_SUB = NB * 128;                          // e4m3 digits, 128 k x NB rows
+  static constexpr int B_STAGE = 2 * B_SUB;
   static constexpr int XV = (MP * 16 + WK_THREADS - 1) / WK_THREADS;  // 16-byte activation pieces per thread
-  static constexpr int PD = MP <= 32 ? 6 : 5;                      // staged input stages in flight
+  static constexpr int PD = MP <= 16 ? 6 : (MP <= 32 ? 5 : 3);    // staged input stages in flight
   static constexpr int RAW_SLOT = WK_THREADS * 16 * (1 + XV);      // one stage's copies, 16 bytes per thread each
-  static constexpr int NC = MP / 4;                                // accumulator columns per epilogue warp
-  static constexpr int PITCH = MP + 4;                             // floats per received row (16-byte rows)
+  static constexpr int NC = MP / 4;                                // tokens per epilogue warp
+  static constexpr int PITCH = MP + 4;                             // int32 per received row (16-byte rows)
   static constexpr int RECV_ROWS = max_recv_rows();
   static constexpr int SMEM = 1024 + NS * B_STAGE + PD * RAW_SLOT + RECV_ROWS * PITCH * 4;
-  static constexpr uint32_t IDESC = make_idesc_f16_f32(TW, MP);
-  // accumulators read per tensor-memory wait in the epilogue (registers: LB * NC)
-  static constexpr int LB = NACC * NC <= 64 ? NACC : NACC / 2;
-  static_assert(NS >= 2 && ACOL + NS * A_COLS <= (int)TMEM_COLS, "tensor memory columns");
+  static constexpr uint32_t IDESC = make_idesc_f16_f32(TW, NB);   // e4m3 x e4m3 has format code 0 like f16
+  static_assert(NB % 16 == 0 && NB <= 256, "MMA N");
+  static_assert(ACOL + NS * A_COLS <= (int)TMEM_COLS, "tensor memory columns");
   static_assert(B_SUB % 1024 == 0, "1024-byte aligned tiles");
   static_assert(SMEM <= 227 * 1024 - 256, "shared memory (static barriers included)");
 };
@@ -119,23 +121,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
-                            *reinterpret_cast<const __half2*>(&c));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// 4 int8 (bytes 0..3) -> fp16 pairs (byte 0, byte 2) and (byte 1, byte 3), exact
-__device__ __forceinline__ uint2 s8x4_to_f16_perm(uint32_t w) {
-  const uint32_t u = w ^ 0x80808080u;
-  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4240);
-  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4341);
-  const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480), __ushort_as_half((unsigned short)0x6480));
-  const __half2 rl = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
-  const __half2 rh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
-  return make_uint2(*reinterpret_cast<const uint32_t*>(&rl), *reinterpret_cast<const uint32_t*>(&rh));
 }
 
 // byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile
@@ -156,36 +141,35 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   return v;
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is 128 lanes (rows) x 8 columns (16 fp16
-// along K, two per column, the lower k in the low half).
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f8f6f4: A is 128 lanes (rows) x 8 columns (32
+// e4m3 along K, four per column, the lowest k in the low byte).
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp writes lane (base + t).
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp writes lane (base + t).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x NC consecutive 32-bit columns (NC = 4, 8, 12 or 16) into r[0..NC)
+// 32 lanes x NC consecutive 32-bit columns (NC = 1, 4, 8, 12 or 16) into r[0..NC)
 template <int NC>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
-  if constexpr (NC == 4) {
+  if constexpr (NC == 1) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));
+  } else if constexpr (NC == 4) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr));
@@ -197,7 +181,7 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
     tmem_ld_cols<8>(taddr, r);
     tmem_ld_cols<4>(taddr + 8, r + 8);
   } else {
-    static_assert(NC == 16, "4, 8, 12 or 16 columns");
+    static_assert(NC == 16, "1, 4, 8, 12 or 16 columns");
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
@@ -214,7 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
                                                                  float* __restrict__ out, int32_t* __restrict__ acc_out,
                                                                  int M, int N, int K) {
   using Cfg = SmallCfg<MP>;
-  constexpr int NS = Cfg::NS, XV = Cfg::XV, NC = Cfg::NC, PD = Cfg::PD, NACC = Cfg::NACC;
+  constexpr int NS = Cfg::NS, XV = Cfg::XV, NC = Cfg::NC, PD = Cfg::PD, NACC = Cfg::NACC, NB = Cfg::NB;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NS];   // a stage's operands written (one arrival per worker warp)
   __shared__ __align__(8) uint64_t empty_bar[NS];  // the MMAs reading a stage slot are done (one commit)
@@ -287,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
     // ================================ MMA issuer ================================
     if (lane == 0) {
       // The issuing thread's own arithmetic is on the critical path: a tiny MMA occupies the
-      // tensor pipe for only ~50 cycles, so each issue here is a few integer adds to
+      // tensor pipe for only ~45 cycles, so each issue here is a few integer adds to
       // descriptors built once (the address field is the low 14 bits; offsets never carry).
       const uint64_t bdesc0 = make_sw128_kmajor_desc(bring);
       const uint32_t acol0 = tmem + (uint32_t)Cfg::ACOL;
@@ -301,9 +285,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
         const uint32_t first = i > 0 ? 1u : 0u;  // accumulate unless this is an accumulator's first MMA
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks)
-          mma_f16_ts(tmem + (uint32_t)((ks % NACC) * MP), a_col + (uint32_t)(8 * ks),
-                     bd + (uint64_t)(((ks >> 2) * Cfg::B_SUB + (ks & 3) * 32) >> 4), Cfg::IDESC,
-                     ks >= NACC ? 1u : first);
+          mma_f8_ts(tmem + (uint32_t)((ks % NACC) * NB), a_col + (uint32_t)(8 * ks),
+                    bd + (uint64_t)(((ks >> 2) * Cfg::B_SUB + (ks & 3) * 32) >> 4), Cfg::IDESC,
+                    ks >= NACC ? 1u : first);
         mma_commit(&empty_bar[s]);
         if (++s == NS) {
           s = 0;
@@ -314,17 +298,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
     }
   } else {
     // ================================ workers ================================
+    // the 16 rows of ones (e4m3 1.0 = 0x38) of every B slot; they never change, and each
+    // thread's writes are fenced before its warp's first arrival like every tile write
+    for (int o = 16 * t; o < NS * 2 * 16 * 128; o += 16 * WK_THREADS) {
+      const int slot = o / (2 * 16 * 128), sub = (o / (16 * 128)) & 1, off = o % (16 * 128);
+      sts128(bring + (uint32_t)(slot * Cfg::B_STAGE + sub * Cfg::B_SUB + Cfg::ONES * 128 + off), 0x38383838u,
+             0x38383838u, 0x38383838u, 0x38383838u);
+    }
     pdl_wait();  // the activations may be the previous kernel's output
 #pragma unroll 1
     for (int p = 0; p < PD; ++p) {  // one commit group per stage (the first also holds the weights)
       if (p < nst) issue_x(p);
       cp_async_commit();
     }
-    // per bit pair j (shift sh = 6 - 2j): mask, and the fma's scale 2^-sh and bias -1024 * 2^-sh
-    const uint32_t kMask[4] = {0x00C000C0u, 0x00300030u, 0x000C000Cu, 0x00030003u};
-    const uint32_t kScale[4] = {0x24002400u, 0x2C002C00u, 0x34003400u, 0x3C003C00u};  // 2^-6, 2^-4, 2^-2, 1
-    const uint32_t kBias[4] = {0xCC00CC00u, 0xD400D400u, 0xDC00DC00u, 0xE400E400u};   // -16, -64, -256, -1024
-    const uint32_t a_lane = tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)(Cfg::ACOL + 32 * q);
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)(Cfg::ACOL + 16 * q);
     for (int i = 0; i < nst; ++i) {
       const int s = i % NS, u = i / NS;
       const uint32_t slot = (uint32_t)((i % PD) * Cfg::RAW_SLOT);
@@ -335,32 +322,37 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       for (int v = 0; v < XV; ++v) xv[v] = lds128(my_w + slot + (uint32_t)(WK_THREADS * 16 * (1 + v)));
       if (u > 0 && !mbar_wait_warp(&empty_bar[s], (uint32_t)(u - 1) & 1u, &abort)) break;
       tc_fence_after();
-      {  // weights: 4 words x 4 bit pairs -> 64 fp16 in 32 tensor-memory columns (pair j: 8j..8j+7)
+      {  // weights: 4 words x 4 bit pairs -> 64 e4m3 w' in 16 tensor-memory columns (pair j: 4j..4j+3)
+        const bool blk_ok = 2 * (st_lo + i) + qb < nblk;  // past the end of K: w' = 0
         const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-        uint32_t a[32];
+        uint32_t a[16];
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          const uint32_t wh = w[wi] >> 8;
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            a[8 * j + 2 * wi] = hfma2_u32((w[wi] & kMask[j]) | 0x64006400u, kScale[j], kBias[j]);
-            a[8 * j + 2 * wi + 1] = hfma2_u32((wh & kMask[j]) | 0x64006400u, kScale[j], kBias[j]);
-          }
-        }
-        tmem_st_32x32b_x32(a_lane + (uint32_t)(s * A_COLS), a);
+          for (int wi = 0; wi < 4; ++wi)
+            a[4 * j + wi] = blk_ok ? ((w[wi] >> (6 - 2 * j)) & 0x03030303u) | 0x50505050u : 0u;
+        tmem_st_32x32b_x16(a_lane + (uint32_t)(s * A_COLS), a);
       }
 #pragma unroll
-      for (int v = 0; v < XV; ++v) {  // activations: 16 int8 (k = 16uu..) -> two chunks of row m
+      for (int v = 0; v < XV; ++v) {  // activations: 16 int8 (k = 16uu..) -> one chunk of each digit row
         const int idx = t + WK_THREADS * v, m = idx >> 4, uu = idx & 15;
         if (idx < MP * 16) {
-          const uint2 f0 = s8x4_to_f16_perm(xv[v].x), f1 = s8x4_to_f16_perm(xv[v].y);
-          const uint2 f2 = s8x4_to_f16_perm(xv[v].z), f3 = s8x4_to_f16_perm(xv[v].w);
+          const uint32_t x4[4] = {xv[v].x ^ 0x80808080u, xv[v].y ^ 0x80808080u, xv[v].z ^ 0x80808080u,
+                                  xv[v].w ^ 0x80808080u};  // u = x + 128, per byte
+          uint32_t d[3][4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            d[0][e] = (x4[e] & 0x07070707u) | 0x50505050u;
+            d[1][e] = ((x4[e] >> 3) & 0x07070707u) | 0x50505050u;
+            d[2][e] = ((x4[e] >> 6) & 0x03030303u) | 0x50505050u;
+          }
           // k = 16uu + e lies in block uu/8, half uu%2, bit pair (uu/2)%4: stage positions
-          // 64q' + 16j' + pe with q' = 2(uu/8) + uu%2, j' = (uu/2)%4
-          const int qq = ((uu >> 3) << 1) | (uu & 1), jj = (uu >> 1) & 3;
-          const uint32_t bt = bring + (uint32_t)(s * Cfg::B_STAGE + qq * Cfg::B_SUB);
-          sts128(bt + sw128(m, 2 * jj), f0.x, f0.y, f1.x, f1.y);
-          sts128(bt + sw128(m, 2 * jj + 1), f2.x, f2.y, f3.x, f3.y);
+          // 64(2(uu/8) + uu%2) + 16((uu/2)%4) + e, i.e. sub-tile uu/8, chunk 4(uu%2) + (uu/2)%4
+          const int chunk = 4 * (uu & 1) + ((uu >> 1) & 3);
+          const uint32_t bt = bring + (uint32_t)(s * Cfg::B_STAGE + (uu >> 3) * Cfg::B_SUB);
+#pragma unroll
+          for (int dg = 0; dg < 3; ++dg)
+            sts128(bt + sw128(dg * MP + m, chunk), d[dg][0], d[dg][1], d[dg][2], d[dg][3]);
         }
       }
       if (i + PD < nst) {  // refill this copy slot with stage i + PD (its bytes are in registers)
@@ -377,29 +369,40 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
     asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may land after the CTA is gone
   }
 
-  // ---- epilogue: sum the accumulators; push rows owned by other cluster CTAs ----
+  // ---- epilogue: integer partials per (row, token); push rows owned by other cluster CTAs ----
   const int quarter = warp & 3;             // tensor-memory lanes this warp may read
-  const int c0 = ((warp - 1) >> 2) * NC;    // this warp's columns (token rows)
+  const int c0 = ((warp - 1) >> 2) * NC;    // this warp's tokens
   int owner = 0;
   while (owner + 1 < cs && row_lo(owner + 1, cs) <= row) ++owner;
   const int o_lo = row_lo(owner, cs), o_rows = row_lo(owner + 1, cs) - o_lo;
-  float sum[NC];
+  int part[NC];
 #pragma unroll
-  for (int c = 0; c < NC; ++c) sum[c] = 0.f;
+  for (int c = 0; c < NC; ++c) part[c] = 0;
   bool have = false;
   if (warp >= 1 && mbar_wait_warp(&done_bar, 0, &abort)) {
     tc_fence_after();
-    const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0;
+    const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint32_t v[NACC][3][NC], w1[NACC][1];
 #pragma unroll
-    for (int j0 = 0; j0 < NACC; j0 += Cfg::LB) {
-      uint32_t v[Cfg::LB][NC];
+    for (int j = 0; j < NACC; ++j) {
 #pragma unroll
-      for (int j = 0; j < Cfg::LB; ++j) tmem_ld_cols<NC>(tbase + (uint32_t)((j0 + j) * MP), v[j]);
-      tmem_ld_wait();
+      for (int dg = 0; dg < 3; ++dg) tmem_ld_cols<NC>(tbase + (uint32_t)(j * NB + dg * MP + c0), v[j][dg]);
+      tmem_ld_cols<1>(tbase + (uint32_t)(j * NB + Cfg::ONES), w1[j]);
+    }
+    tmem_ld_wait();
+    // every accumulator value is an integer below 2^24, so the fp32 sums and conversions are exact
+    float wsum = 0.f;
 #pragma unroll
-      for (int j = 0; j < Cfg::LB; ++j)
+    for (int j = 0; j < NACC; ++j) wsum += __uint_as_float(w1[j][0]);
+    const int wprime = __float2int_rn(wsum);
 #pragma unroll
-        for (int c = 0; c < NC; ++c) sum[c] += __uint_as_float(v[j][c]);  // integers < 2^24: exact
+    for (int c = 0; c < NC; ++c) {
+      float dsum[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < NACC; ++j)
+#pragma unroll
+        for (int dg = 0; dg < 3; ++dg) dsum[dg] += __uint_as_float(v[j][dg][c]);
+      part[c] = __float2int_rn(dsum[0]) + 8 * __float2int_rn(dsum[1]) + 64 * __float2int_rn(dsum[2]) - 712 * wprime;
     }
     have = true;
     if (owner != rank) {
@@ -407,7 +410,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       const uint32_t dst = map_to_rank(recv + (uint32_t)(((slot * o_rows + (row - o_lo)) * Cfg::PITCH + c0) * 4),
                                        (uint32_t)owner);
 #pragma unroll
-      for (int c = 0; c < NC; c += 4) st_cluster_v4(dst + (uint32_t)(c * 4), sum[c], sum[c + 1], sum[c + 2], sum[c + 3]);
+      for (int c = 0; c < NC; c += 4)
+        st_cluster_v4(dst + (uint32_t)(c * 4), __int_as_float(part[c]), __int_as_float(part[c + 1]),
+                      __int_as_float(part[c + 2]), __int_as_float(part[c + 3]));
     }
   }
 
@@ -423,10 +428,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
 #pragma unroll
       for (int c = 0; c < NC; c += 4) {
         const float4 f = lds_f4(src + (uint32_t)(c * 4));
-        sum[c] += f.x;
-        sum[c + 1] += f.y;
-        sum[c + 2] += f.z;
-        sum[c + 3] += f.w;
+        part[c] += __float_as_int(f.x);
+        part[c + 1] += __float_as_int(f.y);
+        part[c + 2] += __float_as_int(f.z);
+        part[c + 3] += __float_as_int(f.w);
       }
     }
     const int n = n0 + row;
@@ -435,7 +440,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       for (int c = 0; c < NC; ++c) {
         const int m = c0 + c;
         if (m < M) {
-          const int a = __float2int_rn(sum[c]) - __ldg(rowsum + m);
+          const int a = part[c] - 9 * __ldg(rowsum + m);  // raw = part - 8 rowsum; acc = raw - rowsum
           const int64_t o = (int64_t)m * N + n;
           out[o] = __fmul_rn(__fdiv_rn(__int2float_rn(a), __ldg(act_scale + m)), w_scale);
           if (acc_out) acc_out[o] = a;
