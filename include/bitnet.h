@@ -68,7 +68,7 @@ extern "C" {
 #define BITNET_QW_SIGN 1    /* q = 0 where |w| < 1e-6, else sign(w); scale = max|w|       */
 
 /* ---- matmul kernel selection (bitnet_i2s_matmul_algo) ---- */
-#define BITNET_ALGO_AUTO 0   /* GEMV for a few rows (M < 9 when K >= 4096, else M < 12),
+#define BITNET_ALGO_AUTO 0   /* GEMV for a few rows (M < 5, or M < 3 when K > 10240),
                                 the few-token kernel up to M = 64, GEMM beyond         */
 #define BITNET_ALGO_GEMV 1   /* force the dp4a decode GEMV (any M)                   */
 #define BITNET_ALGO_GEMM 2   /* force the tcgen05 tensor-core GEMM (any M)           */
@@ -131,13 +131,13 @@ BITNET_API int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, 
  *   xq and wp must be 16-byte aligned; out and acc_out 4-byte aligned.
  *   The 2-bit field value 3 never comes out of bitnet_pack_i2s; if present it is used
  *   arithmetically (3 - 1 = +2), the same rule as the unpacking of [DeepDive] §8.
- *   Kernel choice: for a few rows (M < 9 when K >= 4096, M < 12 otherwise) a dp4a GEMV
- *   streams the packed weights. From there up to M = 64 a few-token tcgen05 kernel decodes
- *   each weight once into fp16 for all token rows
- *   (weights as the MMA's M, K split over a thread-block cluster). For larger M a tcgen05
- *   tile GEMM expands the codes in shared memory. The tensor-core paths are exact: every
- *   partial sum is an integer below 2^24 accumulated in fp32. All give bit-identical
- *   results.
+ *   Kernel choice: for a few rows (M < 5, or M < 3 when K > 10240) a dp4a GEMV streams the
+ *   packed weights. From there up to M = 64 a few-token tcgen05 kernel decodes each weight
+ *   once, as the e4m3 value code + 8, for all token rows, whose int8 values enter as three
+ *   exact e4m3 base-8 digits (weights as the MMA's M, K split over a thread-block cluster).
+ *   For larger M a tcgen05 tile GEMM expands the codes to fp16 in shared memory. The
+ *   tensor-core paths are exact: every partial sum is an integer below 2^24 accumulated in
+ *   fp32. All give bit-identical results.
  */
 BITNET_API int bitnet_i2s_matmul(const int8_t *xq, const float *act_scale, const int32_t *rowsum,
                                  const uint8_t *wp, float w_scale, float *out, int32_t *acc_out,

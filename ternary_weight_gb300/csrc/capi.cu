@@ -21,12 +21,13 @@ constexpr int64_t kMaxK = 1 << 16;          // staged activation rows must fit s
 constexpr int64_t kMaxKTensorCore = 1 << 15; // exact fp32 accumulation bound of the GEMM
 constexpr int64_t kGemvMaxM = 64;           // auto dispatch: GEMV or few-token kernel up to here, GEMM above
 // auto dispatch: the few-token tensor-core kernel from this many rows on. The dp4a GEMV's cost
-// grows with the rows (every weight word is decoded once per row); the tensor-core kernel's
-// barely does. Measured crossovers on the 2B-4T shapes: K = 6912 (N 2560) ties at 8 rows and
-// the tensor-core kernel wins from 9 (16 rows: 16.2 against 24.2 us); K = 2560 (N 6912) the
-// GEMV wins up to 8 (9.9 against 15.4 us) and loses from 12 (17.4 against 15.6 us).
-constexpr int64_t kSmallmMinMLongK = 9;      // K >= 4096
-constexpr int64_t kSmallmMinM = 12;          // shorter rows
+// grows with the rows (every weight word is decoded once per row); the tensor-core kernel's is
+// flat up to 16 rows. Measured (N x K = 6912 x 2560, 2560 x 6912, 2560 x 2560, 28672 x 8192):
+// the persistent few-row GEMV (K <= 10240) wins up to 4 rows (4 rows: 6.2 against 7.6 us at
+// 6912 x 2560) and loses from 5 (9.2 against 7.6 us; 9 rows 16.9 against 7.6). Past K = 10240
+// the plain GEMV takes over and loses from 3 rows (8192 x 28672: 48.4 against 39.5 us).
+constexpr int64_t kSmallmMinM = 5;           // K <= 10240
+constexpr int64_t kSmallmMinMLongK = 3;      // K > 10240
 
 // per-device: 0 = unchecked, 1 = sm_103 ok, -1 = unsupported; and SM count
 std::atomic<int> g_dev_state[kMaxDevices];
@@ -128,9 +129,9 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
     return BITNET_EALIGN;
   if (algo == BITNET_ALGO_AUTO) {
     // dp4a GEMV for a few tokens (it decodes each weight word once per token row, cheap while
-    // the rows are few); the few-token tensor-core kernel from 9 or 12 rows to 64 (each weight
-    // decoded once for all rows); the tile GEMM beyond
-    const int64_t smallm_from = K >= 4096 ? kSmallmMinMLongK : kSmallmMinM;
+    // the rows are few); the few-token tensor-core kernel from 5 rows (3 past K = 10240) to 64
+    // (each weight decoded once for all rows); the tile GEMM beyond
+    const int64_t smallm_from = K > 10240 ? kSmallmMinMLongK : kSmallmMinM;
     if (K > kMaxKTensorCore || M < smallm_from)
       algo = BITNET_ALGO_GEMV;
     else if (M <= kGemvMaxM)

@@ -796,12 +796,12 @@ def test_sweep_plan_matches_group_calls_on_the_decode_layer():
 # ----------------------------------------------------------------------------- few token rows
 
 ROWS_CASES = [
-    # (M, N, K) through auto dispatch: both sides of the GEMV / few-token crossover (8-9 rows at
-    # long K, 11-12 at short), the 2B-4T shapes, a ragged 32-lane layout (K 6912), the 2-lane
-    # layout (K 384), the largest K of the GEMV's staged path, and fewer rows than SMs
-    (2, 6912, 2560), (3, 2560, 6912), (4, 640, 2560), (5, 7, 384), (8, 2560, 6912), (9, 2560, 6912),
-    (11, 6912, 2560), (12, 6912, 2560), (16, 2560, 6912), (16, 300, 10240), (13, 1000, 1152),
-    (2, 152, 128), (16, 1, 256),
+    # (M, N, K) through auto dispatch: both sides of the GEMV / few-token crossover (4-5 rows up
+    # to K = 10240, 2-3 rows beyond), the 2B-4T shapes, a ragged 32-lane layout (K 6912), the
+    # 2-lane layout (K 384), the largest K of the GEMV's staged path, and fewer rows than SMs
+    (2, 6912, 2560), (3, 2560, 6912), (4, 640, 2560), (5, 7, 384), (5, 2560, 6912), (8, 2560, 6912),
+    (9, 2560, 6912), (11, 6912, 2560), (12, 6912, 2560), (16, 2560, 6912), (16, 300, 10240),
+    (13, 1000, 1152), (2, 152, 128), (16, 1, 256), (2, 300, 12288), (3, 300, 12288),
 ]
 
 
