@@ -53,9 +53,11 @@
 //    columns and commits one release of the slot per stage;
 //  * epilogue: each worker warp reads 32 accumulator rows (its tensor-memory lane quarter) and
 //    a quarter of the tokens, forms the integer partial D0 + 8 D1 + 64 D2 - 712 W', and either
-//    keeps it (rows its CTA owns) or stores it as 16-byte pieces into the shared memory of the
-//    cluster CTA that owns those rows; after one cluster barrier the owners add what they
-//    received and write the outputs.
+//    keeps it (rows its CTA owns) or sends it with st.async (16-byte pieces) into the shared
+//    memory of the cluster CTA that owns those rows, counted in bytes on that CTA's receive
+//    barrier; each owner waits for exactly its expected bytes, adds them and writes the
+//    outputs. (A cluster barrier after plain remote stores cost 0.7-1 us: its release waits
+//    for every remote store to be acknowledged.)
 // Every mbarrier wait is bounded; a timeout is recorded in the device error word.
 #include "bitnet_dev.cuh"
 
@@ -131,10 +133,18 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d)
+// 16 bytes into a peer CTA's shared memory; on arrival they count as completed transaction bytes
+// on the peer's mbarrier (both addresses in the shared::cluster window of that CTA)
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, int a, int b, int c, int d, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+                   cluster_addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
                : "memory");
 }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
@@ -203,6 +213,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
   __shared__ __align__(8) uint64_t full_bar[NS];   // a stage's operands written (one arrival per worker warp)
   __shared__ __align__(8) uint64_t empty_bar[NS];  // the MMAs reading a stage slot are done (one commit)
   __shared__ __align__(8) uint64_t done_bar;       // every MMA complete
+  __shared__ __align__(8) uint64_t recv_bar;       // the partials of this CTA's rows from its peers (bytes)
   __shared__ uint32_t tmem_slot;
 
   pdl_launch_dependents();
@@ -255,7 +266,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&done_bar, 1);
+    mbar_init(&recv_bar, 1);
     fence_mbar_init();
+    if (cs > 1)  // every peer sends its partials of this CTA's rows: 4 bytes per row and token
+      mbar_arrive_expect_tx(&recv_bar, (uint32_t)((cs - 1) * (row_lo(rank + 1, cs) - row_lo(rank, cs)) * MP * 4));
   }
   if (warp == 0) {
     tmem_alloc(&tmem_slot, TMEM_COLS);
@@ -264,6 +278,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (cs > 1) cluster_arrive_relaxed();  // this CTA's barriers exist (waited on before the first send)
   const uint32_t tmem = tmem_slot;
   bool abort = false;
 
@@ -405,24 +420,24 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       part[c] = __float2int_rn(dsum[0]) + 8 * __float2int_rn(dsum[1]) + 64 * __float2int_rn(dsum[2]) - 712 * wprime;
     }
     have = true;
-    if (owner != rank) {
+  }
+  if (cs > 1) {
+    cluster_wait();  // every peer's receive barrier is initialised and armed
+    if (have && owner != rank) {
       const int slot = rank - (rank > owner ? 1 : 0);
       const uint32_t dst = map_to_rank(recv + (uint32_t)(((slot * o_rows + (row - o_lo)) * Cfg::PITCH + c0) * 4),
                                        (uint32_t)owner);
+      const uint32_t bar = map_to_rank(smem_u32(&recv_bar), (uint32_t)owner);
 #pragma unroll
       for (int c = 0; c < NC; c += 4)
-        st_cluster_v4(dst + (uint32_t)(c * 4), __int_as_float(part[c]), __int_as_float(part[c + 1]),
-                      __int_as_float(part[c + 2]), __int_as_float(part[c + 3]));
+        st_async_v4(dst + (uint32_t)(c * 4), part[c], part[c + 1], part[c + 2], part[c + 3], bar);
     }
   }
 
-  // ---- every partial pushed (and every tensor-memory access done); owners finish their rows ----
+  // ---- every tensor-memory access done; owners wait for their peers' partials and finish ----
   tc_fence_before();
-  if (cs > 1)
-    cluster_sync_all();
-  else
-    __syncthreads();
-  if (have && owner == rank && !abort) {
+  __syncthreads();
+  if (have && owner == rank && !abort && (cs == 1 || mbar_wait(&recv_bar, 0, &abort))) {
     for (int slot = 0; slot < cs - 1; ++slot) {
       const uint32_t src = recv + (uint32_t)(((slot * o_rows + (row - o_lo)) * Cfg::PITCH + c0) * 4);
 #pragma unroll
@@ -449,7 +464,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
     }
   }
 
-  // ---- teardown: every MMA complete before the tensor memory is freed ----
+  // ---- teardown: every MMA complete before the tensor memory is freed; and no peer may still be
+  // sending into this CTA's shared memory when it exits (the owners waited for every byte unless a
+  // wait gave up, so this bounded wait only matters on that path) ----
+  if (cs > 1 && threadIdx.x == 32) {
+    bool dummy = false;
+    mbar_wait(&recv_bar, 0, &dummy);
+  }
   if (warp == 0) {
     tc_fence_after();
     bool dummy = false;
