@@ -442,7 +442,8 @@ BITNET_API int bitnet_last_device_error(void) {
   int status = BITNET_OK;
   cudaError_t (*readers[])(int*) = {read_clear_device_error_gemm, read_clear_device_error_gemm_ws,
                                     read_clear_device_error_gemv_group, read_clear_device_error_smallm,
-                                    read_clear_device_error_quant_weight, read_clear_device_error_sweep};
+                                    read_clear_device_error_quant_weight, read_clear_device_error_sweep,
+                                    read_clear_device_error_gemv_ring};
   for (auto rd : readers) {
     int v = 0;
     if (rd(&v) != cudaSuccess) return BITNET_ECUDA;

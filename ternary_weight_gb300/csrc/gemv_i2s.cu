@@ -43,6 +43,16 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxActSmem = 64 * 1024;  // bytes of staged activations per CTA
 constexpr int kMaxM1K = 10240;         // largest K of the persistent few-row kernel
+// M = 1 takes the bulk-copy ring kernel for packed weights in [kRingMinBytes (kRingMinBytesLongK
+// when K >= 4096), kRingMaxBytes]. Measured against the register-prefetch kernel, µs per call in
+// back-to-back graphs: 2560 x 6912 (4.4 MB) 3.26 vs 3.60, 13824 x 2560 (8.8 MB) 4.03 vs 4.21,
+// 10000 x 8192 (20.5 MB) 5.73 vs 6.27, 8192 x 10240 (21 MB) 5.79 vs 6.77; but 6912 x 2560 (4.4 MB)
+// 3.22 vs 2.96, 2560 x 2560 3.14 vs 2.54, and 28672 x 8192 (58.7 MB) 12.73 vs 11.99: a CTA that
+// turns the ring twice ends each launch with consumer work on buffered tiles and no copies in
+// flight, which the register-prefetch kernel does not.
+constexpr int64_t kRingMinBytes = 8LL << 20;
+constexpr int64_t kRingMinBytesLongK = 4LL << 20;
+constexpr int64_t kRingMaxBytes = 40LL << 20;
 constexpr int kColBlock = 5;            // chunk columns a lane loads at once (the lane layout keeps
                                         // a row's walk at 5 columns when K <= 10240)
 
@@ -400,6 +410,13 @@ cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int3
   while (log2G > 1 && (C & ((1 << log2G) - 1)) != 0) --log2G;  // C is even, so G >= 2 divides it
   if ((C >> log2G) > 5) log2G = 5;
   const int rpw = 32 >> log2G;
+
+  // large single-token matrices: the bulk-copy ring kernel (the copy engine streams the weights,
+  // every warp of the CTA is free for the dp4a work)
+  const int64_t wbytes = (int64_t)N * (K / 4);
+  if (M == 1 && gemv_ring_supported(M, K) && wbytes >= (K >= 4096 ? kRingMinBytesLongK : kRingMinBytes) &&
+      wbytes <= kRingMaxBytes)
+    return launch_gemv_ring(xq, act_scale, rowsum, wp, w_scale, out, acc_out, N, K, num_sms, stream);
 
   if (M == 1 && K <= 10240) {
     // walk length T <= 5 (the lane layout above). Large matrices (at least two tiles per

@@ -182,10 +182,11 @@ def test_smallm_code3_and_max_magnitude():
     assert np.array_equal(host(g_out).view(np.uint32), o_out.view(np.uint32))
 
 
-# M = 1 matrices large enough for the persistent GEMV's many-CTA configuration (at least two
-# warp tiles per warp with four CTAs per SM on 152 SMs), 32-lane (ragged and not) and 8-lane
-# layouts; every output is compared.
-@pytest.mark.parametrize("N,K", [(10000, 8192), (9800, 6912), (9729, 10240), (38920, 2560)])
+# Large M = 1 matrices, every output compared: 4-40 MB of packed weights take the bulk-copy ring
+# kernel (32-lane rows ragged and not, the 8-lane layout, row slices that end inside a tile); above
+# 40 MB the persistent register-prefetch GEMV in its many-CTA configuration (four CTAs per SM).
+@pytest.mark.parametrize("N,K", [(10000, 8192), (9800, 6912), (9729, 10240), (38920, 2560), (41000, 4096),
+                                 (20003, 8448)])
 def test_chain_parity_gemv_m1_large(N, K):
     x = workloads.activations(1, K, seed=310 + K, dtype="bf16", outlier_p=0.01)
     w = workloads.ternary_weights(N, K, seed=311 + N)
