@@ -69,10 +69,10 @@ extern "C" {
 
 /* ---- matmul kernel selection (bitnet_i2s_matmul_algo) ---- */
 #define BITNET_ALGO_AUTO 0   /* GEMV for a few rows (M < 5, or M < 3 when K > 10240),
-                                the few-token kernel up to M = 64, GEMM beyond         */
+                                the few-token kernel beyond (K <= 32768)               */
 #define BITNET_ALGO_GEMV 1   /* force the dp4a decode GEMV (any M)                   */
 #define BITNET_ALGO_GEMM 2   /* force the tcgen05 tensor-core GEMM (any M)           */
-#define BITNET_ALGO_SMALLM 3 /* force the few-token tensor-core kernel (M <= 64)     */
+#define BITNET_ALGO_SMALLM 3 /* force the few-token tensor-core kernel (any M)       */
 
 /* Library ABI version (major*100 + minor). */
 BITNET_API int bitnet_version(void);
@@ -132,12 +132,13 @@ BITNET_API int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, 
  *   The 2-bit field value 3 never comes out of bitnet_pack_i2s; if present it is used
  *   arithmetically (3 - 1 = +2), the same rule as the unpacking of [DeepDive] §8.
  *   Kernel choice: for a few rows (M < 5, or M < 3 when K > 10240) a dp4a GEMV streams the
- *   packed weights. From there up to M = 64 a few-token tcgen05 kernel decodes each weight
- *   once, as the e4m3 value code + 8, for all token rows, whose int8 values enter as three
- *   exact e4m3 base-8 digits (weights as the MMA's M, K split over a thread-block cluster).
- *   For larger M a tcgen05 tile GEMM expands the codes to fp16 in shared memory. The
- *   tensor-core paths are exact: every partial sum is an integer below 2^24 accumulated in
- *   fp32. All give bit-identical results.
+ *   packed weights. From there a few-token tcgen05 kernel decodes each weight once, as the
+ *   e4m3 value code + 8, for up to 64 token rows, whose int8 values enter as three exact e4m3
+ *   base-8 digits (weights as the MMA's M, K split over a thread-block cluster); more rows go
+ *   in chunks of 64. A tcgen05 tile GEMM that expands the codes to fp16 in shared memory is
+ *   available when forced (BITNET_ALGO_GEMM); bitnet_i2s_matmul_ws is faster for long prompts
+ *   (from about 512 rows). The tensor-core paths are exact: every partial sum is an integer
+ *   below 2^24 accumulated in fp32. All give bit-identical results.
  */
 BITNET_API int bitnet_i2s_matmul(const int8_t *xq, const float *act_scale, const int32_t *rowsum,
                                  const uint8_t *wp, float w_scale, float *out, int32_t *acc_out,
@@ -310,8 +311,8 @@ BITNET_API int bitnet_ffn_act_quant(const float *gate, const float *up, const fl
  *              three may be NULL.
  *   workspace, workspace_bytes : optional (NULL, 0) device workspace, 256-byte aligned, of at
  *              least bitnet_w2a8_ffn_workspace_size(M, K, F) bytes; when given and that size is
- *              non-zero, the three projections run on the expand-once GEMM path of
- *              bitnet_i2s_matmul_ws.
+ *              non-zero (M >= 512 with K, F <= 32768), the three projections run on the
+ *              expand-once GEMM path of bitnet_i2s_matmul_ws.
  *   M >= 1; K and F multiples of 128 with K <= 65536 and F <= 32768; eps finite and > 0.
  */
 BITNET_API int64_t bitnet_w2a8_ffn_workspace_size(int64_t M, int64_t K, int64_t F);

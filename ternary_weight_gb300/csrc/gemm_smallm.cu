@@ -39,8 +39,9 @@
 // that k: a thread's 16 bytes give 16 tensor-memory columns of 4 positions each, and a
 // 16-byte piece of activations (16 consecutive k) is one 16-byte chunk of each digit row.
 //
-// Structure (one CTA per 128 weight rows and a range of stages; a thread-block cluster of up to
-// 8 CTAs splits the stages):
+// Structure (one CTA per 128 weight rows, a range of stages and a chunk of up to 64 tokens; a
+// thread-block cluster of up to 8 CTAs splits the stages; more than 64 tokens take grid.z chunks,
+// each decoding its weight slice again from L2):
 //  * warps 1-16 (workers): warp w owns tensor-memory lanes 32(w%4)..+31, i.e. weight rows, and
 //    the 16-byte quarter q = (w-1)/4 of each row's 64 stage bytes. Each thread copies its own
 //    16 weight bytes and up to two 16-byte pieces of the stage's int8 activations with
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
                                                                  const int32_t* __restrict__ rowsum,
                                                                  const uint8_t* __restrict__ wp, float w_scale,
                                                                  float* __restrict__ out, int32_t* __restrict__ acc_out,
-                                                                 int M, int N, int K) {
+                                                                 int M, int N, int K) {  // M: all tokens
   using Cfg = SmallCfg<MP>;
   constexpr int NS = Cfg::NS, XV = Cfg::XV, NC = Cfg::NC, PD = Cfg::PD, NACC = Cfg::NACC, NB = Cfg::NB;
   extern __shared__ uint8_t smem_raw[];
@@ -217,6 +218,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
   __shared__ uint32_t tmem_slot;
 
   pdl_launch_dependents();
+  // this CTA's chunk of tokens: rows m0 .. m0 + M - 1 (M from here on counts the chunk's tokens)
+  const int m0 = (int)blockIdx.z * MP;
+  M = M - m0 < MP ? M - m0 : MP;
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t bring = raw_addr + ((1024u - (raw_addr & 1023u)) & 1023u);  // NS B tiles
   const uint32_t staged = bring + NS * Cfg::B_STAGE;                         // PD stages of copied inputs
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       if (idx < MP * 16) {
         const bool ok = m < M && 2 * gs + (u >> 3) < nblk;
         cp_async_16(my_w + (uint32_t)((i % PD) * Cfg::RAW_SLOT + WK_THREADS * 16 * (1 + v)),
-                    ok ? xq + (int64_t)m * K + 256 * (int64_t)gs + 16 * u : xq, ok ? 16u : 0u);
+                    ok ? xq + (int64_t)(m0 + m) * K + 256 * (int64_t)gs + 16 * u : xq, ok ? 16u : 0u);
       }
     }
   };
@@ -455,9 +459,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       for (int c = 0; c < NC; ++c) {
         const int m = c0 + c;
         if (m < M) {
-          const int a = part[c] - 9 * __ldg(rowsum + m);  // raw = part - 8 rowsum; acc = raw - rowsum
-          const int64_t o = (int64_t)m * N + n;
-          out[o] = __fmul_rn(__fdiv_rn(__int2float_rn(a), __ldg(act_scale + m)), w_scale);
+          const int a = part[c] - 9 * __ldg(rowsum + m0 + m);  // raw = part - 8 rowsum; acc = raw - rowsum
+          const int64_t o = (int64_t)(m0 + m) * N + n;
+          out[o] = __fmul_rn(__fdiv_rn(__int2float_rn(a), __ldg(act_scale + m0 + m)), w_scale);
           if (acc_out) acc_out[o] = a;
         }
       }
@@ -501,8 +505,10 @@ cudaError_t launch_mp(const int8_t* xq, const float* act_scale, const int32_t* r
   // tiles, 7-CTA clusters pack only two per GPC. The occupancy query decides, shrinking the
   // cluster until every one fits.
   const int64_t n_tiles = (N + TW - 1) / TW;
+  const int64_t n_chunks = (M + MP - 1) / MP;  // token chunks (grid.z)
+  const int64_t n_ctas1 = n_tiles * n_chunks;   // CTAs at cluster size 1
   const int64_t n_stages = (K / 128 + 1) / 2;
-  int64_t cs = num_sms / n_tiles;
+  int64_t cs = num_sms / n_ctas1;
   if (cs > kMaxCluster) cs = kMaxCluster;
   if (cs > n_stages) cs = n_stages;
   if (cs < 1) cs = 1;
@@ -518,16 +524,16 @@ cudaError_t launch_mp(const int8_t* xq, const float* act_scale, const int32_t* r
   cfg.numAttrs = 1;
   for (; cs > 1; --cs) {
     attr[0].val.clusterDim.y = (unsigned)cs;
-    cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs);
+    cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs, (unsigned)n_chunks);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, gemm_smallm_kernel<MP>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();  // the query is only a hint: keep the size from the SM count
       break;
     }
-    if (clusters >= n_tiles) break;
+    if (clusters >= n_ctas1) break;
   }
   attr[0].val.clusterDim.y = (unsigned)cs;
-  cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs);
+  cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)cs, (unsigned)n_chunks);
   // weights stream in while the previous kernel finishes (the kernel waits for it before reading
   // the activations or writing anything)
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -546,7 +552,7 @@ cudaError_t read_clear_device_error_smallm(int* value) {
   return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
 }
 
-bool gemm_smallm_supported(int64_t M, int64_t K) { return M >= 1 && M <= 64 && K <= 32768; }
+bool gemm_smallm_supported(int64_t M, int64_t K) { return M >= 1 && M <= 64LL * 65535 && K <= 32768; }
 
 cudaError_t launch_gemm_smallm(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
                                float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,

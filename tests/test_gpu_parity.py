@@ -148,11 +148,13 @@ def test_chain_parity_gemv(M, N, K, dtype):
 
 # The few-token tensor-core kernel, forced: every MMA width (16/32/48/64 tokens), ragged N (a
 # partial last 128-row tile), K with a half last 256-k stage, K splits over clusters of 1 to 8
-# CTAs, M = 1, and the decode shapes at M = 4 / 16 / 64.
+# CTAs, M = 1, the decode shapes at M = 4 / 16 / 64, and more than 64 tokens in chunks of 64
+# (a ragged last chunk; several chunks with clusters).
 SMALLM_CHAIN = [
     (1, 256, 128, "f32"), (2, 300, 2560, "bf16"), (4, 6912, 2560, "bf16"), (8, 1000, 8192, "bf16"),
     (16, 2560, 6912, "bf16"), (17, 700, 384, "f32"), (33, 129, 1024, "bf16"), (48, 2560, 2560, "f32"),
-    (63, 513, 10240, "bf16"), (64, 6912, 2560, "bf16"), (64, 2560, 6912, "bf16"),
+    (63, 513, 10240, "bf16"), (64, 6912, 2560, "bf16"), (64, 2560, 6912, "bf16"), (65, 300, 2560, "bf16"),
+    (100, 700, 6912, "f32"), (129, 257, 1024, "bf16"), (200, 513, 2560, "bf16"),
 ]
 
 
@@ -297,6 +299,13 @@ def _sampled_full_size(case, algo="auto", n_rows=16, n_cols=384):
                          + workloads.prefill_cases() + workloads.large_cases(), ids=lambda c: c.name)
 def test_full_size_configs(case):
     _sampled_full_size(case)
+
+
+@pytest.mark.parametrize("case", workloads.prefill_cases(), ids=lambda c: c.name)
+def test_full_size_prefill_few_token_kernel(case):
+    """The prefill configs (M = 128 and 512) through the few-token kernel in token chunks, forced;
+    sampled outputs against the oracle."""
+    _sampled_full_size(case, algo="smallm")
 
 
 # ----------------------------------------------------------------------------- fused, grouped linear
@@ -676,10 +685,11 @@ def _ffn_oracle(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps):
 
 FFN_CASES = [
     # (M, K, F, dtype, workspace): the two-launch path (M = 1, including a row too long for
-    # the registers, F = 10240), the few-token and GEMM paths, and the expand-once workspace
+    # the registers, F = 10240), the few-token path (more than 64 rows in chunks), and the
+    # expand-once workspace path (from 512 rows)
     (1, 2560, 6912, "f32", False), (1, 2560, 6912, "bf16", False), (1, 512, 10240, "f32", False),
     (1, 1024, 128, "bf16", False), (2, 2560, 6912, "bf16", False), (17, 640, 1280, "f32", False),
-    (65, 2560, 6912, "bf16", False), (130, 1024, 2048, "f32", True),
+    (65, 2560, 6912, "bf16", False), (130, 1024, 2048, "f32", False), (512, 1024, 2048, "bf16", True),
 ]
 
 
