@@ -389,7 +389,7 @@ cudaError_t launch_gemv_ring(const int8_t* xq, const float* act_scale, const int
                              cudaStream_t stream);
 cudaError_t read_clear_device_error_gemv_ring(int* value);
 
-// Few-token tensor-core matmul (gemm_smallm.cu): 1 <= M <= 64, K <= 32768.
+// Few-token tensor-core matmul (gemm_smallm.cu): any M (64 tokens per CTA), K <= 32768.
 bool gemm_smallm_supported(int64_t M, int64_t K);
 cudaError_t launch_gemm_smallm(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
                                float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,

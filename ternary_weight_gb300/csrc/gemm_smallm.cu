@@ -1,4 +1,4 @@
-// gemm_smallm.cu -- the W2A8 ternary matmul for a few tokens (2 <= M <= 64) on the tensor cores,
+// gemm_smallm.cu -- the W2A8 ternary matmul for a few tokens (64 per CTA, more in chunks) on the tensor cores,
 // with the weights as the MMA's M dimension.
 //
 // Computes, like every other path of the library, raw[m][n] = sum_k code[n][k] * xq[m][k],
