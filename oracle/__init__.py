@@ -189,8 +189,8 @@ def quant_weight(w: np.ndarray, dtype: str = "f32", mode: str = "absmean"):
 
 def ffn_inner(gate: np.ndarray, up: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     """FFN inner activation of M x F fp32 gate and up rows: inner = RMSNorm(max(g, 0)^2 * u)
-    with per-channel weight gamma (F fp32) and epsilon eps, the sum of squares in the fixed
-    order of bitnet_oracle.c. Returns M x F float32."""
+    with per-channel weight gamma (F fp32) and epsilon eps; the sum of squares is the plain
+    ascending sum in double, rounded once to fp32. Returns M x F float32."""
     lib = _load()
     gate = np.ascontiguousarray(gate, dtype=np.float32)
     up = np.ascontiguousarray(up, dtype=np.float32)

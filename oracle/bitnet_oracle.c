@@ -314,33 +314,24 @@ int oracle_quant_weight_bf16(const uint16_t *w, int64_t N, int64_t K, int mode, 
  *     weight gamma and an epsilon eps, neither of which the page prints, so both are inputs:
  *     inner = (h * c) * gamma, c = 1 / sqrt(ss / F + eps), ss = sum of h^2, all in fp32, each
  *     operation one rounding (sqrtf and the divisions are correctly rounded);
- *   - the order of the sum of squares, which the page leaves open, is fixed so that every
- *     implementation gets the same fp32 ss (and from it the same codes downstream): 256
- *     partial sums, partial p taking the h_k with floor(k / 4) mod 256 == p in ascending k,
- *     each by one fused multiply-add h_k * h_k + partial; then, within each run of 32
- *     partials, the tree that adds partial p + d into partial p (p < d) for d = 16, 8, 4, 2, 1;
- *     then the eight run sums as ((R0 + R1) + (R2 + R3)) + ((R4 + R5) + (R6 + R7)).
+ *   - the sum of squares is the plain sum over k = 0 .. F-1 in ascending order, taken in double
+ *     (each h_k * h_k is exact in double, and F terms add at most F * 2^-53 relative error)
+ *     and rounded once to fp32; that is the definition's value to within half an fp32 ulp.
+ *     The page fixes no order; a parallel implementation may sum in any order, and its ss
+ *     then differs from this one by its own rounding error only (the codes downstream are
+ *     compared with that error in mind).
  * --------------------------------------------------------------------------------------- */
 static void ffn_inner_row(const float *g, const float *u, const float *gamma, float eps, int64_t F,
                           float *inner) {
-    float part[256];
-    for (int p = 0; p < 256; ++p) part[p] = 0.0f;
+    double ss = 0.0;
     for (int64_t k = 0; k < F; ++k) {
         const float r = g[k] > 0.0f ? g[k] : 0.0f;
         const float h = (r * r) * u[k];
         inner[k] = h; /* h parked in the output until c is known */
-        const int p = (int)((k / 4) % 256);
-        part[p] = fmaf(h, h, part[p]);
+        ss += (double)h * (double)h;
     }
-    float run[8];
-    for (int w = 0; w < 8; ++w) {
-        float *q = part + 32 * w;
-        for (int d = 16; d >= 1; d /= 2)
-            for (int p = 0; p < d; ++p) q[p] = q[p] + q[p + d];
-        run[w] = q[0];
-    }
-    const float ss = ((run[0] + run[1]) + (run[2] + run[3])) + ((run[4] + run[5]) + (run[6] + run[7]));
-    const float c = 1.0f / sqrtf(ss / (float)F + eps);
+    const float ssf = (float)ss;
+    const float c = 1.0f / sqrtf(ssf / (float)F + eps);
     for (int64_t k = 0; k < F; ++k) inner[k] = (inner[k] * c) * gamma[k];
 }
 

@@ -67,7 +67,7 @@ int oracle_quant_weight_bf16(const uint16_t *w, int64_t N, int64_t K, int mode, 
 
 /* FFN inner activation ([bitnet.rs] "Forward Pass"): per row m of gate and up (M x F fp32),
  * h = max(g, 0)^2 * u, inner = (h * c) * gamma with c = 1 / sqrt(sum(h^2) / F + eps), the sum
- * of squares taken in the fixed order described in bitnet_oracle.c. gamma is F fp32 (shared
+ * of squares the plain ascending sum taken in double and rounded once to fp32. gamma is F fp32 (shared
  * by all rows), eps >= 0. inner is M x F fp32. Returns 0, -1 on bad arguments, -2 if the
  * rounding mode is not round-to-nearest-even. */
 int oracle_ffn_inner(const float *gate, const float *up, const float *gamma, float eps, int64_t M, int64_t F,

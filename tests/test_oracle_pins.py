@@ -438,15 +438,17 @@ def _ffn_rows(M, F, seed):
 @pytest.mark.parametrize("eps", [0.0, 1e-5, 0.5])
 def test_ffn_inner_matches_fp64_definition(eps):
     """[bitnet.rs] "Forward Pass": inner = RMSNorm(sqrelu(gate) * up), against the same
-    formula in float64 (numpy). The fp32 oracle's error is a few ulps plus the sum's
-    rounding (< 40 * 2^-24 relative); a dropped or misplaced term (no square in sqrelu, no
-    gamma, eps outside the root, sum instead of mean) is off by far more."""
+    formula in float64 (numpy). The oracle rounds h twice, the sum of squares once (it is
+    summed in double), then ss / F, + eps, the root, the reciprocal and the two products once
+    each: at most 8 * 2^-24 relative in all. A dropped or misplaced term (no square in sqrelu,
+    no gamma, eps outside the root, sum instead of mean) is off by far more, and so is a sum
+    of squares accumulated in fp32 over the 6912 terms."""
     M, F = 3, 6912
     g, u, gamma = _ffn_rows(M, F, 11)
     got = oracle.ffn_inner(g, u, gamma, eps)
     h = np.maximum(g.astype(np.float64), 0.0) ** 2 * u
     ref = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + eps) * gamma
-    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-30)
+    np.testing.assert_allclose(got, ref, rtol=8 * 2.0 ** -24, atol=1e-30)
 
 
 def test_ffn_inner_sqrelu_zeroes_non_positive_gates():
