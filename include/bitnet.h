@@ -22,7 +22,11 @@
  *
  * Common rules for every entry point:
  *   - All array pointers are DEVICE pointers owned by the caller; the library keeps no
- *     pointer after the call returns and allocates no device memory.
+ *     pointer after the call returns. No call allocates device memory, with two stated
+ *     exceptions: bitnet_sweep_plan_create allocates the plan's device table (cudaMalloc,
+ *     freed by bitnet_sweep_plan_destroy), and the library's device image holds a fixed
+ *     64 MiB scratch array (used only by bitnet_i2s_matmul_noalloc) that every GPU which
+ *     loads the library keeps until the process exits, used or not. Budget for both.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as void*; NULL is
  *     the legacy default stream). Results are valid once the stream has reached the call.
  *   - Arguments are validated on the host before anything is launched; an invalid call
@@ -172,7 +176,9 @@ BITNET_API int bitnet_i2s_matmul_ws(const int8_t *xq, const float *act_scale, co
  *   (bitnet_i2s_matmul_workspace_size) exceeds 64 MiB are refused with BITNET_EINVAL before
  *   any GPU work.
  *   The first call on each device (with that device current) looks up the array's device
- *   address; make that first call before any stream capture.
+ *   address and keeps it for the life of the process; make that first call before any stream
+ *   capture. A cudaDeviceReset of that device after its first call is not supported: the kept
+ *   address would then be stale.
  *   All calls share the array: calls that overlap on the GPU race on it. Each call overwrites
  *   what it uses, so nothing has to be cleared between calls.
  *   Other arguments, results and errors as bitnet_i2s_matmul_ws.
@@ -269,11 +275,14 @@ BITNET_API int bitnet_w2a8_linear(const void *x, int dtype, int64_t M, int64_t K
  *   h = max(g, 0)^2 * u  (as (r * r) * u, r = g > 0 ? g : 0)
  *   inner = (h * c) * gamma,  c = 1 / sqrt(ss / F + eps)        (RMSNorm, weight gamma)
  *   xq, act_scale, rowsum = what bitnet_quant_act gives for the fp32 row inner.
- * ss, the sum of h^2, is taken in a fixed order so the result is reproducible bit for bit:
- * 256 partial sums, partial p accumulating by fused multiply-add, in ascending k, the h_k
- * with floor(k / 4) mod 256 == p; each run of 32 partials combined by the pairwise tree that
- * adds partial p + d into p for d = 16, 8, 4, 2, 1; the eight run sums combined as
- * ((R0 + R1) + (R2 + R3)) + ((R4 + R5) + (R6 + R7)).
+ * The page fixes no order for ss, the sum of h^2. This library adds it in fp32 in a fixed
+ * order, so repeated calls give the same bits: 256 partial sums, partial p accumulating by
+ * fused multiply-add, in ascending k, the h_k with floor(k / 4) mod 256 == p; each run of 32
+ * partials combined by the pairwise tree that adds partial p + d into p for d = 16, 8, 4, 2, 1;
+ * the eight run sums combined as ((R0 + R1) + (R2 + R3)) + ((R4 + R5) + (R6 + R7)). That is
+ * at most F/256 + 8 roundings per term away from the exact sum (8.1e-6 relative at
+ * F = 32768), so inner is within 1e-5 relative of the exactly summed definition, and a code
+ * can differ from the exactly summed one only next to a rounding boundary.
  *
  *   gate, up  : M x F fp32 (device, read), 16-byte aligned
  *   gamma     : F fp32 (device, read), 16-byte aligned, shared by all rows
@@ -361,6 +370,24 @@ BITNET_API int bitnet_sweep_plan_destroy(bitnet_sweep_plan plan);
  * Returns BITNET_OK, BITNET_ETIMEOUT, BITNET_ERANGE or BITNET_ECUDA.
  */
 BITNET_API int bitnet_last_device_error(void);
+
+/*
+ * bitnet_selftest_wait_timeout -- a diagnostic of the failure handling above; the pages have
+ * no counterpart (they describe no GPU failure path). One small kernel takes, on purpose, the
+ * path that bounded waits take when they run out, without faulting or hanging the GPU: one
+ * thread starts a bulk copy of `bytes` bytes from src into shared memory, while a warp waits
+ * on an mbarrier that nothing ever arrives on, giving up after max_polls polls. The warp then
+ * records BITNET_ETIMEOUT in the device error word, and the copying thread waits (bounded) for
+ * its copy to land before the kernel returns, as every producer in the library does.
+ *   src       : device, 16-byte aligned, at least `bytes` bytes (read)
+ *   bytes     : 16..16384, a multiple of 16
+ *   max_polls : 1..2^20 polls of the never-completing barrier
+ *   report    : device, 3 uint32 (written): [0] 1 if the wait gave up, [1] 1 if the copy was
+ *               seen to land, [2] the wrapping sum of the copied 32-bit words
+ * After the kernel has run, bitnet_last_device_error returns BITNET_ETIMEOUT (and clears it).
+ */
+BITNET_API int bitnet_selftest_wait_timeout(const void *src, int64_t bytes, int32_t max_polls,
+                                            uint32_t *report, void *stream);
 
 #ifdef __cplusplus
 }

@@ -49,6 +49,7 @@ SIGNATURES = {
         [_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "bitnet_i2s_matmul_noalloc": ([_P, _P, _P, _P, ctypes.c_float, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "bitnet_last_device_error": ([], ctypes.c_int),
+    "bitnet_selftest_wait_timeout": ([_P, _I64, ctypes.c_int32, _P, _P], ctypes.c_int),
     "bitnet_quant_weight": ([_P, ctypes.c_int, ctypes.c_int, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "bitnet_ffn_act_quant": ([_P, _P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P, _P, _P], ctypes.c_int),
     "bitnet_w2a8_ffn_workspace_size": ([_I64, _I64, _I64], _I64),
@@ -279,6 +280,20 @@ def linear_group(x, wps, w_scales, outs=None, accs=None, xq=None, scale=None, ro
 
 def last_device_error() -> int:
     return lib().bitnet_last_device_error()
+
+
+def selftest_wait_timeout(src, max_polls, report=None, stream=None):
+    """Run the failure-handling self-test: a bounded wait that runs out while a bulk copy of
+    ``src`` (a CUDA tensor of 16..16384 bytes) is in flight. Returns the 3-word uint32 report
+    (gave up, copy landed, wrapping word sum) as an int32 CUDA tensor."""
+    import torch
+
+    report = torch.zeros(3, dtype=torch.int32, device=src.device) if report is None else report
+    _require_cuda(src, report)
+    _check(lib().bitnet_selftest_wait_timeout(_ptr(src), src.numel() * src.element_size(), int(max_polls),
+                                              _ptr(report), _stream(stream)),
+           "bitnet_selftest_wait_timeout")
+    return report
 
 
 def linear(x, wp, w_scale, out=None, algo="auto", stream=None):

@@ -64,20 +64,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete. Returns false (and records a
 // timeout) if it did not complete within kMaxPolls polls; *abort is then set so that the
 // caller's loop can leave early. Once *abort is set no further waiting is done.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool* abort) {
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t parity, bool* abort, uint32_t max_polls) {
   if (*abort) return false;
   const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < kMaxPolls; ++i)
+  for (uint32_t i = 0; i < max_polls; ++i)
     if (mbar_try_wait(a, parity)) return true;
   record_device_error(kErrTimeout);
   *abort = true;
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool* abort) {
+  return mbar_wait_polls(bar, parity, abort, kMaxPolls);
 }
 
 // mbar_wait by every lane of a warp, with the outcome made warp-uniform: a warp never splits at
 // a timeout before warp-collective code (shuffles, tcgen05.ld). All 32 lanes must call it.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, bool* abort) {
   const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+  if (!ok) *abort = true;
+  return ok;
+}
+
+// mbar_wait_warp with a caller-chosen poll limit (the failure-handling self-test).
+__device__ __forceinline__ bool mbar_wait_warp_polls(uint64_t* bar, uint32_t parity, bool* abort, uint32_t max_polls) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_polls(bar, parity, abort, max_polls));
   if (!ok) *abort = true;
   return ok;
 }
@@ -400,6 +410,11 @@ cudaError_t read_clear_device_error_quant_weight(int* value);
 cudaError_t read_clear_device_error_gemm(int* value);
 cudaError_t read_clear_device_error_gemm_ws(int* value);
 cudaError_t read_clear_device_error_gemv_group(int* value);
+cudaError_t read_clear_device_error_selftest(int* value);
+// Failure-handling self-test (selftest.cu): a bounded wait on a barrier nothing arrives on.
+bool selftest_bytes_ok(int64_t bytes);
+cudaError_t launch_wait_timeout_selftest(const void* src, int64_t bytes, uint32_t max_polls, uint32_t* report,
+                                         cudaStream_t stream);
 
 // Host: encode a 2-D tiled TMA tensor map over a row-major [rows][inner] array
 // (gemm_tc_ws.cu). False if the driver entry point is missing or the encoder refuses.

@@ -1,8 +1,11 @@
 // capi.cu -- the extern "C" boundary of libbitnet_gb300 (declared in include/bitnet.h).
 //
 // Every entry point validates its arguments on the host before anything is launched and
-// returns a status code; no C++ exception crosses the ABI. The library holds no device
-// allocation: the only device-side state is one error word written by bounded waits.
+// returns a status code; no C++ exception crosses the ABI. Device-side state: one error word
+// per kernel translation unit (written by bounded waits), the 64 MiB scratch array of
+// noalloc.cu (part of the device image, resident on every GPU that loads the library), and
+// the device table of each sweep plan, the one cudaMalloc the library makes (in
+// bitnet_sweep_plan_create, freed by bitnet_sweep_plan_destroy).
 #include "bitnet.h"
 #include "bitnet_dev.cuh"
 
@@ -440,6 +443,16 @@ BITNET_API int bitnet_sweep_plan_destroy(bitnet_sweep_plan plan) {
   return e1 == cudaSuccess && e2 == cudaSuccess ? BITNET_OK : BITNET_ECUDA;
 }
 
+BITNET_API int bitnet_selftest_wait_timeout(const void* src, int64_t bytes, int32_t max_polls, uint32_t* report,
+                                            void* stream) {
+  if (!src || !report || !selftest_bytes_ok(bytes) || max_polls < 1 || max_polls > (1 << 20)) return BITNET_EINVAL;
+  if (!aligned(src, 16) || !aligned(report, 4)) return BITNET_EALIGN;
+  int sms = 0;
+  if (int st = check_device(&sms)) return st;
+  return status_of(launch_wait_timeout_selftest(src, bytes, (uint32_t)max_polls, report,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 BITNET_API int bitnet_last_device_error(void) {
   int sms = 0;
   if (int st = check_device(&sms)) return st;
@@ -448,7 +461,7 @@ BITNET_API int bitnet_last_device_error(void) {
   cudaError_t (*readers[])(int*) = {read_clear_device_error_gemm, read_clear_device_error_gemm_ws,
                                     read_clear_device_error_gemv_group, read_clear_device_error_smallm,
                                     read_clear_device_error_quant_weight, read_clear_device_error_sweep,
-                                    read_clear_device_error_gemv_ring};
+                                    read_clear_device_error_gemv_ring, read_clear_device_error_selftest};
   for (auto rd : readers) {
     int v = 0;
     if (rd(&v) != cudaSuccess) return BITNET_ECUDA;

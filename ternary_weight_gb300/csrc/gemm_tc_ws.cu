@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_f16_ws_kernel(const __grid_co
           tma_load_2d(a_dst + A_BYTES, &tmB, ks * BK, n0, &full_bar[s]);
         }
       }
-      if (abort) {  // let the copies already issued land before the CTA can exit
+      {  // every copy issued lands before the producer leaves: the MMA thread may have given up
+         // on a full barrier (a bounded wait) while copies were still in flight
         bool dummy = false;
         for (int i = it - STAGES > 0 ? it - STAGES : 0; i < it; ++i) mbar_wait(&full_bar[i % STAGES], (i / STAGES) & 1, &dummy);
       }

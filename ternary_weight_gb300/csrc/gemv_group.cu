@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_group_kernel(const void* __r
         if (issued == kSlots) issue_prefetch(pf);  // ring primed: now the L2 prefetch hint
       }
       if (issued < kSlots) issue_prefetch(pf);
-      if (abort) {  // let every copy this CTA issued land before the CTA can exit
+      {  // every copy this CTA issued lands before the producer leaves: the consumers may have
+         // given up on a full barrier (a bounded wait) while copies were still in flight
         bool dummy = false;
         for (int i = issued - kSlots > 0 ? issued - kSlots : 0; i < issued; ++i)
           mbar_wait(&full_bar[i % kSlots], (i / kSlots) & 1, &dummy);

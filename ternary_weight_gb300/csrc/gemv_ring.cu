@@ -89,8 +89,9 @@ __global__ void __launch_bounds__(kRgThreads, 1) gemv_ring_kernel(const int8_t* 
         mbar_arrive_expect_tx(&full_bar[slot], bytes);
         bulk_copy_g2s(ring + slot * kRgSlotBytes, wp + (int64_t)r0 * row_bytes, bytes, &full_bar[slot]);
       }
-      if (abort) {
-        bool dummy = false;  // let every copy this CTA issued land before the CTA can exit
+      {  // every copy this CTA issued lands before the producer leaves: the consumers may have
+         // given up on a full barrier (a bounded wait) while copies were still in flight
+        bool dummy = false;
         for (int i = issued - kRgSlots > 0 ? issued - kRgSlots : 0; i < issued; ++i)
           mbar_wait(&full_bar[i % kRgSlots], (uint32_t)(i / kRgSlots) & 1u, &dummy);
       }

@@ -140,8 +140,9 @@ __global__ void __launch_bounds__(kSwThreads, 1) gemv_sweep_kernel(const SweepGr
           off += G.N[j];
         }
       }
-      if (abort) {
-        bool dummy = false;  // let every copy this CTA issued land before the CTA can exit
+      {  // every copy this CTA issued lands before the producer leaves: the consumers may have
+         // given up on a full barrier (a bounded wait) while copies were still in flight
+        bool dummy = false;
         for (int i = issued - kSwSlots > 0 ? issued - kSwSlots : 0; i < issued; ++i)
           mbar_wait(&full_bar[i % kSwSlots], (i / kSwSlots) & 1, &dummy);
       }

@@ -13,7 +13,8 @@
 // Host code cannot use the array's name as a device address (on the host it names a host-side
 // stand-in), so the first call on each device, with that device current, asks the runtime for
 // the device address with cudaGetSymbolAddress and caches it; make that first call before any
-// stream capture. All calls share the one array: calls that overlap on the GPU (on different
+// stream capture. The cache is never invalidated, so a cudaDeviceReset of a device after its
+// first call is not supported (the module would be reloaded and the cached address stale). All calls share the one array: calls that overlap on the GPU (on different
 // streams, or from several host threads without ordering) race on it. Nothing in it has to
 // start at zero -- each call overwrites the part it uses before reading it.
 #include "bitnet.h"

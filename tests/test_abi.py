@@ -276,3 +276,12 @@ def test_workspace_size_and_ws_validation(lib):
     assert ws(n=need - 1) == -1
     assert ws(w=FAKE + 16) == -2   # the workspace must be 256-byte aligned
     assert ws(xq=FAKE + 8) == -2
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, 64, 8, FAKE), -1), ((FAKE, 64, 8, None), -1), ((FAKE, 0, 8, FAKE), -1), ((FAKE, 24, 8, FAKE), -1),
+    ((FAKE, 16384 + 16, 8, FAKE), -1), ((FAKE, 64, 0, FAKE), -1), ((FAKE, 64, (1 << 20) + 1, FAKE), -1),
+    ((FAKE + 8, 64, 8, FAKE), -2), ((FAKE, 64, 8, FAKE + 2), -2),
+])
+def test_selftest_rejects_bad_arguments_on_host(lib, args, status):
+    assert lib.bitnet_selftest_wait_timeout(*args, None) == status

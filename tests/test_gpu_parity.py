@@ -270,42 +270,63 @@ def test_misaligned_pointer_is_rejected():
 
 # ----------------------------------------------------------------------------- full-size configs
 
-def _sampled_full_size(case, algo="auto", n_rows=16, n_cols=384):
-    """Full-size GPU run; the oracle recomputes sampled outputs one by one (all of xq/s/rowsum
-    and the packed weights are compared in full)."""
+_ORACLE_FULL = {}
+
+
+def _oracle_full_size(case):
+    """The oracle's pack, quantisation and matmul of a full-size case (every output), computed
+    once per case and shared by the kernel paths that are checked on it."""
+    if case.name not in _ORACLE_FULL:
+        x, w = case.x(), case.weights()
+        o_wp, _ = oracle.pack_i2s(w)
+        o_xq, o_s, o_rs = oracle.quant_act(x, case.act_dtype)
+        o_out, o_acc = oracle.ternary_matmul(o_xq, o_s, o_wp, case.w_scale(), nthreads=NT)
+        _ORACLE_FULL.clear()  # keep one case resident at a time
+        _ORACLE_FULL[case.name] = dict(wp=o_wp, xq=o_xq, s=o_s, rs=o_rs, out=o_out, acc=o_acc)
+    return _ORACLE_FULL[case.name]
+
+
+def _full_size(case, path="auto"):
+    """Full-size GPU run through the C ABI, every element compared with the oracle: packed
+    bytes, xq, s, rowsum, the int32 accumulators and the fp32 outputs, bit for bit. ``path`` is
+    a kernel choice of bitnet_i2s_matmul_algo or "ws" (bitnet_i2s_matmul_ws)."""
     x, w, ws = case.x(), case.weights(), case.w_scale()
     g_wp = binding.pack_i2s(dev(w))
     g_xq, g_s, g_rs = binding.quant_act(x_device(x, case.act_dtype))
     g_acc = torch.empty((case.M, case.N), dtype=torch.int32, device="cuda")
-    g_out = binding.i2s_matmul(g_xq, g_s, g_rs, g_wp, ws, acc_out=g_acc, algo=algo)
+    if path == "ws":
+        g_out = binding.i2s_matmul_ws(g_xq, g_s, g_rs, g_wp, ws, acc_out=g_acc)
+    else:
+        g_out = binding.i2s_matmul(g_xq, g_s, g_rs, g_wp, ws, acc_out=g_acc, algo=path)
     torch.cuda.synchronize()
-    o_wp, _ = oracle.pack_i2s(w)
-    o_xq, o_s, o_rs = oracle.quant_act(x, case.act_dtype)
-    assert np.array_equal(host(g_wp), o_wp)
-    assert np.array_equal(host(g_xq), o_xq)
-    assert np.array_equal(host(g_s).view(np.uint32), o_s.view(np.uint32))
-    assert np.array_equal(host(g_rs), o_rs)
-    rng = np.random.default_rng(700)
-    mi = np.unique(np.concatenate([[0, case.M - 1], rng.integers(0, case.M, n_rows)]))
-    ni = np.unique(np.concatenate([[0, case.N - 1], rng.integers(0, case.N, n_cols)]))
-    o_out, o_acc = oracle.ternary_matmul(o_xq[mi], o_s[mi], o_wp[ni], ws, nthreads=NT)
-    acc = host(g_acc)[np.ix_(mi, ni)]
-    out = host(g_out)[np.ix_(mi, ni)]
-    assert np.array_equal(acc, o_acc)
-    assert_out_close(out, o_out)
+    o = _oracle_full_size(case)
+    assert np.array_equal(host(g_wp), o["wp"])
+    assert np.array_equal(host(g_xq), o["xq"])
+    assert np.array_equal(host(g_s).view(np.uint32), o["s"].view(np.uint32))
+    assert np.array_equal(host(g_rs), o["rs"])
+    assert np.array_equal(host(g_acc), o["acc"])
+    out = host(g_out)
+    assert_out_close(out, o["out"])
+    assert np.array_equal(out.view(np.uint32), o["out"].view(np.uint32))
+    assert binding.last_device_error() == 0
 
 
 @pytest.mark.parametrize("case", [workloads.single_gemv()] + workloads.batched_decode_cases()
                          + workloads.prefill_cases() + workloads.large_cases(), ids=lambda c: c.name)
 def test_full_size_configs(case):
-    _sampled_full_size(case)
+    """Every configuration at full size, in the launch configuration the plain call uses."""
+    _full_size(case)
 
 
-@pytest.mark.parametrize("case", workloads.prefill_cases(), ids=lambda c: c.name)
-def test_full_size_prefill_few_token_kernel(case):
-    """The prefill configs (M = 128 and 512) through the few-token kernel in token chunks, forced;
-    sampled outputs against the oracle."""
-    _sampled_full_size(case, algo="smallm")
+FULL_PREFILL_PATHS = [(c, p) for c in workloads.prefill_cases() + workloads.large_cases()[:1]
+                      for p in ("smallm", "ws")]
+
+
+@pytest.mark.parametrize("case,path", FULL_PREFILL_PATHS, ids=lambda v: v if isinstance(v, str) else v.name)
+def test_full_size_prefill_paths(case, path):
+    """The prefill configurations (M = 128, 512 and 4096) through each tensor-core path the
+    library offers for them, every element against the oracle."""
+    _full_size(case, path)
 
 
 # ----------------------------------------------------------------------------- fused, grouped linear
@@ -631,12 +652,47 @@ def _ffn_gamma(F, seed):
     return workloads.rmsnorm_gamma(F, seed)
 
 
+# The FFN inner row's sum of squares has no order on the page. The oracle takes the plain
+# ascending sum in double, rounded once; the kernels add fp32 partials in a fixed order of
+# their own, at most F/256 + 8 roundings per term for F <= 32768, so their ss is within
+# 136 * 2^-24 = 8.1e-6 relative of the oracle's. That moves c = 1/sqrt(ss/F + eps) by at most
+# half as much, and inner = (h * c) * gamma by that plus a few roundings: below 1e-5 relative.
+# The codes are decided by inner * s; both factors move by at most 1e-5, so a code may differ
+# only where the oracle's product lies within 2e-5 relative of a rounding boundary, and then
+# only to the neighbour on the other side.
+FFN_REL = 1e-5
+
+
+def assert_ffn_inner_close(g_inner, o_inner):
+    err = np.abs(g_inner.astype(np.float64) - o_inner.astype(np.float64))
+    bad = err > FFN_REL * np.abs(o_inner.astype(np.float64))
+    assert not bad.any(), "inner off by more than %g rel at %d places" % (FFN_REL, bad.sum())
+
+
+def assert_quant_of_inner_valid(g_xq, g_s, g_rs, o_inner):
+    """The GPU's quantisation of its own inner rows against the oracle's quantisation of the
+    oracle's inner rows: s within FFN_REL relative; every code equal to the oracle's, except
+    within 2 * FFN_REL of a rounding boundary, where either neighbour is accepted; the row sum
+    equal to the sum of the GPU's own codes. Returns the number of codes that differ."""
+    o_xq, o_s, _ = oracle.quant_act(o_inner)
+    s64, os64 = g_s.astype(np.float64), o_s.astype(np.float64)
+    assert np.all(np.abs(s64 - os64) <= FFN_REL * os64), "act scale off by more than %g rel" % FFN_REL
+    p = o_inner.astype(np.float64) * os64[:, None]
+    w = 2 * FFN_REL * np.abs(p) + 1e-12
+    lo = np.clip(np.rint(p - w), -127, 127)
+    hi = np.clip(np.rint(p + w), -127, 127)
+    g = g_xq.astype(np.float64)
+    assert np.all((g == lo) | (g == hi)), "a code differs from the oracle's away from a rounding boundary"
+    assert np.array_equal(g_rs, g_xq.astype(np.int64).sum(axis=1).astype(np.int32)), "rowsum is not the sum of xq"
+    return int(np.count_nonzero(g_xq != o_xq))
+
+
 @pytest.mark.parametrize("M,F,eps", [
     (1, 128, 1e-5), (3, 6912, 1e-5), (5, 1152, 0.25), (2, 28672, 1e-5), (7, 32768, 1e-6), (300, 2560, 1e-5),
 ])
 def test_ffn_act_quant_parity(M, F, eps):
-    """inner (bit pattern), xq, s and rowsum of the fused sub-norm + quantisation kernel against
-    oracle.ffn_inner followed by oracle.quant_act."""
+    """inner, xq, s and rowsum of the fused sub-norm + quantisation kernel against
+    oracle.ffn_inner followed by oracle.quant_act, within the bound stated above."""
     rng = np.random.default_rng(500 + F + M)
     g = (rng.standard_normal((M, F)) * 1.5).astype(np.float32)
     u = rng.standard_normal((M, F)).astype(np.float32)
@@ -645,11 +701,8 @@ def test_ffn_act_quant_parity(M, F, eps):
     g_xq, g_s, g_rs = binding.ffn_act_quant(dev(g), dev(u), dev(gamma), eps, inner_out=inner)
     torch.cuda.synchronize()
     o_inner = oracle.ffn_inner(g, u, gamma, eps)
-    o_xq, o_s, o_rs = oracle.quant_act(o_inner)
-    assert np.array_equal(host(inner).view(np.uint32), o_inner.view(np.uint32))
-    assert np.array_equal(host(g_xq), o_xq)
-    assert np.array_equal(host(g_s).view(np.uint32), o_s.view(np.uint32))
-    assert np.array_equal(host(g_rs), o_rs)
+    assert_ffn_inner_close(host(inner), o_inner)
+    assert_quant_of_inner_valid(host(g_xq), host(g_s), host(g_rs), o_inner)
 
 
 def test_ffn_act_quant_degenerate_rows():
@@ -665,22 +718,34 @@ def test_ffn_act_quant_degenerate_rows():
     gamma = _ffn_gamma(F, 511)
     g_xq, g_s, g_rs = binding.ffn_act_quant(dev(g), dev(u), dev(gamma), 1e-5)
     torch.cuda.synchronize()
-    o_xq, o_s, o_rs = oracle.quant_act(oracle.ffn_inner(g, u, gamma, 1e-5))
+    o_inner = oracle.ffn_inner(g, u, gamma, 1e-5)
+    o_xq, o_s, o_rs = oracle.quant_act(o_inner)
     assert np.all(o_xq[0] == 0) and o_s[0] == np.float32(127.0) / np.float32(1e-5)
     assert abs(int(o_xq[1, 77])) == 127
-    assert np.array_equal(host(g_xq), o_xq)
-    assert np.array_equal(host(g_s).view(np.uint32), o_s.view(np.uint32))
-    assert np.array_equal(host(g_rs), o_rs)
+    gx = host(g_xq)
+    assert np.all(gx[0] == 0) and host(g_s)[0] == o_s[0]
+    assert abs(int(gx[1, 77])) == 127 and np.count_nonzero(gx[1]) == 1
+    assert_quant_of_inner_valid(gx, host(g_s), host(g_rs), o_inner)
 
 
-def _ffn_oracle(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps):
-    """The FFN block on the CPU: quant_act -> gate/up matmuls -> ffn_inner -> quant_act -> down."""
+def _ffn_oracle_front(x_np, dtype, wg, ag, wu, au, gamma, eps):
+    """The FFN block's first half on the CPU: quant_act -> gate/up matmuls -> ffn_inner."""
     xq, s, _ = oracle.quant_act(x_np, dtype)
     gate, _ = oracle.ternary_matmul(xq, s, oracle.pack_i2s(wg)[0], ag, nthreads=NT)
     up, _ = oracle.ternary_matmul(xq, s, oracle.pack_i2s(wu)[0], au, nthreads=NT)
-    iq, i_s, i_rs = oracle.quant_act(oracle.ffn_inner(gate, up, gamma, eps))
-    out, _ = oracle.ternary_matmul(iq, i_s, oracle.pack_i2s(wd)[0], ad, nthreads=NT)
-    return dict(gate=gate, up=up, xq=iq, s=i_s, rs=i_rs, out=out)
+    return gate, up, oracle.ffn_inner(gate, up, gamma, eps)
+
+
+def check_ffn_block(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps, g_gate, g_up, g_xq, g_s, g_rs, g_out):
+    """gate/up bit for bit; the quantised inner rows valid against the oracle's inner rows;
+    the block output bit for bit equal to the oracle's down projection of the GPU's own codes
+    and scales (so the down matmul is checked exactly whatever codes sat on a boundary)."""
+    o_gate, o_up, o_inner = _ffn_oracle_front(x_np, dtype, wg, ag, wu, au, gamma, eps)
+    assert np.array_equal(g_gate.view(np.uint32), o_gate.view(np.uint32))
+    assert np.array_equal(g_up.view(np.uint32), o_up.view(np.uint32))
+    assert_quant_of_inner_valid(g_xq, g_s, g_rs, o_inner)
+    o_out, _ = oracle.ternary_matmul(g_xq, g_s, oracle.pack_i2s(wd)[0], ad, nthreads=NT)
+    assert np.array_equal(g_out.view(np.uint32), o_out.view(np.uint32))
 
 
 FFN_CASES = [
@@ -693,18 +758,9 @@ FFN_CASES = [
 ]
 
 
-@pytest.mark.parametrize("M,K,F,dtype,use_ws", FFN_CASES)
-def test_w2a8_ffn_parity(M, K, F, dtype, use_ws):
-    """gate/up outputs, the quantised inner rows and the block output, bit for bit."""
-    seed = 520 + M + F
-    x_np = workloads.activations(M, K, seed, dtype)
-    wg = workloads.ternary_weights(F, K, seed + 1)
-    wu = workloads.ternary_weights(F, K, seed + 2)
-    wd = workloads.ternary_weights(K, F, seed + 3)
-    ag, au, ad = (workloads.weight_scale(F, K, seed + 4), workloads.weight_scale(F, K, seed + 5),
-                  workloads.weight_scale(K, F, seed + 6))
-    gamma = _ffn_gamma(F, seed + 7)
-    eps = 1e-5
+def _run_ffn(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps, use_ws):
+    M, K = x_np.shape
+    F = wg.shape[0]
     g_wg, g_wu, g_wd = binding.pack_i2s(dev(wg)), binding.pack_i2s(dev(wu)), binding.pack_i2s(dev(wd))
     gate = torch.empty((M, F), dtype=torch.float32, device="cuda")
     up = torch.empty((M, F), dtype=torch.float32, device="cuda")
@@ -717,15 +773,24 @@ def test_w2a8_ffn_parity(M, K, F, dtype, use_ws):
     g_out = binding.w2a8_ffn(x_device(x_np, dtype), g_wg, ag, g_wu, au, g_wd, ad, dev(gamma), eps,
                              gate_out=gate, up_out=up, xq=xq, scale=s, rowsum=rs, workspace=ws)
     torch.cuda.synchronize()
-    o = _ffn_oracle(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps)
-    assert np.array_equal(host(gate).view(np.uint32), o["gate"].view(np.uint32))
-    assert np.array_equal(host(up).view(np.uint32), o["up"].view(np.uint32))
     # the workspace holds the quantised inner rows as a contiguous M x F array at its start
-    assert np.array_equal(host(xq).reshape(-1)[:M * F].reshape(M, F), o["xq"])
-    assert np.array_equal(host(s).view(np.uint32), o["s"].view(np.uint32))
-    assert np.array_equal(host(rs), o["rs"])
-    assert_out_close(host(g_out), o["out"])
-    assert np.array_equal(host(g_out).view(np.uint32), o["out"].view(np.uint32))
+    return (host(gate), host(up), host(xq).reshape(-1)[:M * F].reshape(M, F), host(s), host(rs), host(g_out))
+
+
+@pytest.mark.parametrize("M,K,F,dtype,use_ws", FFN_CASES)
+def test_w2a8_ffn_parity(M, K, F, dtype, use_ws):
+    """gate/up outputs and the block output bit for bit, the quantised inner rows valid."""
+    seed = 520 + M + F
+    x_np = workloads.activations(M, K, seed, dtype)
+    wg = workloads.ternary_weights(F, K, seed + 1)
+    wu = workloads.ternary_weights(F, K, seed + 2)
+    wd = workloads.ternary_weights(K, F, seed + 3)
+    ag, au, ad = (workloads.weight_scale(F, K, seed + 4), workloads.weight_scale(F, K, seed + 5),
+                  workloads.weight_scale(K, F, seed + 6))
+    gamma = _ffn_gamma(F, seed + 7)
+    eps = 1e-5
+    got = _run_ffn(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps, use_ws)
+    check_ffn_block(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps, *got)
     assert binding.last_device_error() == 0
 
 
@@ -780,28 +845,34 @@ def test_sweep_plan_parity(name, dtype, spec):
     assert binding.last_device_error() == 0
 
 
-def test_sweep_plan_matches_group_calls_on_the_decode_layer():
-    """Two 2B-4T layers through the plan equal the per-group calls on the same buffers."""
-    groups, outs_ref = [], []
-    for layer in range(2):
+def test_sweep_plan_full_decode_step_against_oracle():
+    """The whole 30-layer 2B-4T decode step (120 groups, 521 MB of packed weights) as one
+    persistent plan, every output against oracle.quant_act + oracle.ternary_matmul on the
+    step's own seeded inputs (the headline workload)."""
+    mats = {n: (N, K) for n, N, K in workloads.LAYER_MATRICES}
+    groups, refs = [], []
+    for spec in workloads.decode_sweep_specs():
         for gname, names, K in workloads.LAYER_GROUPS:
-            mats = {n: (N, Kk) for n, N, Kk in workloads.LAYER_MATRICES}
-            x = dev(workloads.activations_f32(1, K, 700 + layer * 10 + len(groups))).view(-1)
+            x_np = workloads.activations_f32(1, K, spec.act_seeds[gname])
+            xq, s, _ = oracle.quant_act(x_np)
             projs = []
             for n in names:
                 N = mats[n][0]
-                w = workloads.ternary_weights(N, K, 800 + len(groups) * 7 + len(projs))
-                projs.append((binding.pack_i2s(dev(w)), 0.016, torch.empty(N, dtype=torch.float32, device="cuda")))
-            groups.append((x, projs))
-            ref = binding.linear_group(x.view(1, -1), [p[0] for p in projs], [p[1] for p in projs])
-            outs_ref.append(ref)
+                w = workloads.ternary_weights(N, K, spec.weight_seeds[n])
+                ws = workloads.weight_scale(N, K, spec.scale_seeds[n])
+                out = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+                projs.append((binding.pack_i2s(dev(w)), ws, out))
+                refs.append(oracle.ternary_matmul(xq, s, oracle.pack_i2s(w)[0], ws, nthreads=NT)[0][0])
+            groups.append((dev(x_np).view(-1), projs))
     plan = binding.SweepPlan(groups)
     plan.run()
     torch.cuda.synchronize()
-    for (x, projs), ref in zip(groups, outs_ref):
-        for (_, _, out), r in zip(projs, ref):
-            assert torch.equal(out.view(torch.int32), r.view(-1).view(torch.int32))
+    outs = [p[2] for _, projs in groups for p in projs]
+    assert len(outs) == len(refs) == 30 * 7
+    for got, ref in zip(outs, refs):
+        assert np.array_equal(host(got).view(np.uint32), ref.view(np.uint32))
     plan.close()
+    assert binding.last_device_error() == 0
 
 
 # ----------------------------------------------------------------------------- few token rows
@@ -904,12 +975,8 @@ def test_random_ffn_blocks(case):
     ag, au, ad = (float(v) for v in rng.uniform(0.005, 0.05, 3))
     gamma = workloads.rmsnorm_gamma(F, 7740 + case)
     use_ws = M > 64 and bool(case % 3)
-    ws = (torch.empty(binding.ffn_workspace_size(M, K, F), dtype=torch.uint8, device="cuda") if use_ws else None)
-    g_out = binding.w2a8_ffn(x_device(x_np, dtype), binding.pack_i2s(dev(wg)), ag, binding.pack_i2s(dev(wu)), au,
-                             binding.pack_i2s(dev(wd)), ad, dev(gamma), 1e-5, workspace=ws)
-    torch.cuda.synchronize()
-    o = _ffn_oracle(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, 1e-5)
-    assert np.array_equal(host(g_out).view(np.uint32), o["out"].view(np.uint32)), (M, K, F)
+    got = _run_ffn(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, 1e-5, use_ws)
+    check_ffn_block(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, 1e-5, *got)
     assert binding.last_device_error() == 0
 
 
