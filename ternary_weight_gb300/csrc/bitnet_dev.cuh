@@ -399,6 +399,14 @@ cudaError_t launch_gemv_ring(const int8_t* xq, const float* act_scale, const int
                              cudaStream_t stream);
 cudaError_t read_clear_device_error_gemv_ring(int* value);
 
+// Prompt-length tensor-core matmul without a workspace (gemm_prefill.cu): TMA-staged packed
+// weights and int8 tokens, expanded to exact fp16 in the kernel; K <= 32768.
+bool gemm_prefill_supported(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_prefill(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
+                                float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
+                                int num_sms, cudaStream_t stream);
+cudaError_t read_clear_device_error_prefill(int* value);
+
 // Few-token tensor-core matmul (gemm_smallm.cu): any M (64 tokens per CTA), K <= 32768.
 bool gemm_smallm_supported(int64_t M, int64_t K);
 cudaError_t launch_gemm_smallm(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,

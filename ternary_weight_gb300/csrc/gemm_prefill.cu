@@ -1,0 +1,563 @@
+// gemm_prefill.cu -- the W2A8 ternary matmul for prompts (from ~100 tokens on) on the tensor cores,
+// with no workspace: the packed weights and the int8 activations are staged by TMA and expanded to
+// exact fp16 inside the kernel.
+//
+// Computes, like every other path of the library, raw[m][n] = sum_k code[n][k] * xq[m][k],
+// acc = raw - rowsum[m], out = (acc / s[m]) * w_scale, with the same integers and the same fp32
+// results. Sources: the raw code dot over the 4x32-interleaved i2_s bytes ("[분석/검증-3]
+// BitNet.cpp ARM 커널 재작성" §3, "[기술 분석 보고서] ... 추론 붕괴 원인 분석" §3.2), the byte
+// layout ("BitNet 딥다이브" §4-2), the dequantisation ("bitnet.rs" "Quantised Forward Pass").
+// "BitNet 딥다이브" §4-5 runs prefill as a separate dense path; this is that path.
+//
+// Tile: 256 weight rows (two MMA tiles of 128: the MMA's M) x 128 tokens (the MMA's N) x a range
+// of 128-k i2_s blocks. The contraction is tcgen05.mma.cta_group::1.kind::f16, M = 128, N = 128,
+// K = 16, fp32 accumulation in tensor memory. Both operands are exact:
+//  * A (weights): the code c in {0..3} as the fp16 subnormal c * 2^-24 (bit pattern c), written by
+//    the converter threads straight into tensor memory with tcgen05.st (two shifts and two masks
+//    give four codes as two fp16 pairs); the expanded weights never touch shared memory;
+//  * B (tokens): the int8 value as an exact fp16 (0x6400 | (x + 128) = 1152 + x, minus 1152),
+//    written into a 128-byte-swizzled K-major shared-memory tile that both weight tiles use;
+//  * every product is c * x * 2^-24 and every partial sum an integer multiple of 2^-24 of
+//    magnitude below 3 * 127 * K * 2^-24 < 1 for K <= 32768: the fp32 accumulators are exact, and
+//    the epilogue's fma(D, 2^24, -rowsum) gives the integer acc = raw - rowsum exactly.
+// K order inside a 64-k stage: the MMA only needs A and B to agree. Word q of a row's 32 staged
+// bytes and bit pair j give, by (w >> (6 - 2j)) & 0x00030003 and the same shifted by 8 more, the
+// codes of bytes (0, 2) and (1, 3) as fp16 pairs; so stage position p holds k = 4 (p / 4) +
+// sigma(p % 4) (plus 32 role) with sigma = (0, 2, 1, 3), and the token bytes are laid out in B in
+// the same order by the byte permutes that convert them.
+//
+// Pipeline, per 128-k block b of the CTA's range (two 64-k stages, h = 0, 1):
+//  * warp 0, one lane: 2-D TMA (cp.async.bulk.tensor) of the block's packed weights (256 rows x
+//    32 bytes) and int8 tokens (128 rows x 128 bytes) into a staging slot (4 slots); the weights
+//    of the first slots are requested before the dependency wait on the previous kernel;
+//  * warps 2-17 (16 converters): per stage, warp (tile, lane quarter, role) turns bit pair
+//    2h + role of its 32 rows into 16 tensor-memory columns of A, and each thread turns one
+//    16-byte piece of token bytes into two fp16 chunks of B; then fences and one arrival per warp;
+//  * warp 1, one lane: per stage 2 x 4 MMAs (both weight tiles, four k16 steps), then a commit
+//    that releases the stage (A columns and B tile) to the converters.
+// The lanes of warps 0 and 1 that do not issue wait at a warp barrier: a lane suspended in an
+// mbarrier poll would hold back the issuing lane of its warp.
+//
+// Epilogue. The division out = RN(RN(acc / s) * w_scale) is exact and branch-free: with the
+// per-token y = RN(1/s) (the correctly rounded reciprocal), q = RN(acc * y) and two residual
+// corrections r = fma(-q, s, acc) (exact), q = fma(r, y, q) give RN(acc / s) (Markstein's method;
+// the first correction makes q faithful, the second rounds correctly). Tokens whose s lies outside
+// [2^-100, 2^100] (quotients that could overflow) take the IEEE division instead. The finished
+// values go to a token-major staging tile in the freed rings and leave by TMA bulk stores (which
+// clip the ragged edges), or, when the output rows are not 16-byte aligned or the int32
+// accumulators are requested too, by plain stores with consecutive lanes on consecutive n.
+// Split K: for short prompts the blocks of one tile are spread over a thread-block cluster of up
+// to 16 CTAs (as many as make every CTA resident at once). Every CTA stages its exact partials
+// token-major in its own shared memory; after a cluster barrier, rank r finishes the tokens
+// [128 r / cs, 128 (r + 1) / cs) of the tile, pulling the peers' partials with coalesced
+// distributed-shared-memory loads; a second cluster barrier keeps every CTA's partials alive until
+// its peers have read them.
+// Every mbarrier wait is bounded; a timeout is recorded in the device error word, and the TMA
+// producer always waits (bounded) for its last copies before it leaves.
+#include "bitnet_dev.cuh"
+
+#include <atomic>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+namespace bitnet {
+namespace {
+
+constexpr int TWR = 256;                 // weight rows per CTA (two MMA tiles)
+constexpr int TT = 128;                  // tokens per CTA (the MMA's N)
+constexpr int CONV_WARPS = 16;           // converters, then the epilogue
+constexpr int CONV_THREADS = CONV_WARPS * 32;
+constexpr int THREADS = CONV_THREADS + 64;
+constexpr int NSS = 4;                   // staging slots (one 128-k block each)
+constexpr int NAB = 4;                   // A/B stages (64 k each)
+constexpr int STG_W = TWR * 32;          // staged packed weights of one block: 256 rows x 32 bytes
+constexpr int STG_X = TT * 128;          // staged int8 tokens of one block: 128 rows x 128 bytes
+constexpr int STG_BYTES = STG_W + STG_X;
+constexpr int B_STAGE = TT * 128;        // fp16 B tile of one stage: 128 rows x 64 k x 2 bytes
+constexpr int SMEM = 1024 + NAB * B_STAGE + NSS * STG_BYTES;
+constexpr int OUT_STAGE = TT * TWR * 4;  // token-major fp32 tile (epilogue; reuses the rings)
+constexpr uint32_t TMEM_COLS = 512;      // accumulators (2 x 128) + A stages (4 x 2 x 32)
+constexpr int ACC_COLS = 2 * TT;
+constexpr int A_STAGE_COLS = 64;         // both tiles: 2 x 32 columns (64 fp16 of k per lane)
+constexpr int kMaxCluster = 16;
+constexpr int kStoreRows = 32;           // tokens per TMA store of a whole tile (cluster size 1)
+constexpr int BAR_ALL = 1;               // named barrier of the whole CTA
+constexpr uint32_t IDESC = make_idesc_f16_f32(128, TT);
+static_assert(ACC_COLS + NAB * A_STAGE_COLS <= (int)TMEM_COLS, "tensor memory columns");
+static_assert(SMEM <= 227 * 1024 - 4096, "shared memory (static part included)");
+static_assert(OUT_STAGE <= NAB * B_STAGE + NSS * STG_BYTES, "the epilogue tile fits the reused rings");
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// shared -> global tile store by the TMA engine (elements outside the tensor are not written)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every bulk store of this thread has finished reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void sts32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float lds32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is 128 lanes (rows) x 8 columns (16 fp16
+// along K, two per column, the lower position in the low half).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp writes lane (base + t).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// four int8 -> four exact fp16 (as two fp16x2 words), in the stage's position order: bytes (0, 2)
+// then bytes (1, 3)
+__device__ __forceinline__ void s8x4_f16_perm(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;                      // x + 128 per byte
+  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4240);  // 0x64uu: 1024 + (x + 128)
+  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4341);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
+}
+
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// RN(a / s) for an integer-valued a (|a| < 2^25) and s in [2^-100, 2^100], given y = RN(1/s):
+// Markstein's residual correction, twice (exact remainders by fma).
+__device__ __forceinline__ float div_by_scale(float a, float s, float y) {
+  float q = __fmul_rn(a, y);
+  float r = __fmaf_rn(-q, s, a);
+  q = __fmaf_rn(r, y, q);
+  r = __fmaf_rn(-q, s, a);
+  return __fmaf_rn(r, y, q);
+}
+
+struct TokenConst {  // per token of the tile, in shared memory
+  float s, y, rs;    // act scale, RN(1/s), -rowsum (exact)
+  uint32_t fast;     // s within [2^-100, 2^100]
+};
+
+__device__ __forceinline__ float finish(float d, const TokenConst& c, float w_scale, int* acc_int) {
+  const float a = __fmaf_rn(d, 16777216.0f, c.rs);  // raw - rowsum, exactly (an integer below 2^25)
+  *acc_int = __float2int_rn(a);
+  const float q = c.fast ? div_by_scale(a, c.s, c.y) : __fdiv_rn(a, c.s);
+  return __fmul_rn(q, w_scale);
+}
+
+__global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                  const __grid_constant__ CUtensorMap tmX,
+                                                                  const __grid_constant__ CUtensorMap tmO,
+                                                                  const float* __restrict__ act_scale,
+                                                                  const int32_t* __restrict__ rowsum, float w_scale,
+                                                                  float* __restrict__ out,
+                                                                  int32_t* __restrict__ acc_out, int M, int N, int K,
+                                                                  int tma_store) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_stg[NSS];   // a block's bytes have landed (TMA transaction bytes)
+  __shared__ __align__(8) uint64_t empty_stg[NSS];  // the converters are done with a staging slot
+  __shared__ __align__(8) uint64_t full_ab[NAB];    // a stage's A columns and B tile are written
+  __shared__ __align__(8) uint64_t empty_ab[NAB];   // the MMAs reading a stage are done (one commit)
+  __shared__ __align__(8) uint64_t done_bar;        // every MMA complete
+  __shared__ uint32_t tmem_slot;
+  __shared__ TokenConst tok[TT];
+
+  pdl_launch_dependents();
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = raw_addr + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t bring = base;                      // NAB fp16 B tiles (1024-byte aligned)
+  const uint32_t stg = base + NAB * B_STAGE;        // NSS staging slots: weights, then tokens
+  const uint32_t ostage = base;                     // epilogue: [token][row] fp32 (after the MMAs)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * TWR, m0 = blockIdx.z * TT;
+  const int cs = (int)gridDim.y;
+  const int rank = cs > 1 ? (int)cluster_ctarank() : 0;
+  const int nblk_all = K / 128;
+  const int b_lo = nblk_all * rank / cs, b_hi = nblk_all * (rank + 1) / cs;
+  const int nblk = b_hi - b_lo, nst = 2 * nblk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSS; ++s) {
+      mbar_init(&full_stg[s], 1);
+      mbar_init(&empty_stg[s], CONV_WARPS);
+    }
+    for (int s = 0; s < NAB; ++s) {
+      mbar_init(&full_ab[s], CONV_WARPS);
+      mbar_init(&empty_ab[s], 1);
+    }
+    mbar_init(&done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  bool abort = false;
+
+  if (warp == 0) {
+    // ================================ TMA producer ================================
+    if (lane == 0) {
+      int issued = 0;
+      // weights do not depend on the previous kernel: the first slots' weights go before the wait
+      const int pre = nblk < NSS ? nblk : NSS;
+      for (int b = 0; b < pre; ++b) {
+        mbar_arrive_expect_tx(&full_stg[b], STG_BYTES);
+        tma_load_2d(stg + b * STG_BYTES, &tmW, 32 * (b_lo + b), n0, &full_stg[b]);
+      }
+      pdl_wait();  // the tokens may be the previous kernel's output
+      for (int b = 0; b < pre; ++b) tma_load_2d(stg + b * STG_BYTES + STG_W, &tmX, 128 * (b_lo + b), m0, &full_stg[b]);
+      issued = pre;
+      for (int b = pre; b < nblk; ++b) {
+        const int slot = b % NSS, use = b / NSS;
+        if (!mbar_wait(&empty_stg[slot], (uint32_t)(use - 1) & 1u, &abort)) break;
+        mbar_arrive_expect_tx(&full_stg[slot], STG_BYTES);
+        tma_load_2d(stg + slot * STG_BYTES, &tmW, 32 * (b_lo + b), n0, &full_stg[slot]);
+        tma_load_2d(stg + slot * STG_BYTES + STG_W, &tmX, 128 * (b_lo + b), m0, &full_stg[slot]);
+        issued = b + 1;
+      }
+      {  // every copy issued lands before the producer leaves (the converters may have given up)
+        bool dummy = false;
+        for (int i = issued - NSS > 0 ? issued - NSS : 0; i < issued; ++i)
+          mbar_wait(&full_stg[i % NSS], (uint32_t)(i / NSS) & 1u, &dummy);
+      }
+    }
+    // The other lanes wait here, at a warp barrier, not in a polling loop of their own: a lane
+    // suspended in mbarrier.try_wait holds back the whole warp, the producing lane included.
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================ MMA issuer ================================
+    if (lane == 0) {
+      const uint64_t bdesc0 = make_sw128_kmajor_desc(bring);
+      const uint32_t acol0 = tmem + (uint32_t)ACC_COLS;
+      for (int i = 0; i < nst; ++i) {
+        const int s = i % NAB;
+        if (!mbar_wait(&full_ab[s], (uint32_t)(i / NAB) & 1u, &abort)) break;
+        tc_fence_after();
+        const uint32_t a_col = acol0 + (uint32_t)(s * A_STAGE_COLS);
+        const uint64_t bd = bdesc0 + (uint64_t)((s * B_STAGE) >> 4);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma_f16_ts(tmem + (uint32_t)(t * TT), a_col + (uint32_t)(32 * t + 8 * j), bd + (uint64_t)((32 * j) >> 4),
+                       IDESC, (i > 0 || j > 0) ? 1u : 0u);
+        mma_commit(&empty_ab[s]);
+      }
+      mma_commit(&done_bar);  // tracks every MMA this thread issued
+    }
+    __syncwarp();  // as for the producer: the idle lanes must not poll beside the issuing lane
+  } else {
+    // ================================ converters ================================
+    const int cw = warp - 2;                  // 0..15
+    const int quarter = warp & 3, tile = (cw >> 2) & 1, role = cw >> 3;
+    const int row = tile * 128 + 32 * quarter + lane;  // this thread's weight row in the tile
+    const int ct = cw * 32 + lane;            // 0..511: this thread's token piece
+    const int pt = ct >> 2, pc = ct & 3;      // token, 16-k chunk of the stage
+    const uint32_t a_lane =
+        tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ACC_COLS + 32 * tile + 16 * role);
+    uint32_t w[8];
+    for (int i = 0; i < nst; ++i) {
+      const int b = i >> 1, h = i & 1, slot = b % NSS, s = i % NAB;
+      const uint32_t sb = stg + slot * STG_BYTES;
+      if (h == 0) {
+        if (!mbar_wait_warp(&full_stg[slot], (uint32_t)(b / NSS) & 1u, &abort)) break;
+        const uint4 v0 = lds_v4(sb + row * 32), v1 = lds_v4(sb + row * 32 + 16);
+        w[0] = v0.x, w[1] = v0.y, w[2] = v0.z, w[3] = v0.w, w[4] = v1.x, w[5] = v1.y, w[6] = v1.z, w[7] = v1.w;
+      }
+      const uint4 xv = lds_v4(sb + STG_W + pt * 128 + 64 * h + 16 * pc);  // 16 k of token pt
+      if (i >= NAB && !mbar_wait_warp(&empty_ab[s], (uint32_t)(i / NAB - 1) & 1u, &abort)) break;
+      tc_fence_after();
+      {  // A: bit pair 2h + role of the row's 32 bytes -> 16 columns (word q: columns 2q, 2q + 1)
+        const int sh = 6 - 2 * (2 * h + role);
+        uint32_t a[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          a[2 * q] = (w[q] >> sh) & 0x00030003u;            // bytes 0, 2: fp16 subnormals c * 2^-24
+          a[2 * q + 1] = (w[q] >> (sh + 8)) & 0x00030003u;  // bytes 1, 3
+        }
+        tmem_st_32x32b_x16(a_lane + (uint32_t)(s * A_STAGE_COLS), a);
+      }
+      {  // B: 16 int8 -> 32 bytes of fp16 = chunks 2pc, 2pc + 1 of the token's row
+        uint32_t f[8];
+        s8x4_f16_perm(xv.x, f[0], f[1]);
+        s8x4_f16_perm(xv.y, f[2], f[3]);
+        s8x4_f16_perm(xv.z, f[4], f[5]);
+        s8x4_f16_perm(xv.w, f[6], f[7]);
+        const uint32_t bt = bring + (uint32_t)(s * B_STAGE);
+        sts128(bt + sw128(pt, 2 * pc), f[0], f[1], f[2], f[3]);
+        sts128(bt + sw128(pt, 2 * pc + 1), f[4], f[5], f[6], f[7]);
+      }
+      tmem_st_wait();            // this thread's tensor-memory writes are complete
+      fence_proxy_async_smem();  // its shared-memory writes -> the tensor core's reads
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&full_ab[s]);
+        if (h == 1) mbar_arrive(&empty_stg[slot]);  // every staged byte of the block has been used
+      }
+    }
+    // the tile's per-token constants (the scales and row sums are the previous kernel's output)
+    pdl_wait();
+    if (ct < TT) {
+      const int m = m0 + ct;
+      const float sc = m < M ? __ldg(act_scale + m) : 1.0f;
+      TokenConst c;
+      c.s = sc;
+      c.y = __frcp_rn(sc);
+      c.rs = -(float)(m < M ? __ldg(rowsum + m) : 0);
+      c.fast = (sc >= 0x1p-100f && sc <= 0x1p100f) ? 1u : 0u;
+      tok[ct] = c;
+    }
+  }
+
+  // ---- every MMA done: the rings are free ----
+  const bool conv = warp >= 2;
+  bool have = false;
+  {
+    bool dummy = false;
+    if (conv)
+      have = mbar_wait_warp(&done_bar, 0, &abort);
+    else
+      mbar_wait_warp(&done_bar, 0, &dummy);
+  }
+  tc_fence_after();
+  __syncthreads();  // tok[] written; every MMA read of the rings done
+
+  const int cw = warp - 2, quarter = warp & 3, tile = (cw >> 2) & 1, role = cw >> 3;
+  const int row = tile * 128 + 32 * quarter + lane;  // the accumulator row this thread reads
+  const int n = n0 + row;
+  const uint32_t tacc = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(tile * TT);
+  const bool plain = !tma_store;  // else: TMA stores of the staged tile
+
+  if (cs == 1) {
+    // the whole tile is this CTA's: finish straight from the accumulators
+    if (conv && have) {
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int cb = 64 * role + 32 * cc;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + (uint32_t)cb, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int t = cb + e;
+          int ai;
+          const float o = finish(__uint_as_float(v[e]), tok[t], w_scale, &ai);
+          if (plain) {
+            const int m = m0 + t;
+            if (m < M && n < N) {
+              out[(int64_t)m * N + n] = o;
+              if (acc_out) acc_out[(int64_t)m * N + n] = ai;
+            }
+          } else {
+            sts32(ostage + (uint32_t)((t * TWR + row) * 4), o);
+          }
+        }
+      }
+    }
+  } else {
+    // split K: stage this CTA's exact partials, then finish the owned tokens from every CTA's
+    if (conv && have) {
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int cb = 64 * role + 32 * cc;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + (uint32_t)cb, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sts32(ostage + (uint32_t)(((cb + e) * TWR + row) * 4), __uint_as_float(v[e]));
+      }
+    }
+    cluster_arrive_release();  // this CTA's partials are staged
+    cluster_wait_acquire();    // and every peer's
+    if (conv && have) {
+      const int t_lo = TT * rank / cs, t_hi = TT * (rank + 1) / cs;
+      const int ct = cw * 32 + lane, crow = ct & (TWR - 1), cn = n0 + crow;
+#pragma unroll 1
+      for (int t = t_lo + (ct >> 8); t < t_hi; t += 2) {
+        const uint32_t off = ostage + (uint32_t)((t * TWR + crow) * 4);
+        float d = lds32(off);
+        for (int p = 0; p < cs; ++p)
+          if (p != rank) d = __fadd_rn(d, ld_cluster_f32(map_to_rank(off, (uint32_t)p)));
+        int ai;
+        const float o = finish(d, tok[t], w_scale, &ai);
+        if (plain) {
+          const int m = m0 + t;
+          if (m < M && cn < N) {
+            out[(int64_t)m * N + cn] = o;
+            if (acc_out) acc_out[(int64_t)m * N + cn] = ai;
+          }
+        } else {
+          sts32(off, o);  // peers only read the tokens they own
+        }
+      }
+    }
+  }
+
+  if (!plain) {  // the finished token rows leave by TMA bulk stores
+    fence_proxy_async_smem();
+    named_bar_sync(BAR_ALL, THREADS);
+    if (threadIdx.x == 0 && !abort) {
+      if (cs == 1) {
+        for (int t = 0; t < TT && m0 + t < M; t += kStoreRows) tma_store_2d(&tmO, n0, m0 + t, ostage + (uint32_t)(t * TWR * 4));
+      } else {
+        const int t_lo = TT * rank / cs, t_hi = TT * (rank + 1) / cs;
+        for (int t = t_lo; t < t_hi && m0 + t < M; ++t) tma_store_2d(&tmO, n0, m0 + t, ostage + (uint32_t)(t * TWR * 4));
+      }
+      bulk_commit();
+      bulk_wait_read();  // the staged tile stays until the engine has read it
+    }
+  }
+  if (cs > 1) {  // no CTA leaves while a peer may still read its staged partials
+    cluster_arrive_release();
+    cluster_wait_acquire();
+  }
+
+  // ---- teardown: every MMA completes before the tensor memory is freed ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// 2-D tensor [rows][inner] of 1- or 4-byte elements, box box_inner x box_rows, no swizzle.
+bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base, int64_t rows, int64_t inner,
+              int box_inner, int box_rows) {
+  return encode_map_2d(map, dt, base, (uint64_t)inner, (uint64_t)rows, (uint64_t)(inner * esize),
+                       (uint32_t)box_inner, (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace
+
+cudaError_t read_clear_device_error_prefill(int* value) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+}
+
+bool gemm_prefill_supported(int64_t M, int64_t N, int64_t K) {
+  return M >= 1 && N >= 1 && K >= 128 && K % 128 == 0 && K <= 32768 && (M + TT - 1) / TT <= 65535 &&
+         (N + TWR - 1) / TWR <= 0x7fffffff;
+}
+
+cudaError_t launch_gemm_prefill(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
+                                float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K,
+                                int num_sms, cudaStream_t stream) {
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gemm_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_prefill_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  // One CTA per SM (the shared memory allows one). Tiles = weight tiles x token tiles; when they
+  // leave SMs idle, the blocks of K are split over a cluster of cs CTAs, as large as lets every
+  // CTA run at once (at least one block each, at most 16), checked with the occupancy query.
+  const int64_t n_w = (N + TWR - 1) / TWR, n_t = (M + TT - 1) / TT, tiles = n_w * n_t;
+  const int64_t nblk = K / 128;
+  int64_t cs = num_sms / tiles;
+  if (cs > kMaxCluster) cs = kMaxCluster;
+  if (cs > nblk) cs = nblk;
+  if (cs < 1) cs = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  for (; cs > 1; --cs) {
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    cfg.gridDim = dim3((unsigned)n_w, (unsigned)cs, (unsigned)n_t);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_prefill_kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();  // the query is only a hint; keep shrinking to the portable size
+      if (cs <= 8) break;
+      continue;
+    }
+    if (clusters >= tiles) break;
+  }
+  attr[0].val.clusterDim.y = (unsigned)cs;
+  cfg.gridDim = dim3((unsigned)n_w, (unsigned)cs, (unsigned)n_t);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
+
+  CUtensorMap mW, mX, mO;
+  if (!make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, N, K / 4, 32, TWR) ||
+      !make_map(&mX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, M, K, 128, TT))
+    return cudaErrorInvalidValue;
+  // The finished tile leaves by TMA stores when the output rows are 16-byte aligned and the
+  // int32 accumulators are not wanted; otherwise element by element.
+  const bool tma_store = (N % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15) == 0 && acc_out == nullptr;
+  std::memset(&mO, 0, sizeof(mO));
+  if (tma_store && !make_map(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, M, N, TWR, cs == 1 ? kStoreRows : 1))
+    return cudaErrorInvalidValue;
+  return cudaLaunchKernelEx(&cfg, gemm_prefill_kernel, mW, mX, mO, act_scale, rowsum, w_scale, out, acc_out, (int)M,
+                            (int)N, (int)K, tma_store ? 1 : 0);
+}
+
+}  // namespace bitnet

@@ -210,6 +210,27 @@ def test_chain_parity_gemm(M, N, K, dtype):
     assert_chain_equal(g, o)
 
 
+# The prompt-length kernel, forced: M = 1 and M below one 128-token tile, ragged token tiles
+# (129, 300), ragged weight tiles (N not a multiple of 256, N < 128), one 128-k block, K splits over
+# clusters of every size the launch picks (1 to 16 CTAs: few tiles and long K), several token
+# tiles with splits, and the 2B-4T prefill shapes.
+PREFILL_CHAIN = [
+    (1, 256, 128, "f32"), (5, 77, 2560, "bf16"), (64, 300, 384, "f32"), (127, 257, 1024, "bf16"),
+    (128, 6912, 2560, "bf16"), (128, 2560, 6912, "bf16"), (129, 513, 1024, "f32"), (200, 1000, 6912, "bf16"),
+    (300, 700, 2560, "bf16"), (256, 640, 8192, "bf16"), (512, 6912, 2560, "bf16"), (130, 100, 32768, "bf16"),
+    (640, 2560, 1152, "f32"), (1000, 129, 256, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype", PREFILL_CHAIN)
+def test_chain_parity_prefill(M, N, K, dtype):
+    x = workloads.activations(M, K, seed=410 + M, dtype=dtype, outlier_p=0.01)
+    w = workloads.ternary_weights(N, K, seed=411 + N)
+    g, o = run_chain(x, dtype, w, workloads.weight_scale(N, K, 412), algo="prefill")
+    assert_chain_equal(g, o)
+    assert binding.last_device_error() == 0
+
+
 def _matmul_only(xq, s, wp, w_scale, algo):
     rs = xq.astype(np.int64).sum(axis=1).astype(np.int32)
     M, N = xq.shape[0], wp.shape[0]
@@ -218,7 +239,7 @@ def _matmul_only(xq, s, wp, w_scale, algo):
     return host(out), host(acc)
 
 
-@pytest.mark.parametrize("algo", ["gemv", "gemm"])
+@pytest.mark.parametrize("algo", ["gemv", "gemm", "prefill"])
 def test_max_magnitude_accumulators(algo):
     """xq all +-127 against all-(+1) weights: |acc| = 127*K, the largest a ternary row gives."""
     K, N, M = 8192, 260, 3
@@ -233,8 +254,8 @@ def test_max_magnitude_accumulators(algo):
     assert np.array_equal(out.view(np.uint32), o_out.view(np.uint32))
 
 
-@pytest.mark.parametrize("algo", ["gemv", "gemm"])
-@pytest.mark.parametrize("M,N,K", [(5, 77, 2560), (130, 300, 1024)])
+@pytest.mark.parametrize("algo", ["gemv", "gemm", "prefill"])
+@pytest.mark.parametrize("M,N,K", [(5, 77, 2560), (130, 300, 1024), (256, 1000, 32768)])
 def test_random_bytes_including_code3(algo, M, N, K):
     """Arbitrary packed bytes (code 3 included, read as +2 by the c - 1 rule)."""
     wp = workloads.random_packed_bytes(N, K, seed=500 + M)
@@ -319,7 +340,7 @@ def test_full_size_configs(case):
 
 
 FULL_PREFILL_PATHS = [(c, p) for c in workloads.prefill_cases() + workloads.large_cases()[:1]
-                      for p in ("smallm", "ws")]
+                      for p in ("smallm", "ws", "prefill")]
 
 
 @pytest.mark.parametrize("case,path", FULL_PREFILL_PATHS, ids=lambda v: v if isinstance(v, str) else v.name)
