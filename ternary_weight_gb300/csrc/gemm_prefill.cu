@@ -22,17 +22,20 @@
 //    the epilogue's fma(D, 2^24, -rowsum) gives the integer acc = raw - rowsum exactly.
 // K order inside a 64-k stage: the MMA only needs A and B to agree. Word q of a row's 32 staged
 // bytes and bit pair j give, by (w >> (6 - 2j)) & 0x00030003 and the same shifted by 8 more, the
-// codes of bytes (0, 2) and (1, 3) as fp16 pairs; so stage position p holds k = 4 (p / 4) +
-// sigma(p % 4) (plus 32 role) with sigma = (0, 2, 1, 3), and the token bytes are laid out in B in
-// the same order by the byte permutes that convert them.
+// codes of bytes (0, 2) and (1, 3) as fp16 pairs; so stage position p holds the stage's k =
+// 4 (p / 4) + sigma(p % 4) with sigma = (0, 2, 1, 3), and the token bytes are laid out in B in the
+// same order by the byte permutes that convert them.
 //
 // Pipeline, per 128-k block b of the CTA's range (two 64-k stages, h = 0, 1):
 //  * warp 0, one lane: 2-D TMA (cp.async.bulk.tensor) of the block's packed weights (256 rows x
-//    32 bytes) and int8 tokens (128 rows x 128 bytes) into a staging slot (4 slots); the weights
-//    of the first slots are requested before the dependency wait on the previous kernel;
-//  * warps 2-17 (16 converters): per stage, warp (tile, lane quarter, role) turns bit pair
-//    2h + role of its 32 rows into 16 tensor-memory columns of A, and each thread turns one
-//    16-byte piece of token bytes into two fp16 chunks of B; then fences and one arrival per warp;
+//    32 bytes) and int8 tokens (two boxes of 128 rows x 64 bytes, one per stage, so that the
+//    converters' 16-byte reads of two neighbouring rows fall in different banks) into a staging
+//    slot (4 slots); the weights of the first slots are requested before the dependency wait;
+//  * warps 2-17 (16 converters) in two groups of 8 that take alternate stages (group g the stages
+//    with h = g), so that each warp has two stage periods for its chain of loads, conversion,
+//    tensor-memory store, fences and arrival: warp (tile, lane quarter) turns bit pairs 2h and
+//    2h + 1 of its 32 rows into 32 tensor-memory columns of A, and each thread turns two 16-byte
+//    pieces of token bytes into fp16 chunks of B; then fences and one arrival per warp;
 //  * warp 1, one lane: per stage 2 x 4 MMAs (both weight tiles, four k16 steps), then a commit
 //    that releases the stage (A columns and B tile) to the converters.
 // The lanes of warps 0 and 1 that do not issue wait at a warp barrier: a lane suspended in an
@@ -44,14 +47,18 @@
 // the first correction makes q faithful, the second rounds correctly). Tokens whose s lies outside
 // [2^-100, 2^100] (quotients that could overflow) take the IEEE division instead. The finished
 // values go to a token-major staging tile in the freed rings and leave by TMA bulk stores (which
-// clip the ragged edges), or, when the output rows are not 16-byte aligned or the int32
-// accumulators are requested too, by plain stores with consecutive lanes on consecutive n.
+// clip the ragged edges), 32 tokens per store as soon as both weight tiles have finished them, or,
+// when the output rows are not 16-byte aligned or the int32 accumulators are requested too, by
+// plain stores with consecutive lanes on consecutive n.
 // Split K: for short prompts the blocks of one tile are spread over a thread-block cluster of up
-// to 16 CTAs (as many as make every CTA resident at once). Every CTA stages its exact partials
-// token-major in its own shared memory; after a cluster barrier, rank r finishes the tokens
-// [128 r / cs, 128 (r + 1) / cs) of the tile, pulling the peers' partials with coalesced
-// distributed-shared-memory loads; a second cluster barrier keeps every CTA's partials alive until
-// its peers have read them.
+// to 16 CTAs (as many as make every CTA resident at once). Every CTA stages its exact partials as
+// int32, token-major, in its own shared memory; after a cluster barrier rank r owns the tokens
+// [8 floor(16 r / cs), 8 floor(16 (r + 1) / cs)) of the tile. With up to 3 CTAs every other rank
+// adds its partials of that range into r's staging with one bulk reduction (cp.reduce.async.bulk,
+// int32 add, by the TMA engine), counted in bytes on r's receive barrier; with more, r pulls them
+// with 16-byte distributed-shared-memory loads, every peer's requested before any is added. r
+// finishes its tokens in place and stores them; a second cluster barrier keeps every CTA alive
+// until its shared memory is no longer read or written by a peer.
 // Every mbarrier wait is bounded; a timeout is recorded in the device error word, and the TMA
 // producer always waits (bounded) for its last copies before it leaves.
 #include "bitnet_dev.cuh"
@@ -71,7 +78,7 @@ constexpr int THREADS = CONV_THREADS + 64;
 constexpr int NSS = 4;                   // staging slots (one 128-k block each)
 constexpr int NAB = 4;                   // A/B stages (64 k each)
 constexpr int STG_W = TWR * 32;          // staged packed weights of one block: 256 rows x 32 bytes
-constexpr int STG_X = TT * 128;          // staged int8 tokens of one block: 128 rows x 128 bytes
+constexpr int STG_X = TT * 128;          // staged int8 tokens of one block: [half][128 rows][64 bytes]
 constexpr int STG_BYTES = STG_W + STG_X;
 constexpr int B_STAGE = TT * 128;        // fp16 B tile of one stage: 128 rows x 64 k x 2 bytes
 constexpr int SMEM = 1024 + NAB * B_STAGE + NSS * STG_BYTES;
@@ -82,7 +89,16 @@ constexpr int A_STAGE_COLS = 64;         // both tiles: 2 x 32 columns (64 fp16 
 constexpr int kMaxCluster = 16;
 constexpr int kStoreRows = 32;           // tokens per TMA store of a whole tile (cluster size 1)
 constexpr int BAR_ALL = 1;               // named barrier of the whole CTA
+constexpr int BAR_HALF = 2;              // named barriers 2, 3: the converter warps of one token half
 constexpr uint32_t IDESC = make_idesc_f16_f32(128, TT);
+// split K: rank r of a cluster of cs finishes tokens [tok_lo(r), tok_lo(r + 1)) of the tile, in
+// whole groups of 8 (every rank has at least one group for cs <= 16)
+__host__ __device__ constexpr int tok_lo(int r, int cs) { return 8 * (16 * r / cs); }
+// Up to this cluster size the peers' partials are added by bulk reductions (few large transfers
+// per CTA); beyond it each owner pulls them with 16-byte distributed-shared-memory loads (many
+// peers, few tokens each), which measured faster there (2B-4T FFN shapes: at 2 CTAs 20.7 against
+// 25.4 us, at 5 CTAs 19.1 against 14.9 us, at 10 CTAs 23.0 against 15.3 us).
+constexpr int kReduceMaxCluster = 3;
 static_assert(ACC_COLS + NAB * A_STAGE_COLS <= (int)TMEM_COLS, "tensor memory columns");
 static_assert(SMEM <= 227 * 1024 - 4096, "shared memory (static part included)");
 static_assert(OUT_STAGE <= NAB * B_STAGE + NSS * STG_BYTES, "the epilogue tile fits the reused rings");
@@ -105,8 +121,8 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int 
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// every bulk store of this thread has finished reading its shared-memory source
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every bulk store of this thread is complete (its shared-memory source read, its writes done)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -114,10 +130,31 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 __device__ __forceinline__ void sts32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ float lds32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ void sts32i(uint32_t addr, int v) {
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int lds32i(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
+}
+// dst (a peer's shared memory) += src (this CTA's), elementwise int32, by the TMA engine; the
+// bytes are counted on the peer's mbarrier. Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t cluster_addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void bulk_reduce_add_s32(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                    uint32_t bar_cluster) {
+  asm volatile(
+      "cp.reduce.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes.add.s32 [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
 }
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   uint4 v;
@@ -126,24 +163,29 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 }
 
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is 128 lanes (rows) x 8 columns (16 fp16
-// along K, two per column, the lower position in the low half).
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// along K, two per column, the lower position in the low half); the B descriptor is given as its
+// two 32-bit halves (the low half carries the address).
+__device__ __forceinline__ void mma_f16_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp writes lane (base + t).
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp writes lane (base + t).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -180,15 +222,20 @@ __device__ __forceinline__ float div_by_scale(float a, float s, float y) {
   return __fmaf_rn(r, y, q);
 }
 
-struct TokenConst {  // per token of the tile, in shared memory
-  float s, y, rs;    // act scale, RN(1/s), -rowsum (exact)
-  uint32_t fast;     // s within [2^-100, 2^100]
-};
+// Per token of the tile, in shared memory as one float4: {act scale s, y = RN(1/s), -rowsum
+// (exact), 1 if s lies in [2^-100, 2^100] else 0}.
+__device__ __forceinline__ float4 token_const(const float4* tok, int t) { return tok[t]; }
 
-__device__ __forceinline__ float finish(float d, const TokenConst& c, float w_scale, int* acc_int) {
-  const float a = __fmaf_rn(d, 16777216.0f, c.rs);  // raw - rowsum, exactly (an integer below 2^25)
+// out = RN(RN((d * 2^24 - rowsum) / s) * w_scale) with the branch-free division (fast tokens)
+__device__ __forceinline__ float finish_fast(float d, float4 c, float w_scale) {
+  const float a = __fmaf_rn(d, 16777216.0f, c.z);  // raw - rowsum, exactly (an integer below 2^25)
+  return __fmul_rn(div_by_scale(a, c.x, c.y), w_scale);
+}
+// the same for any token (the IEEE division where the scale is extreme); also the integer acc
+__device__ __forceinline__ float finish_any(float d, float4 c, float w_scale, int* acc_int) {
+  const float a = __fmaf_rn(d, 16777216.0f, c.z);
   *acc_int = __float2int_rn(a);
-  const float q = c.fast ? div_by_scale(a, c.s, c.y) : __fdiv_rn(a, c.s);
+  const float q = c.w != 0.0f ? div_by_scale(a, c.x, c.y) : __fdiv_rn(a, c.x);
   return __fmul_rn(q, w_scale);
 }
 
@@ -206,8 +253,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
   __shared__ __align__(8) uint64_t full_ab[NAB];    // a stage's A columns and B tile are written
   __shared__ __align__(8) uint64_t empty_ab[NAB];   // the MMAs reading a stage are done (one commit)
   __shared__ __align__(8) uint64_t done_bar;        // every MMA complete
+  __shared__ __align__(8) uint64_t recv_bar;        // the peers' partials of this CTA's tokens (bytes)
   __shared__ uint32_t tmem_slot;
-  __shared__ TokenConst tok[TT];
+  __shared__ float4 tok[TT];
 
   pdl_launch_dependents();
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -230,11 +278,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
       mbar_init(&empty_stg[s], CONV_WARPS);
     }
     for (int s = 0; s < NAB; ++s) {
-      mbar_init(&full_ab[s], CONV_WARPS);
+      mbar_init(&full_ab[s], CONV_WARPS / 2);  // one group writes a stage
       mbar_init(&empty_ab[s], 1);
     }
     mbar_init(&done_bar, 1);
+    mbar_init(&recv_bar, 1);
     fence_mbar_init();
+    if (cs > 1 && cs <= kReduceMaxCluster)  // every peer adds this CTA's tokens: 1 KB per token and peer
+      mbar_arrive_expect_tx(&recv_bar, (uint32_t)((cs - 1) * (tok_lo(rank + 1, cs) - tok_lo(rank, cs)) * TWR * 4));
   }
   if (warp == 0) {
     tmem_alloc(&tmem_slot, TMEM_COLS);
@@ -257,7 +308,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
         tma_load_2d(stg + b * STG_BYTES, &tmW, 32 * (b_lo + b), n0, &full_stg[b]);
       }
       pdl_wait();  // the tokens may be the previous kernel's output
-      for (int b = 0; b < pre; ++b) tma_load_2d(stg + b * STG_BYTES + STG_W, &tmX, 128 * (b_lo + b), m0, &full_stg[b]);
+      for (int b = 0; b < pre; ++b) {
+        tma_load_2d(stg + b * STG_BYTES + STG_W, &tmX, 128 * (b_lo + b), m0, &full_stg[b]);
+        tma_load_2d(stg + b * STG_BYTES + STG_W + STG_X / 2, &tmX, 128 * (b_lo + b) + 64, m0, &full_stg[b]);
+      }
       issued = pre;
       for (int b = pre; b < nblk; ++b) {
         const int slot = b % NSS, use = b / NSS;
@@ -265,6 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
         mbar_arrive_expect_tx(&full_stg[slot], STG_BYTES);
         tma_load_2d(stg + slot * STG_BYTES, &tmW, 32 * (b_lo + b), n0, &full_stg[slot]);
         tma_load_2d(stg + slot * STG_BYTES + STG_W, &tmX, 128 * (b_lo + b), m0, &full_stg[slot]);
+        tma_load_2d(stg + slot * STG_BYTES + STG_W + STG_X / 2, &tmX, 128 * (b_lo + b) + 64, m0, &full_stg[slot]);
         issued = b + 1;
       }
       {  // every copy issued lands before the producer leaves (the converters may have given up)
@@ -278,66 +333,94 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
     __syncwarp();
   } else if (warp == 1) {
     // ================================ MMA issuer ================================
+    // The issuing thread is on the critical path: a 128 x 128 x 16 MMA keeps the tensor pipe busy
+    // for only ~45 cycles, and this warp shares its scheduler with four converter warps. So every
+    // operand of the 8 MMAs of each of the NAB stage slots is formed once, before the loop, and
+    // the loop, unrolled over the slots, issues nothing but the waits, the MMAs and the commits.
     if (lane == 0) {
       const uint64_t bdesc0 = make_sw128_kmajor_desc(bring);
+      const uint32_t bhi = (uint32_t)(bdesc0 >> 32);  // the address field is in the low word and
+      const uint32_t blo0 = (uint32_t)bdesc0;         // the offsets below never carry out of it
       const uint32_t acol0 = tmem + (uint32_t)ACC_COLS;
-      for (int i = 0; i < nst; ++i) {
-        const int s = i % NAB;
-        if (!mbar_wait(&full_ab[s], (uint32_t)(i / NAB) & 1u, &abort)) break;
-        tc_fence_after();
-        const uint32_t a_col = acol0 + (uint32_t)(s * A_STAGE_COLS);
-        const uint64_t bd = bdesc0 + (uint64_t)((s * B_STAGE) >> 4);
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_f16_ts(tmem + (uint32_t)(t * TT), a_col + (uint32_t)(32 * t + 8 * j), bd + (uint64_t)((32 * j) >> 4),
-                       IDESC, (i > 0 || j > 0) ? 1u : 0u);
+      const uint32_t d0 = tmem, d1 = tmem + (uint32_t)TT;
+      auto stage = [&](int s, uint32_t acc_first) {
+        const uint32_t a = acol0 + (uint32_t)(s * A_STAGE_COLS);
+        const uint32_t bl = blo0 + (uint32_t)((s * B_STAGE) >> 4);
+        mma_f16_ts2(d0, a, bl, bhi, IDESC, acc_first);
+        mma_f16_ts2(d0, a + 8, bl + 2, bhi, IDESC, 1u);
+        mma_f16_ts2(d0, a + 16, bl + 4, bhi, IDESC, 1u);
+        mma_f16_ts2(d0, a + 24, bl + 6, bhi, IDESC, 1u);
+        mma_f16_ts2(d1, a + 32, bl, bhi, IDESC, acc_first);
+        mma_f16_ts2(d1, a + 40, bl + 2, bhi, IDESC, 1u);
+        mma_f16_ts2(d1, a + 48, bl + 4, bhi, IDESC, 1u);
+        mma_f16_ts2(d1, a + 56, bl + 6, bhi, IDESC, 1u);
         mma_commit(&empty_ab[s]);
+      };
+      int i = 0;
+      for (uint32_t ph = 0; i < nst; ph ^= 1u) {
+#pragma unroll
+        for (int s = 0; s < NAB; ++s, ++i) {
+          if (i >= nst || !mbar_wait(&full_ab[s], ph, &abort)) break;
+          tc_fence_after();
+          stage(s, i > 0 ? 1u : 0u);
+        }
+        if (abort) break;
       }
       mma_commit(&done_bar);  // tracks every MMA this thread issued
     }
     __syncwarp();  // as for the producer: the idle lanes must not poll beside the issuing lane
   } else {
     // ================================ converters ================================
+    // Two groups of 8 warps take alternate stages (group g the stages with h = g of every block),
+    // so each warp has two stage periods for its loads, conversion, tensor-memory store, fences
+    // and arrival. Within a group, warp (tile, lane quarter) owns 32 weight rows.
     const int cw = warp - 2;                  // 0..15
-    const int quarter = warp & 3, tile = (cw >> 2) & 1, role = cw >> 3;
+    const int grp = cw >> 3, gw = cw & 7;
+    const int quarter = warp & 3, tile = gw >> 2;
     const int row = tile * 128 + 32 * quarter + lane;  // this thread's weight row in the tile
-    const int ct = cw * 32 + lane;            // 0..511: this thread's token piece
-    const int pt = ct >> 2, pc = ct & 3;      // token, 16-k chunk of the stage
-    const uint32_t a_lane =
-        tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ACC_COLS + 32 * tile + 16 * role);
-    uint32_t w[8];
-    for (int i = 0; i < nst; ++i) {
-      const int b = i >> 1, h = i & 1, slot = b % NSS, s = i % NAB;
+    const int gt = gw * 32 + lane;            // 0..255: token pieces gt and gt + 256 of the stage
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ACC_COLS + 32 * tile);
+    for (int b = 0; b < nblk; ++b) {
+      const int i = 2 * b + grp, slot = b % NSS, s = i % NAB;
       const uint32_t sb = stg + slot * STG_BYTES;
-      if (h == 0) {
-        if (!mbar_wait_warp(&full_stg[slot], (uint32_t)(b / NSS) & 1u, &abort)) break;
-        const uint4 v0 = lds_v4(sb + row * 32), v1 = lds_v4(sb + row * 32 + 16);
-        w[0] = v0.x, w[1] = v0.y, w[2] = v0.z, w[3] = v0.w, w[4] = v1.x, w[5] = v1.y, w[6] = v1.z, w[7] = v1.w;
+      if (!mbar_wait_warp(&full_stg[slot], (uint32_t)(b / NSS) & 1u, &abort)) break;
+      // the row's 32 bytes, the two halves in a lane-dependent order (no bank conflicts)
+      const uint32_t c0 = (uint32_t)(lane >> 2) & 1u;
+      const uint4 va = lds_v4(sb + row * 32 + 16 * c0), vb = lds_v4(sb + row * 32 + 16 * (c0 ^ 1u));
+      const uint4 v0 = c0 ? vb : va, v1 = c0 ? va : vb;
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint4 xv[2];  // 16 k of a token each: pieces p = gt + 256v (token p / 4, chunk p % 4)
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const int p = gt + 256 * v;
+        xv[v] = lds_v4(sb + STG_W + grp * (STG_X / 2) + (p >> 2) * 64 + 16 * (p & 3));
       }
-      const uint4 xv = lds_v4(sb + STG_W + pt * 128 + 64 * h + 16 * pc);  // 16 k of token pt
       if (i >= NAB && !mbar_wait_warp(&empty_ab[s], (uint32_t)(i / NAB - 1) & 1u, &abort)) break;
       tc_fence_after();
-      {  // A: bit pair 2h + role of the row's 32 bytes -> 16 columns (word q: columns 2q, 2q + 1)
-        const int sh = 6 - 2 * (2 * h + role);
-        uint32_t a[16];
+      {  // A: bit pairs 2g, 2g + 1 of the row's 32 bytes -> 32 columns (pair jj: 16jj + 2q, + 1)
+        uint32_t a[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          a[2 * q] = (w[q] >> sh) & 0x00030003u;            // bytes 0, 2: fp16 subnormals c * 2^-24
-          a[2 * q + 1] = (w[q] >> (sh + 8)) & 0x00030003u;  // bytes 1, 3
+        for (int jj = 0; jj < 2; ++jj) {
+          const int sh = 6 - 2 * (2 * grp + jj);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            a[16 * jj + 2 * q] = (w[q] >> sh) & 0x00030003u;            // bytes 0, 2: c * 2^-24
+            a[16 * jj + 2 * q + 1] = (w[q] >> (sh + 8)) & 0x00030003u;  // bytes 1, 3
+          }
         }
-        tmem_st_32x32b_x16(a_lane + (uint32_t)(s * A_STAGE_COLS), a);
+        tmem_st_32x32b_x32(a_lane + (uint32_t)(s * A_STAGE_COLS), a);
       }
-      {  // B: 16 int8 -> 32 bytes of fp16 = chunks 2pc, 2pc + 1 of the token's row
+      const uint32_t bt = bring + (uint32_t)(s * B_STAGE);
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {  // B: 16 int8 -> 32 bytes of fp16 = chunks 2c, 2c + 1 of the token's row
+        const int p = gt + 256 * v, t = p >> 2, c = p & 3;
         uint32_t f[8];
-        s8x4_f16_perm(xv.x, f[0], f[1]);
-        s8x4_f16_perm(xv.y, f[2], f[3]);
-        s8x4_f16_perm(xv.z, f[4], f[5]);
-        s8x4_f16_perm(xv.w, f[6], f[7]);
-        const uint32_t bt = bring + (uint32_t)(s * B_STAGE);
-        sts128(bt + sw128(pt, 2 * pc), f[0], f[1], f[2], f[3]);
-        sts128(bt + sw128(pt, 2 * pc + 1), f[4], f[5], f[6], f[7]);
+        s8x4_f16_perm(xv[v].x, f[0], f[1]);
+        s8x4_f16_perm(xv[v].y, f[2], f[3]);
+        s8x4_f16_perm(xv[v].z, f[4], f[5]);
+        s8x4_f16_perm(xv[v].w, f[6], f[7]);
+        sts128(bt + sw128(t, 2 * c), f[0], f[1], f[2], f[3]);
+        sts128(bt + sw128(t, 2 * c + 1), f[4], f[5], f[6], f[7]);
       }
       tmem_st_wait();            // this thread's tensor-memory writes are complete
       fence_proxy_async_smem();  // its shared-memory writes -> the tensor core's reads
@@ -345,20 +428,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&full_ab[s]);
-        if (h == 1) mbar_arrive(&empty_stg[slot]);  // every staged byte of the block has been used
+        mbar_arrive(&empty_stg[slot]);  // this group is done with the block's staged bytes
       }
     }
+    const int ct = cw * 32 + lane;
     // the tile's per-token constants (the scales and row sums are the previous kernel's output)
     pdl_wait();
     if (ct < TT) {
       const int m = m0 + ct;
       const float sc = m < M ? __ldg(act_scale + m) : 1.0f;
-      TokenConst c;
-      c.s = sc;
-      c.y = __frcp_rn(sc);
-      c.rs = -(float)(m < M ? __ldg(rowsum + m) : 0);
-      c.fast = (sc >= 0x1p-100f && sc <= 0x1p100f) ? 1u : 0u;
-      tok[ct] = c;
+      tok[ct] = make_float4(sc, __frcp_rn(sc), -(float)(m < M ? __ldg(rowsum + m) : 0),
+                            (sc >= 0x1p-100f && sc <= 0x1p100f) ? 1.0f : 0.0f);
     }
   }
 
@@ -375,92 +455,174 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
   tc_fence_after();
   __syncthreads();  // tok[] written; every MMA read of the rings done
 
-  const int cw = warp - 2, quarter = warp & 3, tile = (cw >> 2) & 1, role = cw >> 3;
+  // Epilogue roles: converter warp (tile, lane quarter, half): its tile's 32 accumulator rows
+  // (the lane quarter it may read) and tokens [64 half, 64 half + 64).
+  const int cw = warp - 2, quarter = warp & 3, tile = (cw >> 2) & 1, half = cw >> 3;
   const int row = tile * 128 + 32 * quarter + lane;  // the accumulator row this thread reads
   const int n = n0 + row;
   const uint32_t tacc = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(tile * TT);
   const bool plain = !tma_store;  // else: TMA stores of the staged tile
 
   if (cs == 1) {
-    // the whole tile is this CTA's: finish straight from the accumulators
-    if (conv && have) {
+    // the whole tile is this CTA's: finish straight from the accumulators, 32 tokens at a time;
+    // each half's 8 warps meet at a named barrier and one thread stores the 32 finished tokens
+    if (conv) {
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
-        const int cb = 64 * role + 32 * cc;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tacc + (uint32_t)cb, v);
-        tmem_ld_wait();
+        const int cb = 64 * half + 32 * cc;
+        if (have) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + (uint32_t)cb, v);
+          tmem_ld_wait();
+          const bool fast = __all_sync(0xffffffffu, token_const(tok, cb + lane).w != 0.0f) && acc_out == nullptr;
+          if (fast) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = cb + e;
-          int ai;
-          const float o = finish(__uint_as_float(v[e]), tok[t], w_scale, &ai);
-          if (plain) {
-            const int m = m0 + t;
-            if (m < M && n < N) {
-              out[(int64_t)m * N + n] = o;
-              if (acc_out) acc_out[(int64_t)m * N + n] = ai;
+            for (int e = 0; e < 32; ++e) {
+              const float o = finish_fast(__uint_as_float(v[e]), token_const(tok, cb + e), w_scale);
+              if (plain) {
+                const int m = m0 + cb + e;
+                if (m < M && n < N) out[(int64_t)m * N + n] = o;
+              } else {
+                sts32(ostage + (uint32_t)(((cb + e) * TWR + row) * 4), o);
+              }
             }
           } else {
-            sts32(ostage + (uint32_t)((t * TWR + row) * 4), o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              int ai;
+              const float o = finish_any(__uint_as_float(v[e]), token_const(tok, cb + e), w_scale, &ai);
+              if (plain) {
+                const int m = m0 + cb + e;
+                if (m < M && n < N) {
+                  out[(int64_t)m * N + n] = o;
+                  if (acc_out) acc_out[(int64_t)m * N + n] = ai;
+                }
+              } else {
+                sts32(ostage + (uint32_t)(((cb + e) * TWR + row) * 4), o);
+              }
+            }
+          }
+        }
+        if (!plain) {
+          fence_proxy_async_smem();                      // the staged values -> the TMA engine
+          named_bar_sync(BAR_HALF + half, CONV_THREADS / 2);  // this half's 8 warps
+          if (cw == 8 * half && lane == 0 && have && m0 + cb < M) {
+            tma_store_2d(&tmO, n0, m0 + cb, ostage + (uint32_t)(cb * TWR * 4));
+            bulk_commit();
           }
         }
       }
+      if (!plain && cw == 8 * half && lane == 0) bulk_wait_all();  // before the CTA may leave
     }
   } else {
-    // split K: stage this CTA's exact partials, then finish the owned tokens from every CTA's
+    // split K: every CTA stages its exact partials as int32, token-major; after a cluster barrier
+    // the partials of each owner's tokens are summed at the owner, which finishes them in place
+    // and stores them. Small clusters: each CTA sends every peer its range in one bulk reduce-add
+    // (the TMA engine adds it into the owner's staging, counted in bytes on the owner's receive
+    // barrier). Larger clusters: each owner pulls its range from every peer.
     if (conv && have) {
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
-        const int cb = 64 * role + 32 * cc;
+        const int cb = 64 * half + 32 * cc;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tacc + (uint32_t)cb, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sts32(ostage + (uint32_t)(((cb + e) * TWR + row) * 4), __uint_as_float(v[e]));
+        for (int e = 0; e < 32; ++e)
+          sts32i(ostage + (uint32_t)(((cb + e) * TWR + row) * 4), __float2int_rn(__uint_as_float(v[e]) * 16777216.0f));
       }
     }
-    cluster_arrive_release();  // this CTA's partials are staged
-    cluster_wait_acquire();    // and every peer's
-    if (conv && have) {
-      const int t_lo = TT * rank / cs, t_hi = TT * (rank + 1) / cs;
-      const int ct = cw * 32 + lane, crow = ct & (TWR - 1), cn = n0 + crow;
-#pragma unroll 1
-      for (int t = t_lo + (ct >> 8); t < t_hi; t += 2) {
-        const uint32_t off = ostage + (uint32_t)((t * TWR + crow) * 4);
-        float d = lds32(off);
-        for (int p = 0; p < cs; ++p)
-          if (p != rank) d = __fadd_rn(d, ld_cluster_f32(map_to_rank(off, (uint32_t)p)));
-        int ai;
-        const float o = finish(d, tok[t], w_scale, &ai);
-        if (plain) {
-          const int m = m0 + t;
-          if (m < M && cn < N) {
-            out[(int64_t)m * N + cn] = o;
-            if (acc_out) acc_out[(int64_t)m * N + cn] = ai;
-          }
-        } else {
-          sts32(off, o);  // peers only read the tokens they own
+    const int t_lo = tok_lo(rank, cs), t_hi = tok_lo(rank + 1, cs);
+    const int ct = cw * 32 + lane;
+    if (cs <= kReduceMaxCluster) {
+      fence_proxy_async_smem();  // the staged partials -> the bulk reductions (source and target)
+      cluster_arrive_release();
+      cluster_wait_acquire();    // every CTA's partials are staged
+      if (threadIdx.x == 0 && !abort) {
+        for (int p = 0; p < cs; ++p) {
+          if (p == rank) continue;
+          const int p_lo = tok_lo(p, cs), p_hi = tok_lo(p + 1, cs);
+          const uint32_t off = ostage + (uint32_t)(p_lo * TWR * 4);
+          bulk_reduce_add_s32(map_to_rank(off, (uint32_t)p), off, (uint32_t)((p_hi - p_lo) * TWR * 4),
+                              map_to_rank(smem_u32(&recv_bar), (uint32_t)p));
         }
+      }
+      if (conv && have && mbar_wait_warp(&recv_bar, 0, &abort)) {
+        const int crow = ct & (TWR - 1), cn = n0 + crow;
+#pragma unroll 1
+        for (int t = t_lo + (ct >> 8); t < t_hi; t += 2) {  // the token is warp-uniform
+          const uint32_t off = ostage + (uint32_t)((t * TWR + crow) * 4);
+          const float4 c = token_const(tok, t);
+          const float a = (float)(lds32i(off) + (int)c.z);  // raw - rowsum, exactly
+          const float o = __fmul_rn(c.w != 0.0f ? div_by_scale(a, c.x, c.y) : __fdiv_rn(a, c.x), w_scale);
+          if (plain) {
+            const int m = m0 + t;
+            if (m < M && cn < N) {
+              out[(int64_t)m * N + cn] = o;
+              if (acc_out) acc_out[(int64_t)m * N + cn] = (int)a;
+            }
+          } else {
+            sts32(off, o);  // the owned tokens are finished in place
+          }
+        }
+      }
+    } else {
+      cluster_arrive_release();
+      cluster_wait_acquire();  // every CTA's partials are staged
+      if (conv && have) {
+        // thread (row quad, token slot): 4 consecutive rows of one owned token at a time, every
+        // peer's 16 bytes requested before any is added
+        const int quad = ct & 63, r4 = 4 * quad;
+#pragma unroll 1
+        for (int t = t_lo + (ct >> 6); t < t_hi; t += 8) {
+          const uint32_t off = ostage + (uint32_t)((t * TWR + r4) * 4);
+          uint4 part[kMaxCluster];
+#pragma unroll
+          for (int p = 0; p < kMaxCluster; ++p)
+            part[p] = p >= cs ? make_uint4(0u, 0u, 0u, 0u)
+                              : (p == rank ? lds_v4(off) : ld_cluster_v4(map_to_rank(off, (uint32_t)p)));
+          int sum[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int p = 0; p < kMaxCluster; ++p) {
+            sum[0] += (int)part[p].x, sum[1] += (int)part[p].y, sum[2] += (int)part[p].z, sum[3] += (int)part[p].w;
+          }
+          const float4 c = token_const(tok, t);
+          float o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float a = (float)(sum[i] + (int)c.z);  // raw - rowsum, exactly
+            o[i] = __fmul_rn(c.w != 0.0f ? div_by_scale(a, c.x, c.y) : __fdiv_rn(a, c.x), w_scale);
+            if (plain) {
+              const int m = m0 + t, cn = n0 + r4 + i;
+              if (m < M && cn < N) {
+                out[(int64_t)m * N + cn] = o[i];
+                if (acc_out) acc_out[(int64_t)m * N + cn] = (int)a;
+              }
+            }
+          }
+          // peers read only the tokens they own: this token is finished in place
+          if (!plain) sts128(off, __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+        }
+      }
+    }
+    if (!plain) {  // the owned token rows leave by TMA bulk stores of 8 rows
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_ALL, THREADS);
+      if (threadIdx.x == 0 && !abort) {
+        for (int t = t_lo; t < t_hi && m0 + t < M; t += 8) tma_store_2d(&tmO, n0, m0 + t, ostage + (uint32_t)(t * TWR * 4));
+        bulk_commit();
+        bulk_wait_all();
       }
     }
   }
 
-  if (!plain) {  // the finished token rows leave by TMA bulk stores
-    fence_proxy_async_smem();
-    named_bar_sync(BAR_ALL, THREADS);
-    if (threadIdx.x == 0 && !abort) {
-      if (cs == 1) {
-        for (int t = 0; t < TT && m0 + t < M; t += kStoreRows) tma_store_2d(&tmO, n0, m0 + t, ostage + (uint32_t)(t * TWR * 4));
-      } else {
-        const int t_lo = TT * rank / cs, t_hi = TT * (rank + 1) / cs;
-        for (int t = t_lo; t < t_hi && m0 + t < M; ++t) tma_store_2d(&tmO, n0, m0 + t, ostage + (uint32_t)(t * TWR * 4));
-      }
-      bulk_commit();
-      bulk_wait_read();  // the staged tile stays until the engine has read it
+  if (cs > 1) {
+    // no CTA leaves while a reduction may still target or read its shared memory: every owner
+    // has waited for all of its bytes (bounded), which is after every source was read
+    if (threadIdx.x == 32 && cs <= kReduceMaxCluster) {
+      bool dummy = false;
+      mbar_wait(&recv_bar, 0, &dummy);
     }
-  }
-  if (cs > 1) {  // no CTA leaves while a peer may still read its staged partials
     cluster_arrive_release();
     cluster_wait_acquire();
   }
@@ -548,13 +710,13 @@ cudaError_t launch_gemm_prefill(const int8_t* xq, const float* act_scale, const 
 
   CUtensorMap mW, mX, mO;
   if (!make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wp, N, K / 4, 32, TWR) ||
-      !make_map(&mX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, M, K, 128, TT))
+      !make_map(&mX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, M, K, 64, TT))
     return cudaErrorInvalidValue;
   // The finished tile leaves by TMA stores when the output rows are 16-byte aligned and the
   // int32 accumulators are not wanted; otherwise element by element.
   const bool tma_store = (N % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15) == 0 && acc_out == nullptr;
   std::memset(&mO, 0, sizeof(mO));
-  if (tma_store && !make_map(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, M, N, TWR, cs == 1 ? kStoreRows : 1))
+  if (tma_store && !make_map(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, M, N, TWR, cs == 1 ? kStoreRows : 8))
     return cudaErrorInvalidValue;
   return cudaLaunchKernelEx(&cfg, gemm_prefill_kernel, mW, mX, mO, act_scale, rowsum, w_scale, out, acc_out, (int)M,
                             (int)N, (int)K, tma_store ? 1 : 0);
