@@ -23,10 +23,11 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxK = 1 << 16;          // staged activation rows must fit shared memory
 constexpr int64_t kMaxKTensorCore = 1 << 15; // exact fp32 accumulation bound of the GEMM
 // The FFN block runs its projections on the expand-once workspace path from this many rows on
-// (when the caller gives a workspace); below it the few-token kernel is faster. Measured per
-// projection: M = 256, K 2560, N 6912: 28.8 against 31.8 us; M = 512, K 6912, N 2560: 56.6
-// against 53.0 us; M = 1024, K 2560: 86.7 against 53.3 us.
-constexpr int64_t kFfnWsMinM = 512;
+// (when the caller gives a workspace); below it the workspace-free kernels of auto dispatch are
+// faster. Measured per projection (N x K = 6912 x 2560 / 2560 x 6912), prompt-length kernel
+// against the workspace path: M = 1024: 50.9 / 55.0 against 52.9 / 58.0 us; M = 4096: 153.6 /
+// 165.1 against 145.2 / 150.8 us.
+constexpr int64_t kFfnWsMinM = 2048;
 // auto dispatch: the few-token tensor-core kernel from this many rows on. The dp4a GEMV's cost
 // grows with the rows (every weight word is decoded once per row); the tensor-core kernel's is
 // flat up to 16 rows. Measured (N x K = 6912 x 2560, 2560 x 6912, 2560 x 2560, 28672 x 8192):
@@ -35,6 +36,12 @@ constexpr int64_t kFfnWsMinM = 512;
 // the plain GEMV takes over and loses from 3 rows (8192 x 28672: 48.4 against 39.5 us).
 constexpr int64_t kSmallmMinM = 5;           // K <= 10240
 constexpr int64_t kSmallmMinMLongK = 3;      // K > 10240
+// auto dispatch: the prompt-length kernel from this many rows on; below, the few-token kernel in
+// chunks of 64. Measured per call (N x K = 6912 x 2560 / 2560 x 6912): M = 64: 13.7 / 16.4 against
+// 11.0 / 12.0 us; M = 128: 14.3 / 16.5 against 14.4 / 15.0; M = 192: 20.8 / 18.7 against 27.9 /
+// 18.7; M = 512: 25.7 / 29.6 against 43.2 / 56.3.
+constexpr int64_t kPrefillMinM = 128;         // K <= 4096
+constexpr int64_t kPrefillMinMLongK = 192;    // K > 4096
 
 // per-device: 0 = unchecked, 1 = sm_103 ok, -1 = unsupported; and SM count
 std::atomic<int> g_dev_state[kMaxDevices];
@@ -137,12 +144,15 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
   if (algo == BITNET_ALGO_AUTO) {
     // dp4a GEMV for a few tokens (it decodes each weight word once per token row, cheap while
     // the rows are few); from 5 rows (3 past K = 10240) the few-token tensor-core kernel, which
-    // decodes each weight once for up to 64 rows and takes more rows in chunks of 64. It also
-    // beats the in-kernel-expansion tile GEMM at every M measured (M = 128, K 2560, N 6912: 14.7
-    // against 61.0 us; M = 4096: 330 against 351 us), which stays available when forced.
+    // decodes each weight once for up to 64 rows and takes more rows in chunks of 64; from 128
+    // rows (192 past K = 4096) the prompt-length kernel (256 weight rows x 128 tokens per CTA).
+    // The in-kernel-expansion tile GEMM stays available when forced.
     const int64_t smallm_from = K > 10240 ? kSmallmMinMLongK : kSmallmMinM;
+    const int64_t prefill_from = K > 4096 ? kPrefillMinMLongK : kPrefillMinM;
     if (K > kMaxKTensorCore || M < smallm_from)
       algo = BITNET_ALGO_GEMV;
+    else if (M >= prefill_from && gemm_prefill_supported(M, N, K))
+      algo = BITNET_ALGO_PREFILL;
     else
       algo = BITNET_ALGO_SMALLM;
   }
