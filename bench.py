@@ -9,15 +9,23 @@ groups in one persistent launch (bitnet_sweep_plan_run). 521 MB of packed weight
 resident in HBM; the step is one CUDA graph. The metric is algorithmic bytes moved per second
 (GB/s, 2 bits per weight).
 
-Also measured in the same run and reported alongside:
+Also measured in the same run and reported alongside (every kernel leg the median of 20 graph
+replays over rotating buffer sets larger than L2, with its own roofline):
+  * serial_one_stream: the headline steps replayed on one stream, with no launch overlap;
   * decode_chain: the same sweep as a dependent chain, one fused launch per group, each
     waiting for the previous one;
-  * prefill: the prefill GEMM (M=4096, K=6912, N=2560, bf16 activations) in TOPS;
-  * gemv_100b: the 100B-class GEMV;
+  * gemv_2560x2560: config 1, the single GEMV (M=1, K=N=2560);
+  * batched_decode: config 3, M in {1,4,16,64} on both FFN shapes;
+  * prefill_cfg4: config 4, M in {128,512} on both FFN shapes, the plain call (the
+    prompt-length kernel) and the workspace path;
+  * prefill / prefill_m4096_plain_call: config 5a (M=4096, K=6912, N=2560) in TOPS, the
+    workspace path and the plain call;
+  * gemv_100b: config 5b, the 100B-class GEMV;
   * ffn: the fused FFN block;
   * e2e: the end-to-end figure through host buffers;
   * roofline: the roofline fraction of the dominant kernel;
-  * cpu_baseline: the CPU oracle on a bounded sample.
+  * cpu_baseline: the CPU oracle on a bounded sample of the headline workload, and per
+    configuration at one thread and at all of the host's threads.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -63,9 +71,11 @@ def parse_args(argv=None):
     p.add_argument("--no-gemv-leg", action="store_true", help="skip the 100B-class GEMV leg of the default line")
     p.add_argument("--no-ffn-leg", action="store_true", help="skip the fused FFN-block leg of the default line")
     p.add_argument("--no-batched-leg", action="store_true", help="skip the batched-decode leg of the default line")
-    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
+    p.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle CPU-baseline budget (decode sweep sample)")
+    p.add_argument("--load-seconds", type=float, default=1.0,
+                   help="untimed load window before the timed region, sampled for the clocks")
     p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill", "ffn", "quant_weight",
-                                          "batched_decode"],
+                                          "batched_decode", "gemv_2560", "prefill_cfg4"],
                    default="decode_sweep",
                    help="decode_sweep (default, the headline) or one single-kernel leg")
     return p.parse_args(argv)
@@ -253,10 +263,11 @@ def kernel_source_sha(kernel_file):
         os.path.exists(os.path.join(d, kernel_file)) for d in dirs) else None
 
 
-def recorded_traffic(kernel_file):
+def recorded_traffic(kernel_file, match=None):
     """DRAM bytes per launch of a kernel from a committed ncu summary, valid only while the
     kernel source and the headers it includes are unchanged (profiles/traffic.txt: file,
-    source sha16, bytes_per_launch, workload)."""
+    source sha16, bytes_per_launch, workload); `match`, if given, must occur in the workload
+    text (one kernel, several configurations)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     sha = kernel_source_sha(kernel_file)
     if sha is None or not os.path.exists(path):
@@ -265,7 +276,8 @@ def recorded_traffic(kernel_file):
         for line in f:
             parts = line.split()
             if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_file and parts[1] == sha:
-                return float(parts[2])
+                if match is None or match in line:
+                    return float(parts[2])
     return None
 
 
@@ -301,6 +313,49 @@ def oracle_sample(seconds, n_layers):
     desc = "%d projection groups of the decode sweep (quant + GEMVs, layers 0..%d, cycled), %d threads" % (
         groups_done, min(n_layers, (groups_done + 3) // 4) - 1, nt)
     return done_bytes / t_total / 1e9, desc, nt, t_total, groups_done
+
+
+def oracle_configs(budget_s=20.0):
+    """The CPU oracle (as it stands) on each configuration, the way SURVEY's measurement plan asks:
+    one thread for configs 1, 3 and 5b, and all of the host's threads (split over output rows) for
+    every configuration, on bounded samples. Each entry is one call of the oracle's quantisation
+    and matmul on seeded inputs of the configuration's shape (a row sample for the largest
+    matrices, said in the entry). Returns a list of dicts and the thread count."""
+    import oracle
+
+    nt = oracle.default_threads()
+    out = []
+    t_start = time.perf_counter()
+
+    def run(name, M, N, K, act_dtype, seed, threads, n_rows=None, outlier_p=0.0):
+        Ns = min(N, n_rows) if n_rows else N
+        wp, _ = oracle.pack_i2s(workloads.ternary_weights(Ns, K, seed + 1))
+        x = workloads.activations(M, K, seed, act_dtype, outlier_p)
+        ws = workloads.weight_scale(N, K, seed + 2)
+        t0 = time.perf_counter()
+        xq, s_, _ = oracle.quant_act(x, act_dtype)
+        oracle.ternary_matmul(xq, s_, wp, ws, nthreads=threads)
+        dt = time.perf_counter() - t0
+        byts = Ns * K // 4 + M * K + 8 * M + 4 * M * Ns
+        e = {"config": name, "M": M, "N": N, "K": K, "threads": threads, "ms": dt * 1e3,
+             "GB/s": byts / dt / 1e9, "GOPS": 2.0 * M * Ns * K / dt / 1e9}
+        if Ns != N:
+            e["sample"] = "%d of the %d weight rows" % (Ns, N)
+        out.append(e)
+
+    c1 = workloads.single_gemv()
+    c5a, c5b = workloads.large_cases()
+    for threads in (1, nt):
+        run("1: GEMV 2560x2560 M=1", c1.M, c1.N, c1.K, c1.act_dtype, c1.seed, threads)
+        for c in workloads.batched_decode_cases():
+            run("3: " + c.name, c.M, c.N, c.K, c.act_dtype, c.seed, threads, outlier_p=c.outlier_p)
+        run("5b: " + c5b.name, c5b.M, c5b.N, c5b.K, c5b.act_dtype, c5b.seed, threads,
+            n_rows=4096 if threads == 1 else 8192)
+    for c in workloads.prefill_cases():
+        run("4: " + c.name, c.M, c.N, c.K, c.act_dtype, c.seed, nt)
+    if time.perf_counter() - t_start < budget_s:
+        run("5a: " + c5a.name, c5a.M, c5a.N, c5a.K, c5a.act_dtype, c5a.seed, nt, n_rows=640)
+    return out, nt
 
 
 def run_reference(args):
@@ -350,75 +405,151 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------------ single-kernel legs
 
-def kernel_leg(kind, device, peaks, reps=20, warmup=3, sets=None):
-    """One matmul shape over rotating input sets whose total exceeds L2, timed with CUDA events.
+L2_BYTES = 129e6  # GB300 L2
 
-    kind = "prefill": tensor-core GEMM, M=4096, K=6912, N=2560, bf16 activations (8 sets);
-    kind = "gemv_100b": decode GEMV, M=1, K=8192, N=28672, bf16 activations (4 sets, 235 MB).
-    """
+
+def median_replay_seconds(graph, calls, stream, repeats):
+    """Median over `repeats` timed replays of a graph of `calls` launches, per launch."""
+    ts = sorted(time_replays(graph, 1, stream) / calls for _ in range(repeats))
+    return ts[len(ts) // 2]
+
+
+def matmul_leg(name, M, N, K, act_dtype, device, peaks, seed, path="auto", reps=20, repeats=20,
+               outlier_p=0.0, traffic=None):
+    """One matmul configuration through the C ABI, over rotating buffer sets whose total exceeds
+    twice the L2 (each call reads weights, activations and writes outputs no earlier call of the
+    replay left in L2; the sets are device copies of one seeded draw, the kernels' work does not
+    depend on the values). Two graphs are timed, each as the median of `repeats` replays of
+    `calls` back-to-back calls: the matmul alone (the dominant kernel: bitnet_i2s_matmul with
+    automatic kernel choice, or bitnet_i2s_matmul_ws) and the whole step (per-token
+    quantisation of the bf16/fp32 rows, then the matmul; one fused launch when M = 1)."""
+    import math
+
     import torch
 
     from ternary_weight_gb300 import binding
 
-    case = workloads.large_cases()[0 if kind == "prefill" else 1]
-    M, N, K = case.M, case.N, case.K
-    nsets = sets or (8 if kind == "prefill" else 4)
-    data = []
-    for i in range(nsets):
-        w = torch.from_numpy(workloads.ternary_weights(N, K, case.seed + 1 + 97 * i)).to(device)
-        x = torch.from_numpy(workloads.activations(M, K, case.seed + 97 * i, "bf16").view(np.int16)).to(device)
-        wp = binding.pack_i2s(w)
-        xq, s, rs = binding.quant_act(x.view(torch.bfloat16))
-        data.append((xq, s, rs, wp, workloads.weight_scale(N, K, case.seed + 2 + 97 * i),
-                     torch.empty((M, N), dtype=torch.float32, device=device)))
-        del w, x
+    esz = 4 if act_dtype == "f32" else 2
+    per_set = N * K // 4 + M * K * (esz + 1) + 8 * M + 4 * M * N
+    nsets = int(min(192, max(2, math.ceil(2.2 * L2_BYTES / per_set))))
+    w0 = binding.pack_i2s(torch.from_numpy(workloads.ternary_weights(N, K, seed + 1)).to(device))
+    x_np = workloads.activations(M, K, seed, act_dtype, outlier_p)
+    x0 = torch.from_numpy(x_np.view(np.int16) if act_dtype == "bf16" else x_np).to(device)
+    if act_dtype == "bf16":
+        x0 = x0.view(torch.bfloat16)
+    ws = workloads.weight_scale(N, K, seed + 2)
+    sets = []
+    for _ in range(nsets):
+        sets.append(dict(wp=w0.clone(), x=x0.clone(), xq=torch.empty((M, K), dtype=torch.int8, device=device),
+                         s=torch.empty(M, dtype=torch.float32, device=device),
+                         rs=torch.empty(M, dtype=torch.int32, device=device),
+                         out=torch.empty((M, N), dtype=torch.float32, device=device)))
+    wsbuf = (torch.empty(binding.workspace_size(M, N, K), dtype=torch.uint8, device=device)
+             if path == "ws" else None)
+    for d in sets:
+        binding.quant_act(d["x"], xq=d["xq"], scale=d["s"], rowsum=d["rs"])
     stream = torch.cuda.current_stream(device)
 
-    wsbuf = (torch.empty(binding.workspace_size(M, N, K), dtype=torch.uint8, device=device)
-             if kind == "prefill" else None)
-
-    def call(i):
-        xq, s, rs, wp, ws, out = data[i % nsets]
-        if kind == "prefill":  # the prefill path: expand once into the workspace, then the TMA GEMM
-            binding.i2s_matmul_ws(xq, s, rs, wp, ws, workspace=wsbuf, out=out)
+    def mm(i):
+        d = sets[i % nsets]
+        if path == "ws":
+            binding.i2s_matmul_ws(d["xq"], d["s"], d["rs"], d["wp"], ws, workspace=wsbuf, out=d["out"])
         else:
-            binding.i2s_matmul(xq, s, rs, wp, ws, out=out)
+            binding.i2s_matmul(d["xq"], d["s"], d["rs"], d["wp"], ws, out=d["out"])
 
-    for i in range(max(3, warmup)):
-        call(i)
-    torch.cuda.synchronize(device)
-    # capture the timed launches in one graph so host launch cost does not enter the timing
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for i in range(reps):
-            call(i)
-    g.replay()
-    torch.cuda.synchronize(device)
-    st = torch.cuda.Event(enable_timing=True)
-    en = torch.cuda.Event(enable_timing=True)
-    st.record(stream)
-    g.replay()
-    en.record(stream)
-    en.synchronize()
-    dt = st.elapsed_time(en) * 1e-3 / reps
-    if kind == "prefill":
-        tops = 2.0 * M * N * K / dt / 1e12
+    def step(i):
+        d = sets[i % nsets]
+        if M == 1 and path != "ws":
+            binding.linear_group(d["x"], [d["wp"]], [ws], outs=[d["out"]])
+        else:
+            binding.quant_act(d["x"], xq=d["xq"], scale=d["s"], rowsum=d["rs"])
+            mm(i)
+
+    calls = max(reps, nsets)
+    times = {}
+    for label, fn in (("mm", mm), ("step", step)):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(calls):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize(device)
+        times[label] = median_replay_seconds(g, calls, stream, repeats)
+        del g
+    t_mm, t_step = times["mm"], times["step"]
+    ops = 2.0 * M * N * K
+    byts = N * K // 4 + M * K + 8 * M + 4 * M * N
+    per_mm = 3 if path == "ws" else 1
+    per_step = per_mm + (0 if (M == 1 and path != "ws") else 1)
+    leg = {"workload": name, "M": M, "N": N, "K": K, "path": path, "us_per_call": t_mm * 1e6,
+           "gpu_launches_timed": repeats * calls * (per_mm + per_step),
+           "us_per_step": t_step * 1e6, "TOPS": ops / t_mm / 1e12, "GB/s": byts / t_mm / 1e9,
+           "step_TOPS": ops / t_step / 1e12, "step_GB/s": byts / t_step / 1e9, "bytes_per_call": byts,
+           "sets": nsets, "calls_per_replay": calls, "replays": repeats,
+           "timing": "median of %d replays of %d back-to-back calls over %d rotating buffer sets (%.0f MB, "
+                     "more than L2)" % (repeats, calls, nsets, nsets * per_set / 1e6)}
+    if M >= 128:  # a dense contraction: the tensor pipe at the fp16 rate (exact fp16 operands)
         peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        return {"workload": "prefill GEMM M=4096 K=6912 N=2560 (bf16 activations quantised to int8)",
-                "value": tops, "unit": "TOPS", "ms_per_call": dt * 1e3, "launches": reps,
-                "roofline": {"bound": "tensor", "achieved": tops, "peak": peak, "unit": "TFLOP/s",
-                             "frac": tops / peak, "traffic": recorded_traffic("gemm_tc_ws.cu"),
-                             "note": "bitnet_i2s_matmul_ws: codes and int8 activations expanded once to exact "
-                                     "fp16 in a workspace (timed), then a TMA-fed tcgen05 kind::f16 GEMM "
-                                     "(kind::i8 does not exist on sm_103a); peak = measured dense bf16 burst, "
-                                     "the fp16 rate"}}
-    byts = N * K / 4 + M * K + 8 * M + 4 * M * N
-    gbs = byts / dt / 1e9
-    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    return {"workload": "100B-class GEMV M=1 K=8192 N=28672 (bf16 activations quantised to int8)",
-            "value": gbs, "unit": "GB/s", "ms_per_call": dt * 1e3, "launches": reps,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "traffic": recorded_traffic("gemv_i2s.cu")}}
+        leg["value"], leg["unit"] = leg["TOPS"], "TOPS"
+        leg["roofline"] = {"bound": "tensor", "achieved": leg["TOPS"], "peak": peak, "unit": "TFLOP/s",
+                           "frac": leg["TOPS"] / peak, "traffic": traffic,
+                           "peak_source": "measured dense bf16 burst (MEASURED_PEAKS.json bf16_tflops); "
+                                          "the operands are exact fp16, the same rate"}
+    else:
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        leg["value"], leg["unit"] = leg["GB/s"], "GB/s"
+        leg["roofline"] = {"bound": "hbm", "achieved": leg["GB/s"], "peak": peak, "unit": "GB/s",
+                           "frac": leg["GB/s"] / peak, "traffic": traffic,
+                           "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)"}
+    del sets, wsbuf
+    torch.cuda.empty_cache()
+    return leg
+
+
+def config1_leg(device, peaks, reps=20):
+    """Config 1: the single W2A8 GEMV, M=1, K=N=2560, fp32 activations, seed 0."""
+    c = workloads.single_gemv()
+    return matmul_leg("single W2A8 GEMV M=1 K=2560 N=2560 (fp32 activations, per-token int8)", c.M, c.N, c.K,
+                      c.act_dtype, device, peaks, c.seed, reps=reps,
+                      traffic=recorded_traffic("gemv_i2s.cu", "2560x2560"))
+
+
+def config4_legs(device, peaks, reps=20):
+    """Config 4: prefill M in {128, 512} on both FFN shapes, the plain call (the prompt-length
+    kernel, no workspace) and, beside it, the expand-once workspace path."""
+    legs = []
+    for c in workloads.prefill_cases():
+        for path in ("auto", "ws"):
+            kern = "gemm_prefill.cu" if path == "auto" else "gemm_tc_ws.cu"
+            legs.append(matmul_leg("prefill M=%d K=%d N=%d (bf16 activations, per-token int8), %s" % (
+                c.M, c.K, c.N, "plain call" if path == "auto" else "workspace path"), c.M, c.N, c.K, c.act_dtype,
+                device, peaks, c.seed, path=path, reps=reps,
+                traffic=recorded_traffic(kern, "M=%d K=%d N=%d" % (c.M, c.K, c.N))))
+    return legs
+
+
+def prefill_m4096_legs(device, peaks, reps=20):
+    """Config 5a: prefill M=4096, K=6912, N=2560, the workspace path and the plain call."""
+    c = workloads.large_cases()[0]
+    out = {}
+    for path in ("ws", "auto"):
+        kern = "gemm_tc_ws.cu" if path == "ws" else "gemm_prefill.cu"
+        out[path] = matmul_leg("prefill GEMM M=4096 K=6912 N=2560 (bf16 activations, per-token int8), %s" % (
+            "workspace path" if path == "ws" else "plain call"), c.M, c.N, c.K, c.act_dtype, device, peaks,
+            c.seed, path=path, reps=reps, repeats=10,
+            traffic=recorded_traffic(kern, "M=4096 K=6912 N=2560"))
+    return out
+
+
+def gemv_100b_leg(device, peaks, reps=20):
+    """Config 5b: the 100B-class GEMV, M=1, K=8192, N=28672, bf16 activations."""
+    c = workloads.large_cases()[1]
+    return matmul_leg("100B-class GEMV M=1 K=8192 N=28672 (bf16 activations, per-token int8)", c.M, c.N, c.K,
+                      c.act_dtype, device, peaks, c.seed, reps=reps,
+                      traffic=recorded_traffic("gemv_i2s.cu", "K=8192 N=28672"))
 
 
 def ffn_leg(stack, device, peaks, reps=20):
@@ -579,7 +710,7 @@ def batched_decode_leg(device, peaks, reps=20, nsets=32):
                     call(i)
             g.replay()
             torch.cuda.synchronize(device)
-            t = time_replays(g, 3, stream) / (3 * ncalls)
+            t = median_replay_seconds(g, ncalls, stream, max(20, reps))
             byts = N * K // 4 + M * K + 8 * M + 4 * M * N
             gbs = byts / t / 1e9
             cases.append({"M": M, "K": K, "N": N, "us": t * 1e6, "GB/s": gbs, "frac": gbs / peak,
@@ -620,15 +751,38 @@ def run_kernel_workload(args):
                            "frac": leg["value"] / leg["peak"], "traffic": None,
                            "note": "aggregate of the eight matmuls (weights + activations + outputs per call); "
                                    "each call is bound by launch-scale fixed costs, see the per-case figures"}
-    else:
-        leg = kernel_leg(args.workload, device, peaks, reps=args.steps, warmup=args.warmup)
+    elif args.workload == "gemv_2560":
+        leg = config1_leg(device, peaks, reps=args.steps)
+    elif args.workload == "prefill_cfg4":
+        legs = config4_legs(device, peaks, reps=args.steps)
+        plain = [l for l in legs if l["path"] == "auto"]
+        t_all = sum(l["us_per_call"] for l in plain) * 1e-6
+        ops = sum(2.0 * l["M"] * l["N"] * l["K"] for l in plain)
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        leg = {"workload": "prefill M in {128, 512} x (K, N) in {(2560, 6912), (6912, 2560)}, bf16 activations, "
+                           "plain call (prompt-length kernel) and workspace path",
+               "value": ops / t_all / 1e12, "unit": "TOPS", "ms_per_call": t_all * 1e3, "cases": legs,
+               "roofline": {"bound": "tensor", "achieved": ops / t_all / 1e12, "peak": peak, "unit": "TFLOP/s",
+                            "frac": ops / t_all / 1e12 / peak, "traffic": None,
+                            "note": "aggregate of the four plain calls one after another; per case in cases"}}
+    elif args.workload == "gemv_100b":
+        leg = gemv_100b_leg(device, peaks, reps=args.steps)
+    else:  # prefill: config 5a, the workspace path (and the plain call beside it)
+        legs = prefill_m4096_legs(device, peaks, reps=args.steps)
+        leg = dict(legs["ws"])
+        leg["plain_call"] = legs["auto"]
+    if "ms_per_call" not in leg and "us_per_call" in leg:
+        leg["ms_per_call"] = leg["us_per_call"] * 1e-3
     clocks = sampler.stop()
     line = {"metric": METRIC, "value": leg["value"], "unit": leg["unit"], "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": leg["ms_per_call"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "i8xi2->i32", "data": "synthetic",
             "config": {"workload": leg["workload"], "l2": "rotating input sets larger than L2"},
             "gpu_launches": (8 * 3 * max(args.steps, 32) if args.workload == "batched_decode" else
-                             args.steps * {"ffn": 2 * args.layers, "quant_weight": 3 * 2 * 3}.get(args.workload, 1)),
+                             args.steps * {"ffn": 2 * args.layers, "quant_weight": 3 * 2 * 3}.get(args.workload, 1)
+                             if args.workload in ("ffn", "quant_weight") else
+                             leg.get("gpu_launches_timed") or sum(c.get("gpu_launches_timed", 0)
+                                                                  for c in leg.get("cases", []))),
             "clocks": clocks,
             "roofline": leg["roofline"],
             "leg": {k: v for k, v in leg.items() if k not in ("workload", "value", "unit", "roofline")}}
@@ -793,10 +947,17 @@ def run_ours(args):
             g.replay()
     torch.cuda.synchronize(device)
 
-    # ---- timed region: K steps, each one persistent launch; the two buffer sets alternate on
-    # two streams so that a step's kernel ramp overlaps the previous step's tail ----
+    # ---- clocks: the sampler runs through an untimed load window of about a second (the same
+    # steps) and then through the timed region, so that it sees the GPU under sustained load ----
     sampler = ClockSampler(local)
     sampler.start()
+    t_load, n_load = 0.0, 0
+    while t_load < args.load_seconds:
+        n = 200
+        t_load += time_alternating(graphs, streams, n, device)
+        n_load += n
+    # ---- timed region: K steps, each one persistent launch; the two buffer sets alternate on
+    # two streams so that a step's kernel ramp overlaps the previous step's tail ----
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(device)
@@ -805,6 +966,10 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
+    clocks["window"] = ("sampled through an untimed load window of %d steps (%.2f s) and the timed region of "
+                        "%d steps" % (n_load, t_load, args.steps))
+    # the same steps serially on one stream, one buffer set (no overlap of consecutive launches)
+    t_serial = time_replays(graphs[0], args.steps, torch.cuda.current_stream(device))
 
     bytes_step = sweep_bytes(stack)
     per_rank = allgather_floats(dist, world, [t_step, float(bytes_step * args.steps)], device)
@@ -829,19 +994,29 @@ def run_ours(args):
     e2e_bps, _ = aggregate([r[0] for r in per_rank_e2e], [r[1] for r in per_rank_e2e])
 
     chain = chain_leg(stack, device, peaks, max(10, args.steps // 4))
-    prefill = None if args.no_prefill else kernel_leg("prefill", device, peaks)
-    gemv_100b = None if args.no_gemv_leg else kernel_leg("gemv_100b", device, peaks)
     ffn = None if args.no_ffn_leg else ffn_leg(stack, device, peaks)
-    batched = None if args.no_batched_leg else batched_decode_leg(device, peaks)
     plan.close()
     plan_b.close()
+    packed = sum(l.weight_bytes() for g in stack.groups for l in g.linears)
+    act_in, out_bytes = stack.act_bytes_in, stack.out_elems * 4
+    del stack, graphs, sets, x_b, out_b
+    torch.cuda.empty_cache()
+    gemv_2560 = None if args.no_gemv_leg else config1_leg(device, peaks)
+    batched = None if args.no_batched_leg else batched_decode_leg(device, peaks)
+    cfg4 = None if args.no_prefill else config4_legs(device, peaks)
+    m4096 = None if args.no_prefill else prefill_m4096_legs(device, peaks)
+    gemv_100b = None if args.no_gemv_leg else gemv_100b_leg(device, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, desc, nt, _, _ = oracle_sample(args.cpu_seconds, args.layers)
-        cpu = {"value": gbs, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": desc}
+        per_config, nt2 = oracle_configs()
+        cpu = {"value": gbs, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": desc,
+               "per_config": per_config,
+               "per_config_note": "one oracle call (quantisation + matmul) per configuration at 1 thread (configs "
+                                  "1, 3, 5b) and at %d threads (every configuration), rows split over threads; "
+                                  "row samples where stated" % nt2}
 
-    packed = sum(l.weight_bytes() for g in stack.groups for l in g.linears)
     line = {
         "metric": METRIC, "value": value_bps / 1e9, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -860,16 +1035,24 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "roofline": roofline,
-        "e2e": {"value": e2e_bps / 1e9, "unit": UNIT, "h2d_bytes_per_step": stack.act_bytes_in,
-                "d2h_bytes_per_step": stack.out_elems * 4,
+        "e2e": {"value": e2e_bps / 1e9, "unit": UNIT, "h2d_bytes_per_step": act_in,
+                "d2h_bytes_per_step": out_bytes,
                 "note": "per step: pinned host activations -> device, the sweep, all projection outputs -> host; "
                         "two buffer sets (two plans over the same weights) alternate on two streams so one step's "
                         "copies overlap the other's kernel"},
+        "serial_one_stream": {"value": bytes_step / (t_serial / args.steps) / 1e9, "unit": UNIT,
+                              "ms_per_step": t_serial / args.steps * 1e3,
+                              "frac": bytes_step / (t_serial / args.steps) / 1e9 / hbm_peak,
+                              "note": "the same K steps replayed on one stream with one buffer set: no "
+                                      "overlap of a launch's ramp with the previous launch's tail"},
         "decode_chain": chain,
-        "prefill": prefill,
+        "gemv_2560x2560": gemv_2560,
+        "batched_decode": batched,
+        "prefill_cfg4": cfg4,
+        "prefill": m4096["ws"] if m4096 else None,
+        "prefill_m4096_plain_call": m4096["auto"] if m4096 else None,
         "gemv_100b": gemv_100b,
         "ffn": ffn,
-        "batched_decode": batched,
         "cpu_baseline": cpu,
     }
     if rank == 0:
