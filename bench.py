@@ -72,6 +72,8 @@ def parse_args(argv=None):
     p.add_argument("--no-ffn-leg", action="store_true", help="skip the fused FFN-block leg of the default line")
     p.add_argument("--no-batched-leg", action="store_true", help="skip the batched-decode leg of the default line")
     p.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle CPU-baseline budget (decode sweep sample)")
+    p.add_argument("--case", default=None, help="--workload prefill_cfg4: only the cases whose name contains this")
+    p.add_argument("--plain-only", action="store_true", help="--workload prefill_cfg4: only the plain call")
     p.add_argument("--load-seconds", type=float, default=1.0,
                    help="untimed load window before the timed region, sampled for the clocks")
     p.add_argument("--workload", choices=["decode_sweep", "gemv_100b", "prefill", "ffn", "quant_weight",
@@ -514,15 +516,18 @@ def config1_leg(device, peaks, reps=20):
     c = workloads.single_gemv()
     return matmul_leg("single W2A8 GEMV M=1 K=2560 N=2560 (fp32 activations, per-token int8)", c.M, c.N, c.K,
                       c.act_dtype, device, peaks, c.seed, reps=reps,
-                      traffic=recorded_traffic("gemv_i2s.cu", "2560x2560"))
+                      traffic=recorded_traffic("gemv_i2s.cu", "M=1 K=2560 N=2560"))
 
 
-def config4_legs(device, peaks, reps=20):
+def config4_legs(device, peaks, reps=20, case=None, paths=("auto", "ws")):
     """Config 4: prefill M in {128, 512} on both FFN shapes, the plain call (the prompt-length
-    kernel, no workspace) and, beside it, the expand-once workspace path."""
+    kernel, no workspace) and, beside it, the expand-once workspace path. `case`: only the
+    cases whose name contains it."""
     legs = []
     for c in workloads.prefill_cases():
-        for path in ("auto", "ws"):
+        if case and case not in c.name:
+            continue
+        for path in paths:
             kern = "gemm_prefill.cu" if path == "auto" else "gemm_tc_ws.cu"
             legs.append(matmul_leg("prefill M=%d K=%d N=%d (bf16 activations, per-token int8), %s" % (
                 c.M, c.K, c.N, "plain call" if path == "auto" else "workspace path"), c.M, c.N, c.K, c.act_dtype,
@@ -549,7 +554,7 @@ def gemv_100b_leg(device, peaks, reps=20):
     c = workloads.large_cases()[1]
     return matmul_leg("100B-class GEMV M=1 K=8192 N=28672 (bf16 activations, per-token int8)", c.M, c.N, c.K,
                       c.act_dtype, device, peaks, c.seed, reps=reps,
-                      traffic=recorded_traffic("gemv_i2s.cu", "K=8192 N=28672"))
+                      traffic=recorded_traffic("gemv_i2s.cu", "M=1 K=8192 N=28672"))
 
 
 def ffn_leg(stack, device, peaks, reps=20):
@@ -754,7 +759,8 @@ def run_kernel_workload(args):
     elif args.workload == "gemv_2560":
         leg = config1_leg(device, peaks, reps=args.steps)
     elif args.workload == "prefill_cfg4":
-        legs = config4_legs(device, peaks, reps=args.steps)
+        legs = config4_legs(device, peaks, reps=args.steps, case=args.case,
+                            paths=("auto",) if args.plain_only else ("auto", "ws"))
         plain = [l for l in legs if l["path"] == "auto"]
         t_all = sum(l["us_per_call"] for l in plain) * 1e-6
         ops = sum(2.0 * l["M"] * l["N"] * l["K"] for l in plain)
