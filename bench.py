@@ -72,7 +72,9 @@ def parse_args(argv=None):
     p.add_argument("--no-ffn-leg", action="store_true", help="skip the fused FFN-block leg of the default line")
     p.add_argument("--no-batched-leg", action="store_true", help="skip the batched-decode leg of the default line")
     p.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle CPU-baseline budget (decode sweep sample)")
-    p.add_argument("--case", default=None, help="--workload prefill_cfg4: only the cases whose name contains this")
+    p.add_argument("--case", default=None,
+                   help="--workload prefill_cfg4: only the cases whose name contains this; --workload "
+                        "batched_decode: only the case mM_kK (e.g. m16_k2560)")
     p.add_argument("--plain-only", action="store_true", help="--workload prefill_cfg4: only the plain call")
     p.add_argument("--load-seconds", type=float, default=1.0,
                    help="untimed load window before the timed region, sampled for the clocks")
@@ -680,7 +682,7 @@ def quant_weight_leg(device, peaks, reps=10):
                                  "case is bound by the integer work of the exact sum (gbs_bf16)"}}
 
 
-def batched_decode_leg(device, peaks, reps=20, nsets=32):
+def batched_decode_leg(device, peaks, reps=20, nsets=32, case=None):
     """The batched decode matmuls at M in {1, 4, 16, 64} on the FFN shapes (K 2560, N 6912 and
     K 6912, N 2560), bf16 activations with 1% x20 outliers quantised per token, then
     bitnet_i2s_matmul with automatic kernel choice. 32 rotating weight sets per shape (141 MB,
@@ -696,6 +698,8 @@ def batched_decode_leg(device, peaks, reps=20, nsets=32):
         wps = [binding.pack_i2s(torch.from_numpy(workloads.ternary_weights(N, K, 9300 + i)).to(device))
                for i in range(nsets)]
         for M in (1, 4, 16, 64):
+            if case and case != "m%d_k%d" % (M, K):
+                continue
             x = torch.from_numpy(workloads.activations(M, K, 9400 + M, "bf16", 0.01).view(np.int16)).to(device)
             xq, s_, rs = binding.quant_act(x.view(torch.bfloat16))
             out = torch.empty((M, N), dtype=torch.float32, device=device)
@@ -748,7 +752,7 @@ def run_kernel_workload(args):
     elif args.workload == "quant_weight":
         leg = quant_weight_leg(device, peaks, reps=args.steps)
     elif args.workload == "batched_decode":
-        leg = batched_decode_leg(device, peaks, reps=args.steps)
+        leg = batched_decode_leg(device, peaks, reps=args.steps, case=args.case)
         t_all = sum(c["us"] for c in leg["cases"]) * 1e-6
         leg["value"] = sum(c["bytes"] for c in leg["cases"]) / t_all / 1e9  # all eight matmuls, one after another
         leg["ms_per_call"] = t_all * 1e3
