@@ -53,12 +53,13 @@
 // Split K: for short prompts the blocks of one tile are spread over a thread-block cluster of up
 // to 16 CTAs (as many as make every CTA resident at once). Every CTA stages its exact partials as
 // int32, token-major, in its own shared memory; after a cluster barrier rank r owns the tokens
-// [8 floor(16 r / cs), 8 floor(16 (r + 1) / cs)) of the tile. With up to 3 CTAs every other rank
-// adds its partials of that range into r's staging with one bulk reduction (cp.reduce.async.bulk,
-// int32 add, by the TMA engine), counted in bytes on r's receive barrier; with more, r pulls them
-// with 16-byte distributed-shared-memory loads, every peer's requested before any is added. r
-// finishes its tokens in place and stores them; a second cluster barrier keeps every CTA alive
-// until its shared memory is no longer read or written by a peer.
+// [8 floor(16 r / cs), 8 floor(16 (r + 1) / cs)) of the tile and pulls their partials from every
+// peer with 16-byte distributed-shared-memory loads (a warp reads 512 contiguous bytes of one
+// token; every peer's 16 bytes are requested before any is added). r finishes its tokens in place
+// and stores them; a second cluster barrier keeps every CTA alive until no peer reads its shared
+// memory any more. (Bulk reduce-adds by the TMA engine into the owner's staging, tried for small
+// clusters, were slower: 2B-4T FFN shapes, at 3 CTAs 20.3 against 17.1 us, at 2 CTAs 21.8
+// against 21.4.)
 // Every mbarrier wait is bounded; a timeout is recorded in the device error word, and the TMA
 // producer always waits (bounded) for its last copies before it leaves.
 #include "bitnet_dev.cuh"
@@ -94,11 +95,6 @@ constexpr uint32_t IDESC = make_idesc_f16_f32(128, TT);
 // split K: rank r of a cluster of cs finishes tokens [tok_lo(r), tok_lo(r + 1)) of the tile, in
 // whole groups of 8 (every rank has at least one group for cs <= 16)
 __host__ __device__ constexpr int tok_lo(int r, int cs) { return 8 * (16 * r / cs); }
-// Up to this cluster size the peers' partials are added by bulk reductions (few large transfers
-// per CTA); beyond it each owner pulls them with 16-byte distributed-shared-memory loads (many
-// peers, few tokens each), which measured faster there (2B-4T FFN shapes: at 2 CTAs 20.7 against
-// 25.4 us, at 5 CTAs 19.1 against 14.9 us, at 10 CTAs 23.0 against 15.3 us).
-constexpr int kReduceMaxCluster = 3;
 static_assert(ACC_COLS + NAB * A_STAGE_COLS <= (int)TMEM_COLS, "tensor memory columns");
 static_assert(SMEM <= 227 * 1024 - 4096, "shared memory (static part included)");
 static_assert(OUT_STAGE <= NAB * B_STAGE + NSS * STG_BYTES, "the epilogue tile fits the reused rings");
@@ -133,13 +129,7 @@ __device__ __forceinline__ void sts32(uint32_t addr, float v) {
 __device__ __forceinline__ void sts32i(uint32_t addr, int v) {
   asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ int lds32i(uint32_t addr) {
-  int v;
-  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-// dst (a peer's shared memory) += src (this CTA's), elementwise int32, by the TMA engine; the
-// bytes are counted on the peer's mbarrier. Addresses 16-byte aligned, bytes a multiple of 16.
+// 16 bytes of a peer's shared memory (a shared::cluster address, 16-byte aligned)
 __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t cluster_addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -147,14 +137,6 @@ __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t cluster_addr) {
                : "r"(cluster_addr)
                : "memory");
   return v;
-}
-__device__ __forceinline__ void bulk_reduce_add_s32(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                    uint32_t bar_cluster) {
-  asm volatile(
-      "cp.reduce.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes.add.s32 [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(src), "r"(bytes), "r"(bar_cluster)
-      : "memory");
 }
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
   uint4 v;
@@ -226,17 +208,48 @@ __device__ __forceinline__ float div_by_scale(float a, float s, float y) {
 // (exact), 1 if s lies in [2^-100, 2^100] else 0}.
 __device__ __forceinline__ float4 token_const(const float4* tok, int t) { return tok[t]; }
 
-// out = RN(RN((d * 2^24 - rowsum) / s) * w_scale) with the branch-free division (fast tokens)
-__device__ __forceinline__ float finish_fast(float d, float4 c, float w_scale) {
-  const float a = __fmaf_rn(d, 16777216.0f, c.z);  // raw - rowsum, exactly (an integer below 2^25)
-  return __fmul_rn(div_by_scale(a, c.x, c.y), w_scale);
-}
-// the same for any token (the IEEE division where the scale is extreme); also the integer acc
+// out = RN(RN((d * 2^24 - rowsum) / s) * w_scale) for any token (the IEEE division where the scale
+// is extreme), and the integer acc
 __device__ __forceinline__ float finish_any(float d, float4 c, float w_scale, int* acc_int) {
   const float a = __fmaf_rn(d, 16777216.0f, c.z);
   *acc_int = __float2int_rn(a);
   const float q = c.w != 0.0f ? div_by_scale(a, c.x, c.y) : __fdiv_rn(a, c.x);
   return __fmul_rn(q, w_scale);
+}
+
+// Two fp32 lanes per instruction (mul/fma .f32x2, each lane rounded exactly as the scalar
+// operation): the epilogue's per-element arithmetic at half the instruction count.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// RN(RN(a / s) * w_scale) for two values at once, as div_by_scale then __fmul_rn: ns2 = -s,
+// y2 = RN(1/s) of their tokens (fma(q, -s, a) is fma(-q, s, a) exactly)
+__device__ __forceinline__ uint64_t div_scale2(uint64_t a, uint64_t ns2, uint64_t y2, uint64_t ws2) {
+  uint64_t q = mul2(a, y2);
+  uint64_t r = fma2(q, ns2, a);
+  q = fma2(r, y2, q);
+  r = fma2(q, ns2, a);
+  q = fma2(r, y2, q);
+  return mul2(q, ws2);
+}
+// finish_fast for two values at once: d2 the raw accumulators, z2 = -rowsum of their tokens
+__device__ __forceinline__ uint64_t finish_fast2(uint64_t d2, uint64_t ns2, uint64_t y2, uint64_t z2, uint64_t ws2) {
+  return div_scale2(fma2(d2, 0x4B8000004B800000ull, z2), ns2, y2, ws2);  // 2^24 in both lanes
 }
 
 __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -253,9 +266,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
   __shared__ __align__(8) uint64_t full_ab[NAB];    // a stage's A columns and B tile are written
   __shared__ __align__(8) uint64_t empty_ab[NAB];   // the MMAs reading a stage are done (one commit)
   __shared__ __align__(8) uint64_t done_bar;        // every MMA complete
-  __shared__ __align__(8) uint64_t recv_bar;        // the peers' partials of this CTA's tokens (bytes)
   __shared__ uint32_t tmem_slot;
   __shared__ float4 tok[TT];
+  __shared__ __align__(16) float tk_ns[TT], tk_y[TT], tk_z[TT];  // -s, RN(1/s), -rowsum per token
 
   pdl_launch_dependents();
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -282,10 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
       mbar_init(&empty_ab[s], 1);
     }
     mbar_init(&done_bar, 1);
-    mbar_init(&recv_bar, 1);
     fence_mbar_init();
-    if (cs > 1 && cs <= kReduceMaxCluster)  // every peer adds this CTA's tokens: 1 KB per token and peer
-      mbar_arrive_expect_tx(&recv_bar, (uint32_t)((cs - 1) * (tok_lo(rank + 1, cs) - tok_lo(rank, cs)) * TWR * 4));
   }
   if (warp == 0) {
     tmem_alloc(&tmem_slot, TMEM_COLS);
@@ -437,8 +447,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
     if (ct < TT) {
       const int m = m0 + ct;
       const float sc = m < M ? __ldg(act_scale + m) : 1.0f;
-      tok[ct] = make_float4(sc, __frcp_rn(sc), -(float)(m < M ? __ldg(rowsum + m) : 0),
-                            (sc >= 0x1p-100f && sc <= 0x1p100f) ? 1.0f : 0.0f);
+      const float4 c = make_float4(sc, __frcp_rn(sc), -(float)(m < M ? __ldg(rowsum + m) : 0),
+                                   (sc >= 0x1p-100f && sc <= 0x1p100f) ? 1.0f : 0.0f);
+      tok[ct] = c;
+      tk_ns[ct] = -sc;
+      tk_y[ct] = c.y;
+      tk_z[ct] = c.z;
     }
   }
 
@@ -476,14 +490,27 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
           tmem_ld_wait();
           const bool fast = __all_sync(0xffffffffu, token_const(tok, cb + lane).w != 0.0f) && acc_out == nullptr;
           if (fast) {
+            const uint64_t ws2 = f2pack(w_scale, w_scale);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float o = finish_fast(__uint_as_float(v[e]), token_const(tok, cb + e), w_scale);
-              if (plain) {
-                const int m = m0 + cb + e;
-                if (m < M && n < N) out[(int64_t)m * N + n] = o;
-              } else {
-                sts32(ostage + (uint32_t)(((cb + e) * TWR + row) * 4), o);
+            for (int e = 0; e < 32; e += 4) {  // four tokens' constants per 16-byte broadcast read
+              const float4 ns4 = *reinterpret_cast<const float4*>(tk_ns + cb + e);
+              const float4 y4 = *reinterpret_cast<const float4*>(tk_y + cb + e);
+              const float4 z4 = *reinterpret_cast<const float4*>(tk_z + cb + e);
+              float o[4];
+              f2unpack(finish_fast2(f2pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), f2pack(ns4.x, ns4.y),
+                                    f2pack(y4.x, y4.y), f2pack(z4.x, z4.y), ws2),
+                       o[0], o[1]);
+              f2unpack(finish_fast2(f2pack(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), f2pack(ns4.z, ns4.w),
+                                    f2pack(y4.z, y4.w), f2pack(z4.z, z4.w), ws2),
+                       o[2], o[3]);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (plain) {
+                  const int m = m0 + cb + e + i;
+                  if (m < M && n < N) out[(int64_t)m * N + n] = o[i];
+                } else {
+                  sts32(ostage + (uint32_t)(((cb + e + i) * TWR + row) * 4), o[i]);
+                }
               }
             }
           } else {
@@ -516,10 +543,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
     }
   } else {
     // split K: every CTA stages its exact partials as int32, token-major; after a cluster barrier
-    // the partials of each owner's tokens are summed at the owner, which finishes them in place
-    // and stores them. Small clusters: each CTA sends every peer its range in one bulk reduce-add
-    // (the TMA engine adds it into the owner's staging, counted in bytes on the owner's receive
-    // barrier). Larger clusters: each owner pulls its range from every peer.
+    // each owner pulls its tokens' partials from every peer, sums them, finishes them in place
+    // and stores them.
     if (conv && have) {
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
@@ -534,75 +559,49 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
     }
     const int t_lo = tok_lo(rank, cs), t_hi = tok_lo(rank + 1, cs);
     const int ct = cw * 32 + lane;
-    if (cs <= kReduceMaxCluster) {
-      fence_proxy_async_smem();  // the staged partials -> the bulk reductions (source and target)
-      cluster_arrive_release();
-      cluster_wait_acquire();    // every CTA's partials are staged
-      if (threadIdx.x == 0 && !abort) {
-        for (int p = 0; p < cs; ++p) {
-          if (p == rank) continue;
-          const int p_lo = tok_lo(p, cs), p_hi = tok_lo(p + 1, cs);
-          const uint32_t off = ostage + (uint32_t)(p_lo * TWR * 4);
-          bulk_reduce_add_s32(map_to_rank(off, (uint32_t)p), off, (uint32_t)((p_hi - p_lo) * TWR * 4),
-                              map_to_rank(smem_u32(&recv_bar), (uint32_t)p));
-        }
-      }
-      if (conv && have && mbar_wait_warp(&recv_bar, 0, &abort)) {
-        const int crow = ct & (TWR - 1), cn = n0 + crow;
+    cluster_arrive_release();
+    cluster_wait_acquire();  // every CTA's partials are staged
+    if (conv && have) {
+      // thread (row quad, token slot): 4 consecutive rows of one owned token at a time, every
+      // peer's 16 bytes requested before any is added
+      const int quad = ct & 63, r4 = 4 * quad;
 #pragma unroll 1
-        for (int t = t_lo + (ct >> 8); t < t_hi; t += 2) {  // the token is warp-uniform
-          const uint32_t off = ostage + (uint32_t)((t * TWR + crow) * 4);
-          const float4 c = token_const(tok, t);
-          const float a = (float)(lds32i(off) + (int)c.z);  // raw - rowsum, exactly
-          const float o = __fmul_rn(c.w != 0.0f ? div_by_scale(a, c.x, c.y) : __fdiv_rn(a, c.x), w_scale);
+      for (int t = t_lo + (ct >> 6); t < t_hi; t += 8) {
+        const uint32_t off = ostage + (uint32_t)((t * TWR + r4) * 4);
+        uint4 part[kMaxCluster];
+#pragma unroll
+        for (int p = 0; p < kMaxCluster; ++p)
+          part[p] = p >= cs ? make_uint4(0u, 0u, 0u, 0u)
+                            : (p == rank ? lds_v4(off) : ld_cluster_v4(map_to_rank(off, (uint32_t)p)));
+        int sum[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int p = 0; p < kMaxCluster; ++p) {
+          sum[0] += (int)part[p].x, sum[1] += (int)part[p].y, sum[2] += (int)part[p].z, sum[3] += (int)part[p].w;
+        }
+        const float4 c = token_const(tok, t);
+        float a[4], o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = (float)(sum[i] + (int)c.z);  // raw - rowsum, exactly
+        if (c.w != 0.0f) {  // warp-uniform (one token per warp)
+          const uint64_t ns2 = f2pack(-c.x, -c.x), y2 = f2pack(c.y, c.y), ws2 = f2pack(w_scale, w_scale);
+          f2unpack(div_scale2(f2pack(a[0], a[1]), ns2, y2, ws2), o[0], o[1]);
+          f2unpack(div_scale2(f2pack(a[2], a[3]), ns2, y2, ws2), o[2], o[3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = __fmul_rn(__fdiv_rn(a[i], c.x), w_scale);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
           if (plain) {
-            const int m = m0 + t;
+            const int m = m0 + t, cn = n0 + r4 + i;
             if (m < M && cn < N) {
-              out[(int64_t)m * N + cn] = o;
-              if (acc_out) acc_out[(int64_t)m * N + cn] = (int)a;
-            }
-          } else {
-            sts32(off, o);  // the owned tokens are finished in place
-          }
-        }
-      }
-    } else {
-      cluster_arrive_release();
-      cluster_wait_acquire();  // every CTA's partials are staged
-      if (conv && have) {
-        // thread (row quad, token slot): 4 consecutive rows of one owned token at a time, every
-        // peer's 16 bytes requested before any is added
-        const int quad = ct & 63, r4 = 4 * quad;
-#pragma unroll 1
-        for (int t = t_lo + (ct >> 6); t < t_hi; t += 8) {
-          const uint32_t off = ostage + (uint32_t)((t * TWR + r4) * 4);
-          uint4 part[kMaxCluster];
-#pragma unroll
-          for (int p = 0; p < kMaxCluster; ++p)
-            part[p] = p >= cs ? make_uint4(0u, 0u, 0u, 0u)
-                              : (p == rank ? lds_v4(off) : ld_cluster_v4(map_to_rank(off, (uint32_t)p)));
-          int sum[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int p = 0; p < kMaxCluster; ++p) {
-            sum[0] += (int)part[p].x, sum[1] += (int)part[p].y, sum[2] += (int)part[p].z, sum[3] += (int)part[p].w;
-          }
-          const float4 c = token_const(tok, t);
-          float o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float a = (float)(sum[i] + (int)c.z);  // raw - rowsum, exactly
-            o[i] = __fmul_rn(c.w != 0.0f ? div_by_scale(a, c.x, c.y) : __fdiv_rn(a, c.x), w_scale);
-            if (plain) {
-              const int m = m0 + t, cn = n0 + r4 + i;
-              if (m < M && cn < N) {
-                out[(int64_t)m * N + cn] = o[i];
-                if (acc_out) acc_out[(int64_t)m * N + cn] = (int)a;
-              }
+              out[(int64_t)m * N + cn] = o[i];
+              if (acc_out) acc_out[(int64_t)m * N + cn] = (int)a[i];
             }
           }
-          // peers read only the tokens they own: this token is finished in place
-          if (!plain) sts128(off, __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
         }
+        // peers read only the tokens they own: this token is finished in place
+        if (!plain) sts128(off, __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
       }
     }
     if (!plain) {  // the owned token rows leave by TMA bulk stores of 8 rows
@@ -616,13 +615,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
     }
   }
 
-  if (cs > 1) {
-    // no CTA leaves while a reduction may still target or read its shared memory: every owner
-    // has waited for all of its bytes (bounded), which is after every source was read
-    if (threadIdx.x == 32 && cs <= kReduceMaxCluster) {
-      bool dummy = false;
-      mbar_wait(&recv_bar, 0, &dummy);
-    }
+  if (cs > 1) {  // no CTA leaves while a peer may still read its shared memory
     cluster_arrive_release();
     cluster_wait_acquire();
   }

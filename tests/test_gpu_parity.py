@@ -267,6 +267,28 @@ def test_random_bytes_including_code3(algo, M, N, K):
     assert_out_close(out, o_out)
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 6912, 2560), (256, 1000, 2560), (130, 300, 1024), (640, 2562, 1152),
+                                   (128, 2560, 6912), (512, 2560, 6912)])
+@pytest.mark.parametrize("extreme", [False, True])
+def test_prefill_outputs_without_accumulators(M, N, K, extreme):
+    """The call a product makes (no int32 accumulators requested) on the prompt-length kernel: the
+    finish that runs only there (two values per instruction, the staged tile and its bulk stores
+    when the rows are 16-byte aligned, plain stores when N % 4 != 0, split-K sums), and tokens
+    whose scale lies outside [2^-100, 2^100] sharing a 32-token chunk with ordinary ones (the
+    chunk then takes the IEEE division). Every output bit-identical to the oracle."""
+    wp, _ = oracle.pack_i2s(workloads.ternary_weights(N, K, seed=530 + N))
+    xq = workloads.random_int8(M, K, seed=531 + M)
+    s = (np.random.default_rng(532 + M).random(M).astype(np.float32) * 3 + 0.1).astype(np.float32)
+    if extreme:
+        s[3], s[M // 2], s[M - 1] = np.float32(2.0 ** -110), np.float32(2.0 ** 110), np.float32(2.0 ** -101)
+    rs = xq.astype(np.int64).sum(axis=1).astype(np.int32)
+    out = binding.i2s_matmul(dev(xq), dev(s), dev(rs), dev(wp), 0.0173, algo="prefill")
+    o_out, _ = oracle.ternary_matmul(xq, s, wp, 0.0173, nthreads=NT)
+    got = host(out)
+    assert np.array_equal(got.view(np.uint32), o_out.view(np.uint32))
+    assert binding.last_device_error() == 0
+
+
 @pytest.mark.parametrize("M", [1, 2, 3, 63, 64, 65, 127, 128, 129])
 def test_gemv_and_gemm_agree(M):
     K, N = 2560, 600
