@@ -79,6 +79,7 @@ extern "C" {
 #define BITNET_ALGO_GEMM 2   /* force the tcgen05 tensor-core GEMM (any M)           */
 #define BITNET_ALGO_SMALLM 3 /* force the few-token tensor-core kernel (any M)       */
 #define BITNET_ALGO_PREFILL 4 /* force the prompt-length tensor-core kernel (any M)  */
+#define BITNET_ALGO_PREFILL_PAIR 5 /* force its CTA-pair variant (any M)               */
 
 /* Library ABI version (major*100 + minor). */
 BITNET_API int bitnet_version(void);

@@ -24,7 +24,7 @@ BITNET_ERANGE = -6
 BITNET_F32 = 0
 BITNET_BF16 = 1
 
-ALGO = {"auto": 0, "gemv": 1, "gemm": 2, "smallm": 3, "prefill": 4}
+ALGO = {"auto": 0, "gemv": 1, "gemm": 2, "smallm": 3, "prefill": 4, "pair": 5}
 
 # every entry point of include/bitnet.h with its ctypes signature
 _P = ctypes.c_void_p

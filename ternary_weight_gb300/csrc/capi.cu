@@ -137,7 +137,7 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
                                       int64_t N, int64_t K, int algo, void* stream) {
   if (!xq || !act_scale || !rowsum || !wp || !out) return BITNET_EINVAL;
   if (M < 1 || M > INT32_MAX || N < 1 || N > INT32_MAX || !valid_k(K)) return BITNET_EINVAL;
-  if (algo < BITNET_ALGO_AUTO || algo > BITNET_ALGO_PREFILL) return BITNET_EINVAL;
+  if (algo < BITNET_ALGO_AUTO || algo > BITNET_ALGO_PREFILL_PAIR) return BITNET_EINVAL;
   if (!aligned(xq, 16) || !aligned(wp, 16) || !aligned(act_scale, 4) || !aligned(rowsum, 4) || !aligned(out, 4) ||
       (acc_out && !aligned(acc_out, 4)))
     return BITNET_EALIGN;
@@ -160,6 +160,7 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
   if (algo == BITNET_ALGO_GEMV && M > 65535LL * 8) return BITNET_EINVAL;
   if (algo == BITNET_ALGO_SMALLM && !gemm_smallm_supported(M, K)) return BITNET_EINVAL;
   if (algo == BITNET_ALGO_PREFILL && !gemm_prefill_supported(M, N, K)) return BITNET_EINVAL;
+  if (algo == BITNET_ALGO_PREFILL_PAIR && !gemm_pair_supported(M, N, K)) return BITNET_EINVAL;
   int sms = 0;
   if (int st = check_device(&sms)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -173,6 +174,9 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
       break;
     case BITNET_ALGO_PREFILL:
       e = launch_gemm_prefill(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
+      break;
+    case BITNET_ALGO_PREFILL_PAIR:
+      e = launch_gemm_pair(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
       break;
     default:
       e = launch_gemm_i2s_tc(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, sms, s);
@@ -476,7 +480,7 @@ BITNET_API int bitnet_last_device_error(void) {
                                     read_clear_device_error_gemv_group, read_clear_device_error_smallm,
                                     read_clear_device_error_quant_weight, read_clear_device_error_sweep,
                                     read_clear_device_error_gemv_ring, read_clear_device_error_selftest,
-                                    read_clear_device_error_prefill};
+                                    read_clear_device_error_prefill, read_clear_device_error_pair};
   for (auto rd : readers) {
     int v = 0;
     if (rd(&v) != cudaSuccess) return BITNET_ECUDA;

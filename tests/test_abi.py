@@ -63,7 +63,8 @@ def _mm(lib, xq=FAKE, s=FAKE, rs=FAKE, wp=FAKE, out=FAKE, acc=None, M=1, N=1, K=
     (dict(xq=None), -1), (dict(s=None), -1), (dict(rs=None), -1), (dict(wp=None), -1), (dict(out=None), -1),
     (dict(K=100), -1), (dict(K=0), -1), (dict(K=-128), -1), (dict(K=128 * 513 * 2), -1),
     (dict(M=0), -1), (dict(N=0), -1), (dict(M=-5), -1), (dict(N=1 << 31), -1),
-    (dict(algo=5), -1), (dict(algo=-1), -1), (dict(algo=2, K=65536), -1), (dict(algo=4, K=32768 + 128), -1),
+    (dict(algo=6), -1), (dict(algo=-1), -1), (dict(algo=2, K=65536), -1), (dict(algo=4, K=32768 + 128), -1),
+    (dict(algo=5, K=32768 + 128), -1),
     (dict(algo=3, M=64 * 65535 + 1), -1), (dict(algo=3, K=32768 + 128), -1),
     (dict(xq=FAKE + 8), -2), (dict(wp=FAKE + 4), -2), (dict(out=FAKE + 2), -2), (dict(acc=FAKE + 1), -2),
     (dict(s=FAKE + 1), -2), (dict(rs=FAKE + 2), -2),

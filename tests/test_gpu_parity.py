@@ -222,11 +222,13 @@ PREFILL_CHAIN = [
 ]
 
 
+@pytest.mark.parametrize("algo", ["prefill", "pair"])
 @pytest.mark.parametrize("M,N,K,dtype", PREFILL_CHAIN)
-def test_chain_parity_prefill(M, N, K, dtype):
+def test_chain_parity_prefill(M, N, K, dtype, algo):
+    """The prompt-length kernel and its CTA-pair variant, forced."""
     x = workloads.activations(M, K, seed=410 + M, dtype=dtype, outlier_p=0.01)
     w = workloads.ternary_weights(N, K, seed=411 + N)
-    g, o = run_chain(x, dtype, w, workloads.weight_scale(N, K, 412), algo="prefill")
+    g, o = run_chain(x, dtype, w, workloads.weight_scale(N, K, 412), algo=algo)
     assert_chain_equal(g, o)
     assert binding.last_device_error() == 0
 
@@ -239,7 +241,7 @@ def _matmul_only(xq, s, wp, w_scale, algo):
     return host(out), host(acc)
 
 
-@pytest.mark.parametrize("algo", ["gemv", "gemm", "prefill"])
+@pytest.mark.parametrize("algo", ["gemv", "gemm", "prefill", "pair"])
 def test_max_magnitude_accumulators(algo):
     """xq all +-127 against all-(+1) weights: |acc| = 127*K, the largest a ternary row gives."""
     K, N, M = 8192, 260, 3
@@ -254,7 +256,7 @@ def test_max_magnitude_accumulators(algo):
     assert np.array_equal(out.view(np.uint32), o_out.view(np.uint32))
 
 
-@pytest.mark.parametrize("algo", ["gemv", "gemm", "prefill"])
+@pytest.mark.parametrize("algo", ["gemv", "gemm", "prefill", "pair"])
 @pytest.mark.parametrize("M,N,K", [(5, 77, 2560), (130, 300, 1024), (256, 1000, 32768)])
 def test_random_bytes_including_code3(algo, M, N, K):
     """Arbitrary packed bytes (code 3 included, read as +2 by the c - 1 rule)."""
@@ -270,7 +272,8 @@ def test_random_bytes_including_code3(algo, M, N, K):
 @pytest.mark.parametrize("M,N,K", [(512, 6912, 2560), (256, 1000, 2560), (130, 300, 1024), (640, 2562, 1152),
                                    (128, 2560, 6912), (512, 2560, 6912)])
 @pytest.mark.parametrize("extreme", [False, True])
-def test_prefill_outputs_without_accumulators(M, N, K, extreme):
+@pytest.mark.parametrize("algo", ["prefill", "pair"])
+def test_prefill_outputs_without_accumulators(M, N, K, extreme, algo):
     """The call a product makes (no int32 accumulators requested) on the prompt-length kernel: the
     finish that runs only there (two values per instruction, the staged tile and its bulk stores
     when the rows are 16-byte aligned, plain stores when N % 4 != 0, split-K sums), and tokens
@@ -282,7 +285,7 @@ def test_prefill_outputs_without_accumulators(M, N, K, extreme):
     if extreme:
         s[3], s[M // 2], s[M - 1] = np.float32(2.0 ** -110), np.float32(2.0 ** 110), np.float32(2.0 ** -101)
     rs = xq.astype(np.int64).sum(axis=1).astype(np.int32)
-    out = binding.i2s_matmul(dev(xq), dev(s), dev(rs), dev(wp), 0.0173, algo="prefill")
+    out = binding.i2s_matmul(dev(xq), dev(s), dev(rs), dev(wp), 0.0173, algo=algo)
     o_out, _ = oracle.ternary_matmul(xq, s, wp, 0.0173, nthreads=NT)
     got = host(out)
     assert np.array_equal(got.view(np.uint32), o_out.view(np.uint32))
