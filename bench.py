@@ -18,8 +18,8 @@ replays over rotating buffer sets larger than L2, with its own roofline):
   * batched_decode: config 3, M in {1,4,16,64} on both FFN shapes;
   * prefill_cfg4: config 4, M in {128,512} on both FFN shapes, the plain call (the
     prompt-length kernel) and the workspace path;
-  * prefill / prefill_m4096_plain_call: config 5a (M=4096, K=6912, N=2560) in TOPS, the
-    workspace path and the plain call;
+  * prefill / prefill_m4096_workspace_path: config 5a (M=4096, K=6912, N=2560) in TOPS, the
+    plain call (the CTA-pair prompt-length kernel) and the workspace path;
   * gemv_100b: config 5b, the 100B-class GEMV;
   * ffn: the fused FFN block;
   * e2e: the end-to-end figure through host buffers;
@@ -265,6 +265,18 @@ def kernel_source_sha(kernel_file):
     visit(kernel_file)
     return h.hexdigest()[:16] if seen and any(
         os.path.exists(os.path.join(d, kernel_file)) for d in dirs) else None
+
+
+def auto_kernel_file(M, N, K):
+    """The source file of the matmul kernel bitnet_i2s_matmul's automatic choice runs (the rule
+    in capi.cu), for the traffic records."""
+    if K > 32768 or M < (3 if K > 10240 else 5):
+        return "gemv_i2s.cu"
+    if M >= 192:
+        return "gemm_pair.cu"
+    if K <= 4096 and M >= 128:
+        return "gemm_prefill.cu"
+    return "gemm_smallm.cu"
 
 
 def recorded_traffic(kernel_file, match=None):
@@ -530,7 +542,7 @@ def config4_legs(device, peaks, reps=20, case=None, paths=("auto", "ws")):
         if case and case not in c.name:
             continue
         for path in paths:
-            kern = "gemm_prefill.cu" if path == "auto" else "gemm_tc_ws.cu"
+            kern = auto_kernel_file(c.M, c.N, c.K) if path == "auto" else "gemm_tc_ws.cu"
             legs.append(matmul_leg("prefill M=%d K=%d N=%d (bf16 activations, per-token int8), %s" % (
                 c.M, c.K, c.N, "plain call" if path == "auto" else "workspace path"), c.M, c.N, c.K, c.act_dtype,
                 device, peaks, c.seed, path=path, reps=reps,
@@ -539,11 +551,11 @@ def config4_legs(device, peaks, reps=20, case=None, paths=("auto", "ws")):
 
 
 def prefill_m4096_legs(device, peaks, reps=20):
-    """Config 5a: prefill M=4096, K=6912, N=2560, the workspace path and the plain call."""
+    """Config 5a: prefill M=4096, K=6912, N=2560, the plain call and the workspace path."""
     c = workloads.large_cases()[0]
     out = {}
-    for path in ("ws", "auto"):
-        kern = "gemm_tc_ws.cu" if path == "ws" else "gemm_prefill.cu"
+    for path in ("auto", "ws"):
+        kern = "gemm_tc_ws.cu" if path == "ws" else auto_kernel_file(c.M, c.N, c.K)
         out[path] = matmul_leg("prefill GEMM M=4096 K=6912 N=2560 (bf16 activations, per-token int8), %s" % (
             "workspace path" if path == "ws" else "plain call"), c.M, c.N, c.K, c.act_dtype, device, peaks,
             c.seed, path=path, reps=reps, repeats=10,
@@ -777,10 +789,10 @@ def run_kernel_workload(args):
                             "note": "aggregate of the four plain calls one after another; per case in cases"}}
     elif args.workload == "gemv_100b":
         leg = gemv_100b_leg(device, peaks, reps=args.steps)
-    else:  # prefill: config 5a, the workspace path (and the plain call beside it)
+    else:  # prefill: config 5a, the plain call (and the workspace path beside it)
         legs = prefill_m4096_legs(device, peaks, reps=args.steps)
-        leg = dict(legs["ws"])
-        leg["plain_call"] = legs["auto"]
+        leg = dict(legs["auto"])
+        leg["workspace_path"] = legs["ws"]
     if "ms_per_call" not in leg and "us_per_call" in leg:
         leg["ms_per_call"] = leg["us_per_call"] * 1e-3
     clocks = sampler.stop()
@@ -1059,8 +1071,8 @@ def run_ours(args):
         "gemv_2560x2560": gemv_2560,
         "batched_decode": batched,
         "prefill_cfg4": cfg4,
-        "prefill": m4096["ws"] if m4096 else None,
-        "prefill_m4096_plain_call": m4096["auto"] if m4096 else None,
+        "prefill": m4096["auto"] if m4096 else None,
+        "prefill_m4096_workspace_path": m4096["ws"] if m4096 else None,
         "gemv_100b": gemv_100b,
         "ffn": ffn,
         "cpu_baseline": cpu,

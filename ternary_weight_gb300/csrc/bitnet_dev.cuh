@@ -407,14 +407,6 @@ cudaError_t launch_gemm_prefill(const int8_t* xq, const float* act_scale, const 
                                 int num_sms, cudaStream_t stream);
 cudaError_t read_clear_device_error_prefill(int* value);
 
-// The same on CTA pairs (gemm_pair.cu): tcgen05.mma.cta_group::2, 256 weight rows x 256 tokens per
-// pair; K <= 32768.
-bool gemm_pair_supported(int64_t M, int64_t N, int64_t K);
-cudaError_t launch_gemm_pair(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
-                             float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int num_sms,
-                             cudaStream_t stream);
-cudaError_t read_clear_device_error_pair(int* value);
-
 // Few-token tensor-core matmul (gemm_smallm.cu): any M (64 tokens per CTA), K <= 32768.
 bool gemm_smallm_supported(int64_t M, int64_t K);
 cudaError_t launch_gemm_smallm(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,

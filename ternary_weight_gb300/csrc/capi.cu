@@ -8,6 +8,7 @@
 // bitnet_sweep_plan_create, freed by bitnet_sweep_plan_destroy).
 #include "bitnet.h"
 #include "bitnet_dev.cuh"
+#include "gemm_pair.h"
 
 #include <cmath>
 #include <new>
@@ -22,12 +23,6 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxK = 1 << 16;          // staged activation rows must fit shared memory
 constexpr int64_t kMaxKTensorCore = 1 << 15; // exact fp32 accumulation bound of the GEMM
-// The FFN block runs its projections on the expand-once workspace path from this many rows on
-// (when the caller gives a workspace); below it the workspace-free kernels of auto dispatch are
-// faster. Measured per projection (N x K = 6912 x 2560 / 2560 x 6912), prompt-length kernel
-// against the workspace path: M = 1024: 50.9 / 55.0 against 52.9 / 58.0 us; M = 4096: 153.6 /
-// 165.1 against 145.2 / 150.8 us.
-constexpr int64_t kFfnWsMinM = 2048;
 // auto dispatch: the few-token tensor-core kernel from this many rows on. The dp4a GEMV's cost
 // grows with the rows (every weight word is decoded once per row); the tensor-core kernel's is
 // flat up to 16 rows. Measured (N x K = 6912 x 2560, 2560 x 6912, 2560 x 2560, 28672 x 8192):
@@ -36,12 +31,14 @@ constexpr int64_t kFfnWsMinM = 2048;
 // the plain GEMV takes over and loses from 3 rows (8192 x 28672: 48.4 against 39.5 us).
 constexpr int64_t kSmallmMinM = 5;           // K <= 10240
 constexpr int64_t kSmallmMinMLongK = 3;      // K > 10240
-// auto dispatch: the prompt-length kernel from this many rows on; below, the few-token kernel in
-// chunks of 64. Measured per call (N x K = 6912 x 2560 / 2560 x 6912): M = 64: 13.7 / 16.4 against
-// 11.0 / 12.0 us; M = 128: 14.3 / 16.5 against 14.4 / 15.0; M = 192: 20.8 / 18.7 against 27.9 /
-// 18.7; M = 512: 25.7 / 29.6 against 43.2 / 56.3.
-constexpr int64_t kPrefillMinM = 128;         // K <= 4096
-constexpr int64_t kPrefillMinMLongK = 192;    // K > 4096
+// auto dispatch: the prompt-length kernels. Measured per call, µs (N x K = 6912 x 2560 / 2560 x
+// 6912; few-token chunks, one-CTA kernel, CTA-pair kernel): M = 128: 14.5 / 15.1, 14.1 / 16.7,
+// 15.9 / 16.9; M = 192: 28.0 / 18.7, 19.1 / 18.6, 15.9 / 17.2; M = 256: 28.6 / 28.8, 19.1 / 18.7,
+// 16.0 / 17.3; M = 512: 43.2 / 56.3, 25.2 / 25.8, 21.1 / 21.7; M = 4096: 329 / 256, 151 / 164,
+// 127 / 130. So the pair kernel from 192 rows, the one-CTA kernel from 128 rows up to K = 4096,
+// and the few-token chunks below.
+constexpr int64_t kPrefillMinM = 128;         // the one-CTA kernel, K <= 4096
+constexpr int64_t kPairMinM = 192;            // the CTA-pair kernel
 
 // per-device: 0 = unchecked, 1 = sm_103 ok, -1 = unsupported; and SM count
 std::atomic<int> g_dev_state[kMaxDevices];
@@ -145,13 +142,15 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
     // dp4a GEMV for a few tokens (it decodes each weight word once per token row, cheap while
     // the rows are few); from 5 rows (3 past K = 10240) the few-token tensor-core kernel, which
     // decodes each weight once for up to 64 rows and takes more rows in chunks of 64; from 128
-    // rows (192 past K = 4096) the prompt-length kernel (256 weight rows x 128 tokens per CTA).
-    // The in-kernel-expansion tile GEMM stays available when forced.
+    // rows up to K = 4096 the one-CTA prompt-length kernel (256 weight rows x 128 tokens per
+    // CTA); from 192 rows the CTA-pair kernel (256 x 256 per pair). The in-kernel-expansion tile
+    // GEMM stays available when forced.
     const int64_t smallm_from = K > 10240 ? kSmallmMinMLongK : kSmallmMinM;
-    const int64_t prefill_from = K > 4096 ? kPrefillMinMLongK : kPrefillMinM;
     if (K > kMaxKTensorCore || M < smallm_from)
       algo = BITNET_ALGO_GEMV;
-    else if (M >= prefill_from && gemm_prefill_supported(M, N, K))
+    else if (M >= kPairMinM && gemm_pair_supported(M, N, K))
+      algo = BITNET_ALGO_PREFILL_PAIR;
+    else if (K <= 4096 && M >= kPrefillMinM && gemm_prefill_supported(M, N, K))
       algo = BITNET_ALGO_PREFILL;
     else
       algo = BITNET_ALGO_SMALLM;
@@ -300,14 +299,12 @@ namespace {
 bool valid_ffn_shape(int64_t M, int64_t K, int64_t F) {
   return M >= 1 && M <= INT32_MAX && valid_k(K) && valid_k(F) && F <= kFfnMaxF;
 }
-// workspace of the expand-once GEMM path for the three projections (gate and up: N = F over
-// K; down: N = K over F), or 0 when that path does not apply (fewer than 512 rows, where the
-// few-token kernel is faster, or K or F too long)
-int64_t ffn_ws_bytes(int64_t M, int64_t K, int64_t F) {
-  if (M < kFfnWsMinM || K > kMaxKTensorCore || F > kMaxKTensorCore) return 0;
-  const int64_t a = gemm_ws_bytes(M, F, K), b = gemm_ws_bytes(M, K, F);
-  return a > b ? a : b;
-}
+// Workspace the FFN block uses: none. Its projections take the workspace-free kernels of auto
+// dispatch at every M: the CTA-pair prompt-length kernel measured faster than the expand-once
+// workspace path at every size tried (per projection, N x K = 6912 x 2560 / 2560 x 6912: M = 1024
+// 41.7 / 44.0 against 52.6 / 58.0 us, M = 2048 63.9 / 86.0 against 82.9 / 94.5, M = 4096 127 /
+// 130 against 145 / 151, M = 8192 252 / 218 against 269 / 272).
+int64_t ffn_ws_bytes(int64_t, int64_t, int64_t) { return 0; }
 }  // namespace
 
 BITNET_API int64_t bitnet_w2a8_ffn_workspace_size(int64_t M, int64_t K, int64_t F) {
@@ -358,9 +355,6 @@ BITNET_API int bitnet_w2a8_ffn(const void* x, int dtype, int64_t M, int64_t K, i
     return status_of(launch_gemv_group_ffn(ffn, dn, QuantOut{xq, act_scale, rowsum}, Prefetch{}, F, sms, s));
   }
   auto matmul = [&](const uint8_t* wp, float a, float* o, int64_t N, int64_t Kd) -> int {
-    if (workspace && ws_need > 0)
-      return bitnet_i2s_matmul_ws(xq, act_scale, rowsum, wp, a, o, nullptr, M, N, Kd, workspace, workspace_bytes,
-                                  stream);
     return bitnet_i2s_matmul_algo(xq, act_scale, rowsum, wp, a, o, nullptr, M, N, Kd, BITNET_ALGO_AUTO, stream);
   };
   if (cudaError_t e = launch_quant_act(x, dtype, M, K, xq, act_scale, rowsum, s)) return status_of(e);

@@ -48,6 +48,7 @@
 // Every mbarrier wait is bounded; a timeout is recorded in the device error word, and the TMA
 // producer waits (bounded) for its copies in flight before it leaves.
 #include "bitnet_dev.cuh"
+#include "gemm_pair.h"
 
 #include <atomic>
 #include <cstring>

@@ -797,7 +797,8 @@ def check_ffn_block(x_np, dtype, wg, ag, wu, au, wd, ad, gamma, eps, g_gate, g_u
 FFN_CASES = [
     # (M, K, F, dtype, workspace): the two-launch path (M = 1, including a row too long for
     # the registers, F = 10240), the few-token path (more than 64 rows in chunks), the
-    # prompt-length kernel (from 128 rows), and the expand-once workspace path (from 2048 rows)
+    # prompt-length kernels (from 128 rows; the CTA-pair kernel from 192), and a call that passes
+    # a workspace (which the block no longer needs: its size is 0)
     (1, 2560, 6912, "f32", False), (1, 2560, 6912, "bf16", False), (1, 512, 10240, "f32", False),
     (1, 1024, 128, "bf16", False), (2, 2560, 6912, "bf16", False), (17, 640, 1280, "f32", False),
     (65, 2560, 6912, "bf16", False), (130, 1024, 2048, "f32", False), (512, 1024, 2048, "bf16", False),
