@@ -272,10 +272,8 @@ def auto_kernel_file(M, N, K):
     in capi.cu), for the traffic records."""
     if K > 32768 or M < (3 if K > 10240 else 5):
         return "gemv_i2s.cu"
-    if M >= 192:
+    if M >= 65:
         return "gemm_pair.cu"
-    if K <= 4096 and M >= 128:
-        return "gemm_prefill.cu"
     return "gemm_smallm.cu"
 
 

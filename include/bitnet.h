@@ -73,9 +73,8 @@ extern "C" {
 
 /* ---- matmul kernel selection (bitnet_i2s_matmul_algo) ---- */
 #define BITNET_ALGO_AUTO 0   /* GEMV for a few rows (M < 5, or M < 3 when K > 10240),
-                                the few-token kernel beyond, the one-CTA prompt-length
-                                kernel from M = 128 (K <= 4096), its CTA-pair variant
-                                from M = 192; K <= 32768                                 */
+                                the few-token kernel up to M = 64, the CTA-pair
+                                prompt-length kernel beyond; K <= 32768                  */
 #define BITNET_ALGO_GEMV 1   /* force the dp4a decode GEMV (any M)                   */
 #define BITNET_ALGO_GEMM 2   /* force the tcgen05 tensor-core GEMM (any M)           */
 #define BITNET_ALGO_SMALLM 3 /* force the few-token tensor-core kernel (any M)       */
@@ -143,15 +142,15 @@ BITNET_API int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, 
  *   packed weights. From there a few-token tcgen05 kernel decodes each weight once, as the
  *   e4m3 value code + 8, for up to 64 token rows, whose int8 values enter as three exact e4m3
  *   base-8 digits (weights as the MMA's M, K split over a thread-block cluster); more rows go
- *   in chunks of 64. From 128 rows (up to K = 4096) the prompt-length kernel takes over:
- *   TMA-staged packed weights and int8 tokens, expanded in the kernel to exact fp16 (the codes
- *   into tensor memory, the tokens into shared memory), 256 weight rows x 128 tokens per CTA,
- *   K split over a cluster when the tiles are few. From 192 rows its CTA-pair variant runs:
- *   the same expansion with the 2-SM MMA (tcgen05.mma.cta_group::2), 256 weight rows x 256
- *   tokens per pair of CTAs. Neither uses a workspace. A tcgen05 tile GEMM that expands the
- *   codes to fp16 in shared memory is available when forced (BITNET_ALGO_GEMM). The
- *   tensor-core paths are exact: every partial sum is an integer below 2^24 accumulated in
- *   fp32. All give bit-identical results.
+ *   in chunks of 64 when forced. Beyond 64 rows the prompt-length kernel takes over: TMA-staged
+ *   packed weights and int8 tokens, expanded in the kernel to exact fp16 (the codes into tensor
+ *   memory, the tokens into shared memory), with the 2-SM MMA (tcgen05.mma.cta_group::2): 256
+ *   weight rows x 128 tokens (up to 128 rows) or x 256 tokens per pair of CTAs, K split over a
+ *   cluster when the tiles are few. A one-CTA variant (256 weight rows x 128 tokens per CTA)
+ *   is available when forced (BITNET_ALGO_PREFILL). Neither uses a workspace. A tcgen05 tile
+ *   GEMM that expands the codes to fp16 in shared memory is available when forced
+ *   (BITNET_ALGO_GEMM). The tensor-core paths are exact: every partial sum is an integer below
+ *   2^24 accumulated in fp32. All give bit-identical results.
  */
 BITNET_API int bitnet_i2s_matmul(const int8_t *xq, const float *act_scale, const int32_t *rowsum,
                                  const uint8_t *wp, float w_scale, float *out, int32_t *acc_out,

@@ -31,14 +31,13 @@ constexpr int64_t kMaxKTensorCore = 1 << 15; // exact fp32 accumulation bound of
 // the plain GEMV takes over and loses from 3 rows (8192 x 28672: 48.4 against 39.5 us).
 constexpr int64_t kSmallmMinM = 5;           // K <= 10240
 constexpr int64_t kSmallmMinMLongK = 3;      // K > 10240
-// auto dispatch: the prompt-length kernels. Measured per call, µs (N x K = 6912 x 2560 / 2560 x
-// 6912; few-token chunks, one-CTA kernel, CTA-pair kernel): M = 128: 14.5 / 15.1, 14.1 / 16.7,
-// 15.9 / 16.9; M = 192: 28.0 / 18.7, 19.1 / 18.6, 15.9 / 17.2; M = 256: 28.6 / 28.8, 19.1 / 18.7,
-// 16.0 / 17.3; M = 512: 43.2 / 56.3, 25.2 / 25.8, 21.1 / 21.7; M = 4096: 329 / 256, 151 / 164,
-// 127 / 130. So the pair kernel from 192 rows, the one-CTA kernel from 128 rows up to K = 4096,
-// and the few-token chunks below.
-constexpr int64_t kPrefillMinM = 128;         // the one-CTA kernel, K <= 4096
-constexpr int64_t kPairMinM = 192;            // the CTA-pair kernel
+// auto dispatch: the CTA-pair prompt-length kernel beyond one 64-token chunk of the few-token
+// kernel. Measured per call, us (N x K = 6912 x 2560 / 2560 x 6912; few-token chunks, one-CTA
+// prompt-length kernel, CTA-pair kernel): M = 64: 11.1 / 12.0, 13.6 / 16.4, 12.7 / 13.6;
+// M = 96: 14.3 / 14.9, 13.7 / 16.5, 12.7 / 13.6; M = 128: 14.5 / 15.0, 14.0 / 16.7, 12.8 / 13.7;
+// M = 192: 27.9 / 18.7, 19.0 / 18.7, 15.9 / 17.2; M = 512: 43.2 / 56.3, 25.2 / 25.8, 21.1 / 21.7;
+// M = 4096: 329 / 256, 151 / 164, 127 / 130. The one-CTA kernel stays available when forced.
+constexpr int64_t kPairMinM = 65;
 
 // per-device: 0 = unchecked, 1 = sm_103 ok, -1 = unsupported; and SM count
 std::atomic<int> g_dev_state[kMaxDevices];
@@ -141,17 +140,14 @@ BITNET_API int bitnet_i2s_matmul_algo(const int8_t* xq, const float* act_scale, 
   if (algo == BITNET_ALGO_AUTO) {
     // dp4a GEMV for a few tokens (it decodes each weight word once per token row, cheap while
     // the rows are few); from 5 rows (3 past K = 10240) the few-token tensor-core kernel, which
-    // decodes each weight once for up to 64 rows and takes more rows in chunks of 64; from 128
-    // rows up to K = 4096 the one-CTA prompt-length kernel (256 weight rows x 128 tokens per
-    // CTA); from 192 rows the CTA-pair kernel (256 x 256 per pair). The in-kernel-expansion tile
-    // GEMM stays available when forced.
+    // decodes each weight once for up to 64 rows; beyond 64 rows the CTA-pair prompt-length
+    // kernel (256 weight rows x 128 or 256 tokens per pair of CTAs). The one-CTA prompt-length
+    // kernel and the in-kernel-expansion tile GEMM stay available when forced.
     const int64_t smallm_from = K > 10240 ? kSmallmMinMLongK : kSmallmMinM;
     if (K > kMaxKTensorCore || M < smallm_from)
       algo = BITNET_ALGO_GEMV;
     else if (M >= kPairMinM && gemm_pair_supported(M, N, K))
       algo = BITNET_ALGO_PREFILL_PAIR;
-    else if (K <= 4096 && M >= kPrefillMinM && gemm_prefill_supported(M, N, K))
-      algo = BITNET_ALGO_PREFILL;
     else
       algo = BITNET_ALGO_SMALLM;
   }

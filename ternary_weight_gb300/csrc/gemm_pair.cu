@@ -57,32 +57,42 @@ namespace bitnet {
 namespace {
 
 constexpr int PR = 128;                  // weight rows per CTA (half of the pair's M)
-constexpr int PT = 256;                  // tokens per pair tile (the MMA's N)
-constexpr int HT = 128;                  // tokens of B staged and converted by each CTA
 constexpr int CONV_WARPS = 16;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
 constexpr int THREADS = CONV_THREADS + 64;
-constexpr int NSS = 4;                   // staging slots (one 128-k block each)
 constexpr int NAB = 8;                   // A/B stages (64 k each)
 constexpr int STG_W = PR * 32;           // packed weights of one block: 128 rows x 32 bytes
-constexpr int STG_X = HT * 128;          // int8 tokens of one block: [half][128 rows][64 bytes]
-constexpr int STG_BYTES = STG_W + STG_X;
-constexpr int B_STAGE = HT * 128;        // fp16 B of one stage: 128 tokens x 64 k x 2 bytes
-constexpr int SMEM = 1024 + NAB * B_STAGE + NSS * STG_BYTES;
-constexpr int OUT_STAGE = PT * PR * 4;   // token-major fp32 tile of the epilogue (reuses the rings)
-constexpr uint32_t TMEM_COLS = 512;      // accumulator (256) + 8 A stages x 32
-constexpr int ACC_COLS = PT;
+constexpr uint32_t TMEM_COLS = 512;      // accumulator (up to 256) + 8 A stages x 32
 constexpr int A_STAGE_COLS = 32;         // 128 rows x 64 k fp16
 constexpr int kMaxSplit = 8;             // k-slices: a cluster of at most 16 CTAs
 constexpr int kStoreRows = 32;           // tokens per TMA store (no split)
 constexpr int BAR_ALL = 1;               // named barrier of the whole CTA
 constexpr int BAR_TQ = 2;                // named barriers 2..5: the 4 warps of one token quarter
-constexpr uint32_t IDESC = make_idesc_f16_f32(256, PT);
-// split K: slice r of cs owns tokens [tok_lo(r), tok_lo(r + 1)) of the pair tile, in groups of 8
-__host__ __device__ constexpr int tok_lo(int r, int cs) { return 8 * (32 * r / cs); }
-static_assert(ACC_COLS + NAB * A_STAGE_COLS <= (int)TMEM_COLS, "tensor memory columns");
-static_assert(SMEM <= 227 * 1024 - 8192, "shared memory (static part included)");
-static_assert(OUT_STAGE <= NAB * B_STAGE + NSS * STG_BYTES, "the epilogue tile fits the reused rings");
+
+constexpr int NSS = 4;                   // staging slots (one 128-k block each); 6 or 8 measured no
+                                         // faster with the 128-token tile, nor 6 with the 256-token one
+// The token tile: HT tokens of B per CTA, PT = 2 HT per pair (the MMA's N): 256 for long prompts,
+// 128 for prompts of about a hundred tokens (the 256-token tile would be half empty there).
+template <int HT_>
+struct PairTile {
+  static constexpr int HT = HT_;
+  static constexpr int PT = 2 * HT;
+  static constexpr int XV = HT / 64;               // 16-byte token pieces per converter thread and stage
+  static constexpr int STG_X = HT * 128;           // int8 tokens of one block: [half][HT rows][64 bytes]
+  static constexpr int STG_BYTES = STG_W + STG_X;
+  static constexpr int B_STAGE = HT * 128;         // fp16 B of one stage: HT tokens x 64 k x 2 bytes
+  static constexpr int SMEM = 1024 + NAB * B_STAGE + NSS * STG_BYTES;
+  static constexpr int OUT_STAGE = PT * PR * 4;    // token-major fp32 tile of the epilogue (reuses the rings)
+  static constexpr int ACC_COLS = PT;
+  static constexpr int TCH = PT / 128;             // 32-token chunks per epilogue warp
+  static constexpr uint32_t IDESC = make_idesc_f16_f32(256, PT);
+  // split K: slice r of cs owns tokens [tok_lo(r), tok_lo(r + 1)) of the pair tile, in groups of 8
+  static __host__ __device__ constexpr int tok_lo(int r, int cs) { return 8 * ((PT / 8) * r / cs); }
+  static_assert(HT == 64 || HT == 128, "token tile");
+  static_assert(ACC_COLS + NAB * A_STAGE_COLS <= (int)TMEM_COLS, "tensor memory columns");
+  static_assert(SMEM <= 227 * 1024 - 8192, "shared memory (static part included)");
+  static_assert(OUT_STAGE <= NAB * B_STAGE + NSS * STG_BYTES, "the epilogue tile fits the reused rings");
+};
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
@@ -142,13 +152,13 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 // D (both CTAs' tensor memory, 128 lanes each) (+)= A (both CTAs' tensor memory at a_tmem) * B^T
 // (the descriptor's tile in both CTAs' shared memory: N / 2 rows each)
 __device__ __forceinline__ void mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
-                                            uint32_t accumulate) {
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "mov.b64 bd, {%2, %3};\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], bd, %5, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(accumulate), "r"(IDESC)
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(accumulate), "r"(idesc)
       : "memory");
 }
 // one arrival on the barrier at this offset in every CTA of cta_mask once the MMAs issued so far
@@ -264,6 +274,7 @@ __device__ __forceinline__ uint64_t finish_fast2(uint64_t d2, uint64_t ns2, uint
   return div_scale2(fma2(d2, 0x4B8000004B800000ull, z2), ns2, y2, ws2);  // 2^24 in both lanes
 }
 
+template <int HT_>
 __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                const __grid_constant__ CUtensorMap tmX,
                                                                const __grid_constant__ CUtensorMap tmO,
@@ -271,6 +282,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
                                                                const int32_t* __restrict__ rowsum, float w_scale,
                                                                float* __restrict__ out, int32_t* __restrict__ acc_out,
                                                                int M, int N, int K, int tma_store) {
+  using T = PairTile<HT_>;
+  constexpr int HT = T::HT, PT = T::PT, XV = T::XV, STG_X = T::STG_X, STG_BYTES = T::STG_BYTES;
+  constexpr int B_STAGE = T::B_STAGE, ACC_COLS = T::ACC_COLS, TCH = T::TCH;
+  constexpr uint32_t IDESC = T::IDESC;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_stg[NSS];   // a block's bytes have landed (TMA transaction bytes)
   __shared__ __align__(8) uint64_t empty_stg[NSS];  // both groups are done with a staged block
@@ -369,10 +384,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       auto stage = [&](int s, uint32_t acc_first) {
         const uint32_t a = acol0 + (uint32_t)(s * A_STAGE_COLS);
         const uint32_t bl = blo0 + (uint32_t)((s * B_STAGE) >> 4);
-        mma_pair_ts(tmem, a, bl, bhi, acc_first);
-        mma_pair_ts(tmem, a + 8, bl + 2, bhi, 1u);
-        mma_pair_ts(tmem, a + 16, bl + 4, bhi, 1u);
-        mma_pair_ts(tmem, a + 24, bl + 6, bhi, 1u);
+        mma_pair_ts(tmem, a, bl, bhi, IDESC, acc_first);
+        mma_pair_ts(tmem, a + 8, bl + 2, bhi, IDESC, 1u);
+        mma_pair_ts(tmem, a + 16, bl + 4, bhi, IDESC, 1u);
+        mma_pair_ts(tmem, a + 24, bl + 6, bhi, IDESC, 1u);
         mma_commit_pair(&empty_ab[s], pair_mask);
       };
       int i = 0;
@@ -394,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     const int grp = cw >> 3, gw = cw & 7;
     const int quarter = warp & 3, jj = gw >> 2;  // tensor-memory lane quarter; bit pair 2h + jj
     const int row = 32 * quarter + lane;         // this thread's weight row (of the CTA's 128)
-    const int gt = gw * 32 + lane;               // token pieces gt and gt + 256 of the stage
+    const int gt = gw * 32 + lane;               // token pieces gt (and gt + 256) of the stage
     const uint32_t a_lane = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ACC_COLS + 16 * jj);
     const uint32_t full_remote = map_to_rank(smem_u32(&full_ab[0]), lead);
     for (int b = 0; b < nblk; ++b) {
@@ -405,9 +420,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       const uint4 va = lds_v4(sb + row * 32 + 16 * c0), vb = lds_v4(sb + row * 32 + 16 * (c0 ^ 1u));
       const uint4 v0 = c0 ? vb : va, v1 = c0 ? va : vb;
       const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      uint4 xv[2];
+      uint4 xv[XV];
 #pragma unroll
-      for (int v = 0; v < 2; ++v) {
+      for (int v = 0; v < XV; ++v) {
         const int p = gt + 256 * v;
         xv[v] = lds_v4(sb + STG_W + grp * (STG_X / 2) + (p >> 2) * 64 + 16 * (p & 3));
       }
@@ -425,7 +440,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       }
       const uint32_t bt = bring + (uint32_t)(s * B_STAGE);
 #pragma unroll
-      for (int v = 0; v < 2; ++v) {  // B: 16 int8 -> 32 bytes of fp16 = chunks 2c, 2c + 1 of the token's row
+      for (int v = 0; v < XV; ++v) {  // B: 16 int8 -> 32 bytes of fp16 = chunks 2c, 2c + 1 of the token's row
         const int p = gt + 256 * v, t = p >> 2, c = p & 3;
         uint32_t f[8];
         s8x4_f16_perm(xv[v].x, f[0], f[1]);
@@ -476,7 +491,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   __syncthreads();  // tok[] written; every MMA read of the rings done
 
   // Epilogue roles: converter warp (lane quarter, token quarter tq): its 32 accumulator rows and
-  // tokens [64 tq, 64 tq + 64) of the pair tile.
+  // tokens [PT/4 tq, PT/4 (tq + 1)) of the pair tile, in TCH chunks of 32.
   const int cw = warp - 2, quarter = warp & 3, tq = (cw >> 2) & 3;
   const int row = 32 * quarter + lane;
   const int n = n0 + row;
@@ -486,8 +501,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   if (cs == 1) {
     if (conv) {
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const int cb = 64 * tq + 32 * cc;
+      for (int cc = 0; cc < TCH; ++cc) {
+        const int cb = (PT / 4) * tq + 32 * cc;
         if (have) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tacc + (uint32_t)cb, v);
@@ -551,8 +566,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     // finishes them in place and stores them.
     if (conv && have) {
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const int cb = 64 * tq + 32 * cc;
+      for (int cc = 0; cc < TCH; ++cc) {
+        const int cb = (PT / 4) * tq + 32 * cc;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tacc + (uint32_t)cb, v);
         tmem_ld_wait();
@@ -561,7 +576,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
           sts32i(ostage + (uint32_t)(((cb + e) * PR + row) * 4), __float2int_rn(__uint_as_float(v[e]) * 16777216.0f));
       }
     }
-    const int t_lo = tok_lo(slice, cs), t_hi = tok_lo(slice + 1, cs);
+    const int t_lo = T::tok_lo(slice, cs), t_hi = T::tok_lo(slice + 1, cs);
     const int ct = cw * 32 + lane;
     cluster_arrive_release();
     cluster_wait_acquire();  // every CTA's partials are staged
@@ -641,30 +656,29 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* b
 
 }  // namespace
 
-bool gemm_pair_supported(int64_t M, int64_t N, int64_t K) {
-  return M >= 1 && N >= 1 && K >= 128 && K % 128 == 0 && K <= 32768 && (M + PT - 1) / PT <= 65535 &&
-         2 * ((N + 2 * PR - 1) / (2 * PR)) <= 0x7fffffff;
-}
+namespace {
 
-cudaError_t launch_gemm_pair(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
-                             float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int num_sms,
-                             cudaStream_t stream) {
+template <int HT>
+cudaError_t launch_pair(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
+                        float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int num_sms,
+                        cudaStream_t stream) {
+  using T = PairTile<HT>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    e = cudaFuncSetAttribute(gemm_pair_kernel<HT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(gemm_pair_kernel<HT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  // One CTA per SM. Pair tiles = (N / 256) x (M / 256); when their CTAs leave SMs idle, the blocks
+  // One CTA per SM. Pair tiles = (N / 256) x (M / PT); when their CTAs leave SMs idle, the blocks
   // of K are split over cs slices (a cluster of 2 x cs CTAs, cs <= 8, at least one block each),
   // as many as let every CTA run at once (the occupancy query).
-  const int64_t n_w = (N + 2 * PR - 1) / (2 * PR), n_t = (M + PT - 1) / PT, tiles = n_w * n_t;
+  const int64_t n_w = (N + 2 * PR - 1) / (2 * PR), n_t = (M + T::PT - 1) / T::PT, tiles = n_w * n_t;
   const int64_t nblk = K / 128;
   int64_t cs = num_sms / (2 * tiles);
   if (cs > kMaxSplit) cs = kMaxSplit;
@@ -672,7 +686,7 @@ cudaError_t launch_gemm_pair(const int8_t* xq, const float* act_scale, const int
   if (cs < 1) cs = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM;
+  cfg.dynamicSmemBytes = T::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -684,7 +698,7 @@ cudaError_t launch_gemm_pair(const int8_t* xq, const float* act_scale, const int
     attr[0].val.clusterDim.y = (unsigned)cs;
     cfg.gridDim = dim3((unsigned)(2 * n_w), (unsigned)cs, (unsigned)n_t);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_pair_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_pair_kernel<HT>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();  // the query is only a hint; keep shrinking to the portable size
       if (2 * cs <= 8) break;
       continue;
@@ -705,8 +719,25 @@ cudaError_t launch_gemm_pair(const int8_t* xq, const float* act_scale, const int
   std::memset(&mO, 0, sizeof(mO));
   if (tma_store && !make_map(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out, M, N, PR, cs == 1 ? kStoreRows : 8))
     return cudaErrorInvalidValue;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, mW, mX, mO, act_scale, rowsum, w_scale, out, acc_out, (int)M,
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<HT>, mW, mX, mO, act_scale, rowsum, w_scale, out, acc_out, (int)M,
                             (int)N, (int)K, tma_store ? 1 : 0);
+}
+
+}  // namespace
+
+bool gemm_pair_supported(int64_t M, int64_t N, int64_t K) {
+  return M >= 1 && N >= 1 && K >= 128 && K % 128 == 0 && K <= 32768 && (M + 127) / 128 <= 65535 &&
+         2 * ((N + 2 * PR - 1) / (2 * PR)) <= 0x7fffffff;
+}
+
+// The 128-token tile (64 per CTA) up to 128 rows, where the 256-token tile would be at least half
+// empty; the 256-token tile beyond.
+cudaError_t launch_gemm_pair(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
+                             float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int num_sms,
+                             cudaStream_t stream) {
+  if (M <= 128)
+    return launch_pair<64>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, num_sms, stream);
+  return launch_pair<128>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, num_sms, stream);
 }
 
 cudaError_t read_clear_device_error_pair(int* value) {
