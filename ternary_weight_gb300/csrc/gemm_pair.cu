@@ -731,12 +731,27 @@ bool gemm_pair_supported(int64_t M, int64_t N, int64_t K) {
 }
 
 // The 128-token tile (64 per CTA) up to 128 rows, where the 256-token tile would be at least half
-// empty; the 256-token tile beyond.
+// empty; the 256-token tile beyond. When the pair tiles fill some whole waves (one pair per two
+// SMs) and leave a partial one, the token rows of that last wave go to a second launch that
+// splits K over up to 8 slices, so that the tail takes a fraction of a round instead of a whole
+// one (M = 4096, N = 2560: 160 tiles on 76 pairs, 3 rounds for 2.1 rounds of work).
 cudaError_t launch_gemm_pair(const int8_t* xq, const float* act_scale, const int32_t* rowsum, const uint8_t* wp,
                              float w_scale, float* out, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int num_sms,
                              cudaStream_t stream) {
   if (M <= 128)
     return launch_pair<64>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, num_sms, stream);
+  constexpr int64_t PT = PairTile<128>::PT;
+  const int64_t n_w = (N + 2 * PR - 1) / (2 * PR), n_t = (M + PT - 1) / PT;
+  const int64_t wave = num_sms / 2, rounds = n_w * n_t / (wave > 0 ? wave : 1);
+  const int64_t n_t_main = rounds * wave / n_w;               // token rows filling whole waves
+  const int64_t tail_tiles = (n_t - n_t_main) * n_w;
+  if (rounds >= 1 && n_t_main >= 1 && n_t_main < n_t && wave / tail_tiles >= 2) {
+    const int64_t m_main = n_t_main * PT;
+    cudaError_t e = launch_pair<128>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, m_main, N, K, num_sms, stream);
+    if (e != cudaSuccess) return e;
+    return launch_pair<128>(xq + m_main * K, act_scale + m_main, rowsum + m_main, wp, w_scale, out + m_main * N,
+                            acc_out ? acc_out + m_main * N : nullptr, M - m_main, N, K, num_sms, stream);
+  }
   return launch_pair<128>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, num_sms, stream);
 }
 
