@@ -277,6 +277,19 @@ def auto_kernel_file(M, N, K):
     return "gemm_smallm.cu"
 
 
+def plain_call_launches(M, N, K, num_sms):
+    """Kernel launches of one bitnet_i2s_matmul call: 1, or 2 when the CTA-pair kernel runs the
+    partial last wave of its 256 x 256 tiles as a second, split-K launch (the rule in
+    gemm_pair.cu)."""
+    if auto_kernel_file(M, N, K) != "gemm_pair.cu" or M <= 128:
+        return 1
+    n_w, n_t, wave = (N + 255) // 256, (M + 255) // 256, num_sms // 2
+    rounds = n_w * n_t // max(wave, 1)
+    n_t_main = rounds * wave // n_w
+    tail = (n_t - n_t_main) * n_w
+    return 2 if rounds >= 1 and 1 <= n_t_main < n_t and wave // tail >= 2 else 1
+
+
 def recorded_traffic(kernel_file, match=None):
     """DRAM bytes per launch of a kernel from a committed ncu summary, valid only while the
     kernel source and the headers it includes are unchanged (profiles/traffic.txt: file,
@@ -496,7 +509,8 @@ def matmul_leg(name, M, N, K, act_dtype, device, peaks, seed, path="auto", reps=
     t_mm, t_step = times["mm"], times["step"]
     ops = 2.0 * M * N * K
     byts = N * K // 4 + M * K + 8 * M + 4 * M * N
-    per_mm = 3 if path == "ws" else 1
+    per_mm = 3 if path == "ws" else plain_call_launches(
+        M, N, K, torch.cuda.get_device_properties(device).multi_processor_count)
     per_step = per_mm + (0 if (M == 1 and path != "ws") else 1)
     leg = {"workload": name, "M": M, "N": N, "K": K, "path": path, "us_per_call": t_mm * 1e6,
            "gpu_launches_timed": repeats * calls * (per_mm + per_step),
