@@ -213,13 +213,16 @@ def test_chain_parity_gemm(M, N, K, dtype):
 # The prompt-length kernels, forced: M = 1 and M below one 128-token tile, ragged token tiles
 # (129, 300), ragged weight tiles (N not a multiple of 256, N < 128), one 128-k block, K splits over
 # clusters of every size the launch picks (1 to 16 CTAs: few tiles and long K), several token
-# tiles with splits, the 2B-4T prefill shapes, and (2200 rows over 2560) pair tiles that fill one
-# whole wave and leave a ragged tail, which the CTA-pair kernel runs as a second, split-K launch.
+# tiles with splits, the 2B-4T prefill shapes, (2200 rows over 2560) pair tiles that fill one
+# whole wave and leave a ragged tail, which the CTA-pair kernel runs as a second, split-K launch,
+# both sides of the pair kernel's token-tile switch (128 / 129 rows) with one 128-k block, and the
+# longest K (32768) with a ragged pair tile.
 PREFILL_CHAIN = [
     (1, 256, 128, "f32"), (5, 77, 2560, "bf16"), (64, 300, 384, "f32"), (127, 257, 1024, "bf16"),
     (128, 6912, 2560, "bf16"), (128, 2560, 6912, "bf16"), (129, 513, 1024, "f32"), (200, 1000, 6912, "bf16"),
     (300, 700, 2560, "bf16"), (256, 640, 8192, "bf16"), (512, 6912, 2560, "bf16"), (130, 100, 32768, "bf16"),
     (640, 2560, 1152, "f32"), (1000, 129, 256, "bf16"), (2200, 2560, 256, "f32"),
+    (128, 257, 128, "bf16"), (129, 256, 128, "f32"), (65, 6912, 256, "bf16"), (300, 300, 32768, "bf16"),
 ]
 
 
