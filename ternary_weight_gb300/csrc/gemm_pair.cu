@@ -1,7 +1,8 @@
-// gemm_pair.cu -- the W2A8 ternary matmul for long prompts on CTA pairs: the prompt-length kernel's
-// in-kernel expansion (packed weights and int8 tokens staged by TMA, expanded to exact fp16) with
-// the 2-SM MMA, tcgen05.mma.cta_group::2.kind::f16, M = 256 weight rows over the pair, N = 256
-// tokens, K = 16. No workspace.
+// gemm_pair.cu -- the W2A8 ternary matmul for prompts (beyond 64 tokens) on CTA pairs: the
+// prompt-length kernel's in-kernel expansion (packed weights and int8 tokens staged by TMA,
+// expanded to exact fp16) with the 2-SM MMA, tcgen05.mma.cta_group::2.kind::f16, M = 256 weight
+// rows over the pair, N = PT = 2 HT tokens (HT = 128, or 64 for prompts up to 128 tokens),
+// K = 16. No workspace.
 //
 // Computes, like every other path of the library, raw[m][n] = sum_k code[n][k] * xq[m][k],
 // acc = raw - rowsum[m], out = (acc / s[m]) * w_scale, with the same integers and the same fp32
@@ -14,37 +15,39 @@
 // is set by the latency of the operand ring's cycle: the converter warps of a stage wait for the
 // MMAs that last read its slot, and tensor memory holds only 4 slots of A next to the 2 x 128
 // accumulator columns. Here the pair's M = 256 puts 128 weight rows in each SM: per 64-k stage and
-// SM the converters expand half the weights (128 rows) and the same 128 tokens as before, the
-// accumulator is 128 rows x 256 tokens (256 columns, the same flops per SM), A takes 32 columns a
-// stage, so 8 slots fit, and one MMA instruction covers what took four.
+// SM the converters expand half the weights (128 rows) and HT tokens, the accumulator is 128 rows
+// x PT tokens (256 columns at HT = 128: the same flops per SM as the one-CTA kernel), A takes 32
+// columns a stage, so 8 slots fit, and one MMA instruction covers what took four.
 //
 // Operands and K order are those of the one-CTA kernel:
 //  * A (weights): the code c as the fp16 subnormal c * 2^-24, written with tcgen05.st into this
 //    CTA's tensor memory; the MMA reads A from both CTAs' tensor memory at the same address;
 //  * B (tokens): 0x6400 | (x + 128) minus 1152 = x as an exact fp16, into a 128-byte-swizzled
 //    K-major tile in shared memory. The pair's B is split by N: CTA 0 of the pair holds tokens
-//    0..127 of the tile, CTA 1 tokens 128..255, at the same shared-memory offset;
+//    0..HT-1 of the tile, CTA 1 tokens HT..PT-1, at the same shared-memory offset;
 //  * every partial sum is a multiple of 2^-24 below 1 in magnitude (K <= 32768): exact in fp32.
 // Stage position p holds k = 4 (p / 4) + sigma(p % 4), sigma = (0, 2, 1, 3), in A and B alike.
 //
 // Roles per CTA (576 threads):
-//  * warp 0, one lane: 2-D TMA of this CTA's 128 weight rows x 32 bytes and 128 tokens x 2 x 64
+//  * warp 0, one lane: 2-D TMA of this CTA's 128 weight rows x 32 bytes and HT tokens x 2 x 64
 //    bytes per 128-k block into 4 staging slots (the weights of the first slots before the
 //    dependency wait);
 //  * warps 2-17: two groups of 8 converter warps on alternate 64-k stages; in a group, warp
 //    (lane quarter q, half jj) writes bit pair 2h + jj of its 32 rows as 16 A columns, and every
-//    thread converts two 16-byte token pieces into B. One arrival per warp on the stage's full
+//    thread converts HT / 64 16-byte token pieces into B. One arrival per warp on the stage's full
 //    barrier, which lives in the pair's even CTA (the odd CTA's warps arrive remotely);
 //  * warp 1 of the even CTA, one lane: waits for both CTAs' operands,
 //    issues the stage's 4 MMAs and one commit multicast to both CTAs' empty barriers; a last
 //    commit multicasts the completion of every MMA;
-//  * epilogue: each CTA reads its 128 rows x 256 tokens from its own tensor memory and finishes
+//  * epilogue: each CTA reads its 128 rows x PT tokens from its own tensor memory and finishes
 //    them as the one-CTA kernel does (Markstein's division, two values per instruction, TMA
 //    bulk stores of token-major staged rows).
 // Split K: when the pair tiles leave SMs idle, cs k-slices run as a cluster of 2 x cs CTAs (rank =
 // pair position + 2 x slice); each CTA stages its int32 partials and the slice r owner of tokens
-// [8 floor(32 r / cs), 8 floor(32 (r + 1) / cs)) pulls them from the same pair position of every
-// slice with 16-byte distributed-shared-memory loads.
+// [8 floor((PT / 8) r / cs), 8 floor((PT / 8) (r + 1) / cs)) pulls them from the same pair
+// position of every slice with 16-byte distributed-shared-memory loads. When the pair tiles fill
+// whole waves and leave a partial one, the host runs the partial wave's token rows as a second,
+// split-K launch.
 // Every mbarrier wait is bounded; a timeout is recorded in the device error word, and the TMA
 // producer waits (bounded) for its copies in flight before it leaves.
 #include "bitnet_dev.cuh"
