@@ -537,9 +537,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
             tma_store_2d(&tmO, n0, m0 + cb, ostage + (uint32_t)(cb * TWR * 4));
             bulk_commit();
           }
+          __syncwarp();  // the warp converges before the next collective tensor-memory load
         }
       }
       if (!plain && cw == 8 * half && lane == 0) bulk_wait_all();  // before the CTA may leave
+      __syncwarp();  // and before the warp reaches the teardown barrier as a whole
     }
   } else {
     // split K: every CTA stages its exact partials as int32, token-major; after a cluster barrier
@@ -612,6 +614,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_prefill_kernel(const __grid_c
         bulk_commit();
         bulk_wait_all();
       }
+      __syncwarp();
     }
   }
 

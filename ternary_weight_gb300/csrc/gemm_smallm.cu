@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_smallm_kernel(const int8_t* _
       }
       mma_commit(&done_bar);  // tracks every MMA this thread issued
     }
+    __syncwarp();  // the warp converges before its collective tensor-memory loads
   } else {
     // ================================ workers ================================
     // the 16 rows of ones (e4m3 1.0 = 0x38) of every B slot; they never change, and each

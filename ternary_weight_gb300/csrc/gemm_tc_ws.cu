@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_f16_ws_kernel(const __grid_co
         for (int i = it - STAGES > 0 ? it - STAGES : 0; i < it; ++i) mbar_wait(&full_bar[i % STAGES], (i / STAGES) & 1, &dummy);
       }
     }
+    __syncwarp();  // the warp reaches the teardown barrier as a whole
   } else if (warp == 1) {
     // ================================ MMA issuer ================================
     if (lane == 0) {
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_f16_ws_kernel(const __grid_co
       }
       mma_commit(&done_bar);  // tracks every MMA this thread issued
     }
+    __syncwarp();  // the warp reaches the teardown barrier and the free as a whole
   } else {
     // ================================ epilogue (warps 2-5) ================================
     // Warp q reads accumulator lanes 32q..32q+31 (rows m0 + 32q + lane) 32 columns at a time,
