@@ -456,22 +456,37 @@ cudaError_t launch_gemv_i2s(const int8_t* xq, const float* act_scale, const int3
   // below, it wins up to 4 rows (N 6912, K 2560: 4.1 against 5.1 us at M = 2; N 2560, K 6912:
   // 8.0 against 10.5 us at M = 4), and from 5 to 8 rows only at long K (15.2 against 15.8 us
   // at M = 8, K 6912; 10.8 against 9.9 us at M = 8, K 2560).
+  //
+  // With walks of 4 or 5 chunks, each lane takes two weight rows: every 16-byte activation load
+  // from shared memory then serves two rows, which halves the activation reads (at one row per
+  // lane, N 6912, K 2560, M = 4 reads ~70 MB of shared memory, ~1.8 us of its bandwidth). The
+  // occupancy that suits it follows the lane layout (us, bit-identical):
+  //  * 32 lanes per row (K 6912): two CTAs per SM; M = 4 8.0 -> 7.5, M = 2 5.25 -> 5.0;
+  //  * fewer lanes per row, several row groups per warp (K 2560): one CTA per SM for 3-4 rows
+  //    (6.2 -> 5.8 at M = 4, 5.9 -> 5.5 at M = 3; two CTAs per SM were slower, 7.3); 2 rows keep
+  //    one row per lane (4.2 against 4.8).
   if (M >= 2 && K <= kMaxM1K && (M <= 4 || (M <= 8 && K >= 4096))) {
     const int T = (C + (1 << log2G) - 1) >> log2G;
-#define BITNET_MT(MT_, TB_)                                                                               \
-  launch_m1<MT_, 1, TB_, (MT_ >= 8 ? 1 : 2)>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, log2G, \
-                                             num_sms, stream)
-#define BITNET_MT_T(MT_)              \
-  switch (T) {                         \
-    case 1: return BITNET_MT(MT_, 1);  \
-    case 2: return BITNET_MT(MT_, 2);  \
-    case 3: return BITNET_MT(MT_, 3);  \
-    case 4: return BITNET_MT(MT_, 4);  \
-    default: return BITNET_MT(MT_, 5); \
+    const bool wide = log2G == 5;  // 32 lanes per row
+#define BITNET_MT(MT_, R_, TB_, LB_) \
+  launch_m1<MT_, R_, TB_, LB_>(xq, act_scale, rowsum, wp, w_scale, out, acc_out, M, N, K, log2G, num_sms, stream)
+#define BITNET_MT_T(MT_, LB_)                                       \
+  switch (T) {                                                       \
+    case 1: return BITNET_MT(MT_, 1, 1, LB_);                        \
+    case 2: return BITNET_MT(MT_, 1, 2, LB_);                        \
+    case 3: return BITNET_MT(MT_, 1, 3, LB_);                        \
+    case 4: return BITNET_MT(MT_, 1, 4, LB_);                        \
+    default: return BITNET_MT(MT_, 1, 5, LB_);                       \
   }
-    if (M <= 2) BITNET_MT_T(2)
-    if (M <= 4) BITNET_MT_T(4)
-    BITNET_MT_T(8)
+    if (M <= 4 && T >= 4 && (wide || M > 2)) {
+      const int lb = wide ? 2 : 1;
+      if (M <= 2) return T == 4 ? BITNET_MT(2, 2, 4, 2) : BITNET_MT(2, 2, 5, 2);
+      if (lb == 2) return T == 4 ? BITNET_MT(4, 2, 4, 2) : BITNET_MT(4, 2, 5, 2);
+      return T == 4 ? BITNET_MT(4, 2, 4, 1) : BITNET_MT(4, 2, 5, 1);
+    }
+    if (M <= 2) BITNET_MT_T(2, 2)
+    if (M <= 4) BITNET_MT_T(4, 2)
+    BITNET_MT_T(8, 1)
 #undef BITNET_MT_T
 #undef BITNET_MT
   }

@@ -936,6 +936,9 @@ ROWS_CASES = [
     (2, 6912, 2560), (3, 2560, 6912), (4, 640, 2560), (5, 7, 384), (5, 2560, 6912), (8, 2560, 6912),
     (9, 2560, 6912), (11, 6912, 2560), (12, 6912, 2560), (16, 2560, 6912), (16, 300, 10240),
     (13, 1000, 1152), (2, 152, 128), (16, 1, 256), (2, 300, 12288), (3, 300, 12288),
+    # two weight rows per lane (walks of 4-5 chunks): both lane layouts, ragged N (a lane's second
+    # row past the end), and a ragged 5-chunk walk (K 9216)
+    (2, 2560, 6912), (4, 6912, 2560), (4, 1001, 6912), (3, 999, 2560), (2, 300, 10240), (4, 300, 9216),
 ]
 
 
